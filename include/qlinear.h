@@ -1,0 +1,180 @@
+/*
+ * qlinear.h - C ABI of libqlinear.so: weight-only quantized linear layers over
+ * MLX-style affine weights (4, 6 or 8 bits, group 64) kept as stored, for GB300
+ * (sm_103a).
+ *
+ * Sources (TensorFold pull requests, cited by page title and section):
+ *   [P1696] PR #1696, LFM3 on Intel Iris Xe (later revision), "What it adds":
+ *           MLX 4-bit group 64 "as stored"; N-row matvecs that sum each row as the
+ *           one-row kernels do; decode fuses w1 + w3 + SwiGLU and the four attention
+ *           matvecs; "Prompt GEMM": an fma chain per 64-wide k block, blocks added
+ *           in order, so a row's sum does not depend on how the prompt is cut.
+ *   [P1514] PR #1514, LFM3-1.7B on Apple Metal, "What changes": MLX 4/6/8-bit
+ *           checkpoints; paired FFN projections keep their retained rounding
+ *           boundaries.
+ *
+ * Weight layout (the pages print none; this is the stated reading): W is [n, k],
+ * k contiguous.  Row i of `wq` is a little-endian bit stream of k*bits/32 uint32
+ * words; value j of the row is the unsigned field at bits [bits*j, bits*j + bits)
+ * (for 4 bits: nibble j%8 of word j/8, low nibble first; for 6 bits a field may
+ * straddle two words).  `scales` and `biases` are bf16 bit patterns [n, k/64];
+ * the dequantized weight is w[i][j] = scales[i][j/64] * q[i][j] + biases[i][j/64].
+ *
+ * Conventions for every call:
+ *   - every pointer is a DEVICE pointer owned by the caller; the library keeps no
+ *     reference to it after the call is enqueued;
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); every call is
+ *     asynchronous and enqueues its kernels on `stream`; nothing synchronizes
+ *     except qlinear_last_error();
+ *   - bf16 values are passed as their uint16_t bit patterns; outputs are float32
+ *     unless stated otherwise;
+ *   - activations x are row-major [rows, k] with row stride `ldx` elements;
+ *     outputs are row-major [rows, n] with row stride `ldy` elements;
+ *   - `wq` and `x` must be 16-byte aligned and `ldx` a multiple of 8;
+ *   - return value: QL_OK (0) or a negative QL_ERR_* code; arguments are checked
+ *     on the host before anything is enqueued, so an error return enqueues nothing
+ *     (except QL_ERR_LAUNCH, reported after a failed launch);
+ *   - results are deterministic: the same inputs give the same bits, and the
+ *     summation order of each output is a function of k (and bits) only.
+ *
+ * Tolerance against the float64 definition (per output):
+ *   |y - y64| <= 1e-5 * sum_j |w[i][j] * x[j]| + 1e-6.
+ */
+#ifndef QLINEAR_H
+#define QLINEAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  QL_OK = 0,
+  QL_ERR_NULL = -1,     /* a required pointer is NULL */
+  QL_ERR_SHAPE = -2,    /* n <= 0, k <= 0, k % 64 != 0, k too large, m < 0, or shapes that must match do not */
+  QL_ERR_BITS = -3,     /* bits not in {4, 6, 8}, or the fused weights differ in bits */
+  QL_ERR_GROUP = -4,    /* group != 64 */
+  QL_ERR_ROWS = -5,     /* rows outside 1..16 */
+  QL_ERR_ALIGN = -6,    /* wq/x not 16-byte aligned, ldx % 8 != 0, or a leading dimension too small */
+  QL_ERR_ARCH = -7,     /* the current device is not compute capability 10.3 (sm_103) */
+  QL_ERR_LAUNCH = -8,   /* the kernel launch failed (cudaGetLastError after launch) */
+  QL_ERR_TIMEOUT = -9,  /* a bounded device-side wait gave up (reported by qlinear_last_error) */
+  QL_ERR_CUDA = -10,    /* another CUDA runtime error (device query, tensor-map encoding) */
+  QL_ERR_NOMEM = -11    /* the library could not allocate its scratch buffer */
+};
+
+/* One quantized weight matrix, as stored.  All pointers are device pointers. */
+typedef struct ql_weight {
+  const uint32_t *wq;     /* [n, k*bits/32] packed codes, 16-byte aligned                     */
+  const uint16_t *scales; /* [n, k/64] bf16 bits                                               */
+  const uint16_t *biases; /* [n, k/64] bf16 bits                                               */
+  int32_t n;              /* output channels (rows of W), >= 1                                  */
+  int32_t k;              /* input channels, multiple of 64, <= 65536                           */
+  int32_t bits;           /* 4, 6 or 8                                                          */
+  int32_t group;          /* must be 64                                                         */
+} ql_weight;
+
+/*
+ * qlinear_mv - decode matvec, one activation row: y[i] = sum_j w[i][j] x[j].
+ * [P1696] "What it adds" (decode keeps qmv).  Exactly qlinear_mv_rows with rows = 1.
+ *   x: bf16 [k]; y: float [n].
+ */
+int qlinear_mv(const ql_weight *w, const uint16_t *x, float *y, void *stream);
+
+/*
+ * qlinear_mv_rows - N-row decode matvec for 1..16 stream rows sharing one weight
+ * pass: y[r][i] = sum_j w[i][j] x[r][j].
+ * [P1696] "What it adds": streams share a decode step through N-row matvecs that
+ * sum each row as the one-row kernels do.  Row r of the result is bit-equal to
+ * qlinear_mv on x[r] alone, for every rows in 1..16.
+ *   x: bf16 [rows, ldx] (ldx >= k); y: float [rows, ldy] (ldy >= n).
+ */
+int qlinear_mv_rows(const ql_weight *w, const uint16_t *x, int32_t rows, int64_t ldx,
+                    float *y, int64_t ldy, void *stream);
+
+/*
+ * qffn_swiglu_mv - fused FFN gate/up decode step: h[r][i] = bf16(silu(a) * c) with
+ * a = (w1 x[r])[i], c = (w3 x[r])[i], silu(t) = t / (1 + exp(-t)) in float32, rounded
+ * to bf16 (nearest even) - the retained rounding boundary before the down projection.
+ * [P1696] "What it adds" (decode fuses w1 + w3 + SwiGLU); [P1514] "What changes".
+ * One weight pass over w1 and w3.  a and c are bit-equal to qlinear_mv_rows(w1/w3)
+ * and h is bit-equal to qswiglu() applied to those.
+ *   w1, w3: same n, k, bits; x: bf16 [rows, ldx]; h: bf16 bits [rows, ldh] (ldh >= n).
+ */
+int qffn_swiglu_mv(const ql_weight *w1, const ql_weight *w3, const uint16_t *x, int32_t rows,
+                   int64_t ldx, uint16_t *h, int64_t ldh, void *stream);
+
+/*
+ * qattn_proj_mv - the four attention projections (q, k, v, gate) of one activation
+ * in ONE launch.  [P1696] "What it adds" (decode fuses the four attention matvecs).
+ * Outputs are dense row-major [rows, n_i]; each is bit-equal to qlinear_mv_rows on
+ * that weight alone.
+ *   wq, wk, wv, wg: same k and bits, any n; x: bf16 [rows, ldx].
+ */
+int qattn_proj_mv(const ql_weight *wq, const ql_weight *wk, const ql_weight *wv,
+                  const ql_weight *wg, const uint16_t *x, int32_t rows, int64_t ldx,
+                  float *q, float *k, float *v, float *g, void *stream);
+
+/*
+ * qlinear_pgemm - prompt-window GEMM: Y[m][i] = sum_j w[i][j] X[m][j] for m rows.
+ * [P1696] "What it adds" > "Prompt GEMM": each output is an fp32 chain over 64-wide
+ * k blocks added in order, so a row's result does not depend on how the prompt is
+ * cut into windows.  Here: for every block b the tensor cores form the exact-code
+ * partial P_b = sum_{j in b} q[i][j] X[m][j] (codes converted exactly to bf16,
+ * fp32 accumulation), the chain y = fma(scale_b, P_b, y) runs over b = 0..k/64-1 in
+ * order, and the bias term sum_b bias_b * S_b (S_b = sum_{j in b} X[m][j], split
+ * exactly into three bf16 parts) is added last.  Every row depends only on its own
+ * X row: row m of any window equals row m of the whole prompt, bit for bit.
+ *   X: bf16 [m, ldx] (16-byte aligned, ldx % 8 == 0); Y: float [m, ldy] (ldy >= n).
+ *   m may be 0: then nothing is checked beyond the weight and nothing is enqueued
+ *   (X and Y may be NULL).  Uses a library-owned device scratch buffer of
+ *   m * round_up(3*k/64, 64) bf16 values for the split row sums, allocated with
+ *   cudaMalloc on first need per device and grown on demand (growth synchronizes
+ *   the device); calls on one device must be ordered on one stream because they
+ *   share that buffer.
+ */
+int qlinear_pgemm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, float *Y,
+                  int64_t ldy, void *stream);
+
+/*
+ * qswiglu - h[r][i] = bf16(silu(a[r][i]) * c[r][i]) (float32 math, nearest-even
+ * rounding): the SwiGLU of qffn_swiglu_mv on its own, used as its "fusion off" control.
+ *   a, c: float [rows, lda]; h: bf16 bits [rows, ldh]; rows >= 1, n >= 1.
+ */
+int qswiglu(const float *a, const float *c, int32_t rows, int32_t n, int64_t lda,
+            uint16_t *h, int64_t ldh, void *stream);
+
+/*
+ * qlinear_last_error - synchronizes `stream`, then returns and clears the device
+ * status word: QL_OK, or QL_ERR_TIMEOUT if a bounded device-side wait gave up in a
+ * kernel enqueued since the last call.  Returns QL_ERR_CUDA if synchronization fails.
+ */
+int qlinear_last_error(void *stream);
+
+/*
+ * qlinear_set_wait_budget_ns - bound, in nanoseconds, for every device-side wait of
+ * the kernels enqueued after this call (default 2e9).  A wait that exceeds it makes
+ * the kernel record QL_ERR_TIMEOUT and return instead of spinning.  Returns the
+ * previous value.
+ */
+uint64_t qlinear_set_wait_budget_ns(uint64_t ns);
+
+/*
+ * qlinear_wait_probe - enqueues one CTA that waits on a shared-memory barrier that
+ * nothing ever completes, bounded by `budget_ns`; the kernel records QL_ERR_TIMEOUT
+ * and returns.  Exercises the timeout path of qlinear_last_error without a fault.
+ */
+int qlinear_wait_probe(uint64_t budget_ns, void *stream);
+
+/* qlinear_strerror - static description of a QL_* code. */
+const char *qlinear_strerror(int code);
+
+/* qlinear_version - (major << 16) | minor of this library. */
+int qlinear_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLINEAR_H */

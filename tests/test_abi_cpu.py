@@ -1,0 +1,104 @@
+"""Host-side checks of libqlinear.so that need no GPU: the library builds, loads,
+exports every entry point that include/qlinear.h declares, and rejects bad
+arguments before touching the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qlinear.h")
+
+
+@pytest.fixture(scope="module")
+def q():
+    from weight_only_bit_mlx_gb300 import build
+    build.build_library()
+    from weight_only_bit_mlx_gb300 import qlinear
+    return qlinear
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(q\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_five_paths():
+    names = declared_functions()
+    for f in ("qlinear_mv", "qlinear_mv_rows", "qffn_swiglu_mv", "qattn_proj_mv", "qlinear_pgemm"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(q):
+    lib = ctypes.CDLL(q.LIB_PATH)
+    out = subprocess.run(["nm", "-D", "--defined-only", q.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s+(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in exported, name
+
+
+def test_strerror_and_version(q):
+    assert q.qlinear_strerror(0) == "ok"
+    assert "wait" in q.qlinear_strerror(q.QL_ERR_TIMEOUT)
+    assert q.qlinear_strerror(12345).startswith("unknown")
+    assert q.qlinear_version() >= 1
+
+
+def _w(q, **kw):
+    d = dict(wq=0x10000, scales=0x20000, biases=0x30000, n=64, k=128, bits=4, group=64)
+    d.update(kw)
+    return q.ql_weight(d["wq"], d["scales"], d["biases"], d["n"], d["k"], d["bits"], d["group"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(wq=0), "QL_ERR_NULL"),
+    (dict(group=32), "QL_ERR_GROUP"),
+    (dict(bits=5), "QL_ERR_BITS"),
+    (dict(bits=2), "QL_ERR_BITS"),
+    (dict(k=96), "QL_ERR_SHAPE"),
+    (dict(k=0), "QL_ERR_SHAPE"),
+    (dict(n=0), "QL_ERR_SHAPE"),
+    (dict(wq=0x10004), "QL_ERR_ALIGN"),
+])
+def test_bad_weight_rejected_on_host(q, kw, code):
+    w = _w(q, **kw)
+    x, y = 0x40000, 0x50000
+    assert q.LIB.qlinear_mv_rows(ctypes.byref(w), x, 1, 128, y, 64, None) == getattr(q, code)
+    assert q.LIB.qlinear_pgemm(ctypes.byref(w), x, 8, 128, y, 64, None) == getattr(q, code)
+
+
+def test_bad_rows_and_layout_rejected_on_host(q):
+    w = _w(q)
+    L = q.LIB
+    assert L.qlinear_mv_rows(ctypes.byref(w), 0x40000, 0, 128, 0x50000, 64, None) == q.QL_ERR_ROWS
+    assert L.qlinear_mv_rows(ctypes.byref(w), 0x40000, 17, 128, 0x50000, 64, None) == q.QL_ERR_ROWS
+    assert L.qlinear_mv_rows(ctypes.byref(w), 0x40008, 2, 128, 0x50000, 64, None) == q.QL_ERR_ALIGN
+    assert L.qlinear_mv_rows(ctypes.byref(w), 0x40000, 2, 124, 0x50000, 64, None) == q.QL_ERR_ALIGN
+    assert L.qlinear_mv_rows(ctypes.byref(w), 0x40000, 2, 64, 0x50000, 64, None) == q.QL_ERR_ALIGN
+    assert L.qlinear_mv_rows(ctypes.byref(w), 0x40000, 2, 128, 0x50000, 32, None) == q.QL_ERR_ALIGN
+    assert L.qlinear_mv_rows(ctypes.byref(w), 0, 1, 128, 0x50000, 64, None) == q.QL_ERR_NULL
+    assert L.qlinear_mv_rows(ctypes.byref(w), 0x40000, 1, 128, 0, 64, None) == q.QL_ERR_NULL
+    assert L.qlinear_pgemm(ctypes.byref(w), 0x40000, -1, 128, 0x50000, 64, None) == q.QL_ERR_SHAPE
+    assert L.qlinear_pgemm(ctypes.byref(w), 0x40000, 4, 120, 0x50000, 64, None) == q.QL_ERR_ALIGN
+    w3 = _w(q, n=32)
+    assert L.qffn_swiglu_mv(ctypes.byref(w), ctypes.byref(w3), 0x40000, 1, 128, 0x50000, 64,
+                            None) == q.QL_ERR_SHAPE
+    w6 = _w(q, bits=6)
+    assert L.qffn_swiglu_mv(ctypes.byref(w), ctypes.byref(w6), 0x40000, 1, 128, 0x50000, 64,
+                            None) == q.QL_ERR_BITS
+    wk = _w(q, k=256)
+    assert L.qattn_proj_mv(ctypes.byref(w), ctypes.byref(wk), ctypes.byref(w), ctypes.byref(w), 0x40000, 1,
+                           128, 0x50000, 0x50000, 0x50000, 0x50000, None) == q.QL_ERR_SHAPE
+    assert L.qswiglu(0x40000, 0x50000, 0, 8, 8, 0x60000, 8, None) == q.QL_ERR_SHAPE
+    assert L.qswiglu(0, 0x50000, 1, 8, 8, 0x60000, 8, None) == q.QL_ERR_NULL
+
+
+def test_wait_budget_setter(q):
+    old = q.qlinear_set_wait_budget_ns(12345)
+    assert q.qlinear_set_wait_budget_ns(old) == 12345

@@ -1,0 +1,106 @@
+"""Prompt-window GEMM on the GPU: parity with the float64 oracle and bit-exact
+invariance of every row across window cuts (TensorFold PR #1696, later revision,
+"What it adds" > "Prompt GEMM": blocks added in order so a row's sum does not
+depend on how the prompt is cut; "Checks": windows of 64, 128, 256 and a ragged
+cut, every row alone equal to the row in a window)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import qlinear_oracle as orc
+from tests import _util as U
+from weight_only_bit_mlx_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    from weight_only_bit_mlx_gb300 import qlinear
+    assert torch.cuda.is_available()
+    return qlinear
+
+
+@pytest.fixture(scope="module")
+def prompt(q):
+    # prefill pgemm: X bf16 [1024, 2048] ~ N(0, 1); W 2048 -> 8192, 4-bit g64
+    w = U.weight(8192, 2048, 4, config_id=3, tensor_id=0)
+    X = synth.make_x(1024, 2048, config_id=3)
+    wd, Xd = U.dev_weight(w), U.dev_x(X)
+    Y = q.qlinear_pgemm(wd, Xd)
+    torch.cuda.synchronize()
+    return w, X, wd, Xd, Y
+
+
+def test_prompt_gemm_against_oracle(prompt):
+    w, X, wd, Xd, Y = prompt
+    y64, A = orc.pgemm(X, w)
+    U.assert_close(Y, y64, A, "pgemm 1024x2048x8192")
+
+
+@pytest.mark.parametrize("cut", [[64] * 16, [128] * 8, [256] * 4, [100, 300, 624]],
+                         ids=["w64", "w128", "w256", "ragged"])
+def test_window_cuts_bit_exact(q, prompt, cut):
+    w, X, wd, Xd, Y = prompt
+    lo = 0
+    for m in cut:
+        Yw = q.qlinear_pgemm(wd, Xd[lo:lo + m])
+        assert torch.equal(Yw, Y[lo:lo + m]), f"window [{lo}, {lo + m}) differs"
+        lo += m
+    assert lo == 1024
+
+
+def test_rows_alone_bit_exact(q, prompt):
+    w, X, wd, Xd, Y = prompt
+    for r in [0, 1, 127, 128, 129, 500, 1023]:
+        assert torch.equal(q.qlinear_pgemm(wd, Xd[r:r + 1]), Y[r:r + 1]), f"row {r}"
+
+
+@pytest.mark.parametrize("bits", [4, 6, 8])
+@pytest.mark.parametrize("m,n,k", [(77, 200, 64), (130, 1000, 192), (300, 256, 8192), (256, 512, 2048),
+                                   (1, 128, 4096)])
+def test_shapes_against_oracle(q, bits, m, n, k):
+    w = U.weight(n, k, bits, config_id=60, tensor_id=bits)
+    X = synth.make_x(m, k, config_id=60)
+    wd, Xd = U.dev_weight(w), U.dev_x(X)
+    Y = q.qlinear_pgemm(wd, Xd)
+    torch.cuda.synchronize()
+    y64, A = orc.pgemm(X, w)
+    U.assert_close(Y, y64, A, f"pgemm bits={bits} m={m} n={n} k={k}")
+    # ragged cut of the same rows
+    if m > 3:
+        cut = m // 3
+        Y2 = torch.cat([q.qlinear_pgemm(wd, Xd[:cut]), q.qlinear_pgemm(wd, Xd[cut:])])
+        assert torch.equal(Y2, Y)
+
+
+def test_strided_input_and_output(q):
+    n, k, m = 384, 1024, 200
+    w = U.dev_weight(U.weight(n, k, 4, config_id=61))
+    Xw = U.dev_x(synth.make_x(m, k + 128, config_id=61))
+    Xs = Xw[:, 128:]
+    Yref = q.qlinear_pgemm(w, Xs.contiguous())
+    Yout = torch.full((m, n + 5), float("nan"), device="cuda")
+    q.qlinear_pgemm(w, Xs, Y=Yout[:, :n])
+    assert torch.equal(Yout[:, :n], Yref)
+    assert torch.isnan(Yout[:, n:]).all()
+
+
+def test_empty_window(q):
+    w = U.dev_weight(U.weight(128, 128, 4, config_id=62))
+    Y = q.qlinear_pgemm(w, torch.empty(0, 128, dtype=torch.bfloat16, device="cuda"))
+    assert Y.shape == (0, 128)
+
+
+def test_row_independence_of_other_rows(q):
+    # changing other rows of the window must not change a row's bits
+    n, k = 256, 2048
+    w = U.dev_weight(U.weight(n, k, 4, config_id=63))
+    X = U.dev_x(synth.make_x(128, k, config_id=63))
+    Y = q.qlinear_pgemm(w, X)
+    X2 = X.clone()
+    X2[1::2] = X2[1::2] * 3.0
+    Y2 = q.qlinear_pgemm(w, X2)
+    assert torch.equal(Y[0::2], Y2[0::2])

@@ -1,0 +1,615 @@
+// pgemm.cu - prompt-window GEMM over MLX affine 4/6/8-bit group-64 weights on the
+// sm_103a tensor cores (TMA -> in-SMEM exact dequant -> tcgen05.mma -> TMEM).
+//
+// TensorFold PR #1696 (later revision), "What it adds" > "Prompt GEMM": prompt
+// windows take a GEMM that dequantizes the 4-bit weights as it loads each weight
+// tile; every output sums an fma chain per 64-wide k block and adds the blocks in
+// order, so a row's sum does not depend on how the prompt is cut.
+//
+// For output Y[m][n] with 64-wide blocks b = 0..G-1:
+//   P_b[m][n] = sum_{j in b} X[m][j] * q[n][j]      tcgen05.mma, bf16 x bf16 -> fp32
+//               (codes converted exactly to bf16 in shared memory; fresh TMEM
+//                accumulator per block, double-buffered)
+//   y = fma(scale[n][b], P_b, y)  for b = 0..G-1 in order      (epilogue registers)
+//   Y = y + sum_b bias[n][b] * S_b[m]                            (added last)
+// with S_b[m] = sum_{j in b} X[m][j] computed by a pre-pass in fp32 and split
+// exactly into three bf16 parts, so the bias term is one more small tcgen05
+// contraction (k' = 3G) instead of a second fma per element and block.
+// Every quantity of row m depends only on X[m][:] and W: the tensor core computes
+// each output from its own row and column, tiles out of range are zero-filled by
+// TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
+//
+// Warp roles (one CTA per 128 x 128 output tile, 448 threads):
+//   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block)
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 2-5   converters: packed codes -> bf16 (SWIZZLE_128B K-major), scales -> fp32
+//   warps 6-13  epilogue: TMEM -> registers, scale chain, bias add, store
+//               (two warps per TMEM lane quarter, 64 columns each)
+// Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
+// QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "pgemm.cuh"
+#include "sync.cuh"
+
+namespace qlk {
+
+namespace pg {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 64;
+constexpr int kStages = 4;   // TMA stages (X/S tile + packed W tile)
+constexpr int kBStages = 3;  // converted bf16 W tiles
+constexpr int kScStages = 4; // fp32 scale rows
+constexpr int kConvWarps = 4;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each owning half the columns
+constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kABytes = BM * BK * 2;
+constexpr int kBBytes = BN * BK * 2;
+constexpr int kTmemCols = 2 * BN;
+constexpr uint64_t kDrainBudgetNs = 2000000000ull;
+
+template <int BITS> struct Cfg {
+  static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
+  static constexpr int kWBytes = BN * kRowBytes;         // packed W tile
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffW = kOffB + kBStages * kBBytes;
+  static constexpr int kOffSc = kOffW + kStages * kWBytes;
+  static constexpr int kOffBar = kOffSc + kScStages * BN * 4;
+  // barriers: tma_full, tma_empty, b_full, b_empty, acc_full[2], acc_empty[2], sc_full, sc_empty, mma_done
+  static constexpr int kNumBars = 2 * kStages + 2 * kBStages + 4 + 2 * kScStages + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+struct Params {
+  const uint16_t *scales;
+  const uint16_t *biases;
+  float *Y;
+  int64_t ldy;
+  int M, N, G, NBB;
+  int *status;
+  uint64_t budget_ns;
+};
+
+// ---- PTX wrappers --------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_addr(dst)),
+      "l"(map), "r"(smem_addr(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major, M x N
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(void *p, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(p)), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// bits [off, off + 32) of a little-endian array of 32-bit words (off is a constant
+// after unrolling; the word after the last is never needed for the fields used)
+template <int NW>
+__device__ __forceinline__ uint32_t window32(const uint32_t (&w)[NW], int off) {
+  const int i = off >> 5, s = off & 31;
+  if (s == 0) return w[i];
+  const uint32_t hi = (i + 1 < NW) ? w[i + 1] : 0u;
+  return __funnelshift_r(w[i], hi, s);
+}
+
+// One packed row of one k block (64 codes) -> 8 chunks of 8 bf16 codes, chunk c
+// holding k = 8c .. 8c+7 in natural order.
+template <int BITS>
+__device__ __forceinline__ uint4 convert_chunk(const uint32_t (&w)[BK * BITS / 32], int c) {
+  uint4 o;
+  if constexpr (BITS == 4) {
+    const uint32_t x = w[c], x4 = x >> 4;
+    o.x = q4_pair(x, x4, 0); o.y = q4_pair(x, x4, 1); o.z = q4_pair(x, x4, 2); o.w = q4_pair(x, x4, 3);
+  } else if constexpr (BITS == 8) {
+    o.x = q8_pair(w[2 * c], 0); o.y = q8_pair(w[2 * c], 1);
+    o.z = q8_pair(w[2 * c + 1], 0); o.w = q8_pair(w[2 * c + 1], 1);
+  } else {
+    o.x = q6_pair(window32(w, 48 * c));
+    o.y = q6_pair(window32(w, 48 * c + 12));
+    o.z = q6_pair(window32(w, 48 * c + 24));
+    o.w = q6_pair(window32(w, 48 * c + 36));
+  }
+  return o;
+}
+
+// ---- the GEMM kernel -------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 1)
+    pgemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ Params p) {
+  using C = Cfg<BITS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem + C::kOffA;
+  uint8_t *sB = smem + C::kOffB;
+  uint8_t *sW = smem + C::kOffW;
+  float *sSc = reinterpret_cast<float *>(smem + C::kOffSc);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint64_t *tma_full = bars;
+  uint64_t *tma_empty = tma_full + kStages;
+  uint64_t *b_full = tma_empty + kStages;
+  uint64_t *b_empty = b_full + kBStages;
+  uint64_t *acc_full = b_empty + kBStages;
+  uint64_t *acc_empty = acc_full + 2;
+  uint64_t *sc_full = acc_empty + 2;
+  uint64_t *sc_empty = sc_full + kScStages;
+  uint64_t *mma_done = sc_empty + kScStages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int G = p.G, KB = p.G + p.NBB;
+  const uint64_t budget = p.budget_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) { mbar_init(&tma_full[i], 1); mbar_init(&tma_empty[i], 1 + kConvThreads); }
+    for (int i = 0; i < kBStages; ++i) { mbar_init(&b_full[i], kConvThreads); mbar_init(&b_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kEpiThreads); }
+    for (int i = 0; i < kScStages; ++i) { mbar_init(&sc_full[i], kConvThreads); mbar_init(&sc_empty[i], kEpiThreads); }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmS);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    record_status(p.status, kErrTimeout);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+        if (!mbar_wait_bounded(&tma_empty[s], ph ^ 1u, budget, abort_flag)) { give_up(); break; }
+        if (kb < G) {
+          mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kABytes + C::kWBytes));
+          tma_load_2d(sA + s * kABytes, &tmX, &tma_full[s], kb * BK, m0);
+          tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
+        } else {
+          mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kABytes);
+          tma_load_2d(sA + s * kABytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
+        }
+        issued = kb + 1;
+      }
+      // drain: every copy this CTA started must land before its shared memory goes away
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int uses = (issued - 1 - s) / kStages + 1;
+        (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      bool any = false;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % kStages, sb = kb % kBStages;
+        const int a = kb < G ? kb : G;
+        if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / kStages) & 1u, budget, abort_flag)) { give_up(); break; }
+        if (!mbar_wait_bounded(&b_full[sb], (uint32_t)(kb / kBStages) & 1u, budget, abort_flag)) { give_up(); break; }
+        if (kb <= G) {
+          if (!mbar_wait_bounded(&acc_empty[a & 1], ((uint32_t)(a >> 1) & 1u) ^ 1u, budget, abort_flag)) {
+            give_up();
+            break;
+          }
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)((a & 1) * BN);
+        const uint64_t ad = sw128_desc(smem_addr(sA + s * kABytes));
+        const uint64_t bd = sw128_desc(smem_addr(sB + sb * kBBytes));
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t acc = (kk > 0 || kb > G) ? 1u : 0u;
+          mma_bf16(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
+        }
+        any = true;
+        mma_commit(&tma_empty[s]);
+        mma_commit(&b_empty[sb]);
+        if (kb < G || kb == KB - 1) mma_commit(&acc_full[a & 1]);
+      }
+      if (any) {
+        mma_commit(mma_done);
+        (void)mbar_wait_bounded(mma_done, 0u, kDrainBudgetNs, nullptr);
+      }
+    }
+  } else if (warp < 2 + kConvWarps) {
+    // ------------------------------------------------------------ converters
+    const int ct = threadIdx.x - 64;  // 0..127: one row of the W tile
+    const int n = n0 + ct;
+    const bool nvalid = n < p.N;
+    const uint16_t *srow = p.scales + (size_t)(nvalid ? n : 0) * G;
+    const uint16_t *brow = p.biases + (size_t)(nvalid ? n : 0) * G;
+    uint32_t s_next = nvalid ? ldg_u16(srow) : 0u;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % kStages, sb = kb % kBStages;
+      uint32_t s_cur = s_next;
+      if (kb + 1 < G) s_next = nvalid ? ldg_u16(srow + kb + 1) : 0u;
+      if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / kStages) & 1u, budget, abort_flag)) { give_up(); break; }
+      if (!mbar_wait_bounded(&b_empty[sb], ((uint32_t)(kb / kBStages) & 1u) ^ 1u, budget, abort_flag)) {
+        give_up();
+        break;
+      }
+      uint8_t *brow_s = sB + sb * kBBytes + ct * 128;
+      const int sw = ct & 7;
+      if (kb < G) {
+        constexpr int NW = BK * BITS / 32;
+        uint32_t w[NW];
+        const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes;
+#pragma unroll
+        for (int i = 0; i < NW / 4; ++i) {
+          uint4 v = lds128(wp + 16 * i);
+          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) sts128(brow_s + ((c ^ sw) << 4), convert_chunk<BITS>(w, c));
+        const int sc = kb % kScStages;
+        if (!mbar_wait_bounded(&sc_empty[sc], ((uint32_t)(kb / kScStages) & 1u) ^ 1u, budget, abort_flag)) {
+          give_up();
+          break;
+        }
+        sSc[sc * BN + ct] = bf16_to_f32(s_cur);
+        fence_proxy_async();
+        mbar_arrive(&b_full[sb]);
+        mbar_arrive(&sc_full[sc]);
+        mbar_arrive(&tma_empty[s]);
+      } else {
+        // bias block: column t of block jb is k' = 64*jb + t of the [part][group]
+        // layout; its B value is bias[n][k' mod G] (zero past 3G)
+        const int base = (kb - G) * BK;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t h[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            int j = base + 8 * c + e;
+            uint32_t v = 0u;
+            if (nvalid && j < 3 * G) {
+              if (j >= G) j -= G;
+              if (j >= G) j -= G;
+              v = ldg_u16(brow + j);
+            }
+            h[e] = v;
+          }
+          uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+          sts128(brow_s + ((c ^ sw) << 4), o);
+        }
+        fence_proxy_async();
+        mbar_arrive(&b_full[sb]);
+        mbar_arrive(&tma_empty[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    constexpr int CW = BN / 2;  // columns owned by one thread
+    const int q = warp & 3;     // TMEM lane quarter this warp may access
+    const int half = (warp - (2 + kConvWarps)) / 4;
+    const int row = 32 * q + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(half * CW);
+    float y[CW];
+#pragma unroll
+    for (int i = 0; i < CW; ++i) y[i] = 0.0f;
+    bool ok = true;
+    for (int kb = 0; kb < G; ++kb) {
+      const int buf = kb & 1, sc = kb % kScStages;
+      bool w_ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)(kb >> 1) & 1u, budget, abort_flag) &&
+                  mbar_wait_bounded(&sc_full[sc], (uint32_t)(kb / kScStages) & 1u, budget, abort_flag);
+      if (!__all_sync(0xffffffffu, w_ok)) {
+        give_up();
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float4 *sc4 = reinterpret_cast<const float4 *>(sSc + sc * BN + half * CW);
+#pragma unroll
+      for (int j = 0; j < CW / 16; ++j) {
+        uint32_t r[16];
+        tmem_ld16(lane_base + (uint32_t)(buf * BN + 16 * j), r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 s4 = sc4[4 * j + i];
+          y[16 * j + 4 * i + 0] = __fmaf_rn(s4.x, __uint_as_float(r[4 * i + 0]), y[16 * j + 4 * i + 0]);
+          y[16 * j + 4 * i + 1] = __fmaf_rn(s4.y, __uint_as_float(r[4 * i + 1]), y[16 * j + 4 * i + 1]);
+          y[16 * j + 4 * i + 2] = __fmaf_rn(s4.z, __uint_as_float(r[4 * i + 2]), y[16 * j + 4 * i + 2]);
+          y[16 * j + 4 * i + 3] = __fmaf_rn(s4.w, __uint_as_float(r[4 * i + 3]), y[16 * j + 4 * i + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+      mbar_arrive(&sc_empty[sc]);
+    }
+    if (ok) {
+      bool w_ok = mbar_wait_bounded(&acc_full[G & 1], (uint32_t)(G >> 1) & 1u, budget, abort_flag);
+      if (!__all_sync(0xffffffffu, w_ok)) {
+        give_up();
+        ok = false;
+      }
+    }
+    if (ok) {
+      tc_fence_after();
+      const int buf = G & 1;
+#pragma unroll
+      for (int j = 0; j < CW / 16; ++j) {
+        uint32_t r[16];
+        tmem_ld16(lane_base + (uint32_t)(buf * BN + 16 * j), r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[16 * j + i] = __fadd_rn(y[16 * j + i], __uint_as_float(r[i]));
+      }
+      tc_fence_before();
+      const int m = m0 + row;
+      const int nb = n0 + half * CW;
+      if (m < p.M) {
+        float *yrow = p.Y + (size_t)m * p.ldy + nb;
+        const bool vec = (nb + CW <= p.N) && ((reinterpret_cast<uintptr_t>(yrow) & 15u) == 0);
+        if (vec) {
+#pragma unroll
+          for (int i = 0; i < CW / 4; ++i)
+            reinterpret_cast<float4 *>(yrow)[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < CW; ++i)
+            if (nb + i < p.N) yrow[i] = y[i];
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---- row sums, split exactly into three bf16 parts ------------------------------
+// S[m][b] = sum_{j in b} X[m][j] (fp32, j in increasing order); written as
+// out[m][p*G + b] = part p (p = 0: nearest bf16 of S, 1: of the remainder, 2: rest).
+__global__ void xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx, uint16_t *out, int64_t ldo) {
+  const int64_t total = (int64_t)M * G;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / G;
+    const int b = (int)(i % G);
+    const uint16_t *xr = X + m * ldx + (int64_t)b * 64;
+    float s = 0.0f;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const uint4 u = ldg_v4(xr + 8 * v);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s = __fadd_rn(s, bf16_to_f32(wv[e] & 0xFFFFu));
+        s = __fadd_rn(s, bf16_to_f32(wv[e] >> 16));
+      }
+    }
+    const uint16_t h0 = f32_to_bf16_rn(s);
+    const float r1 = __fsub_rn(s, bf16_to_f32(h0));
+    const uint16_t h1 = f32_to_bf16_rn(r1);
+    const float r2 = __fsub_rn(r1, bf16_to_f32(h1));
+    const uint16_t h2 = f32_to_bf16_rn(r2);
+    uint16_t *o = out + m * ldo + b;
+    o[0] = h0;
+    o[G] = h1;
+    o[2 * G] = h2;
+  }
+}
+
+}  // namespace pg
+
+// ---- host side -----------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+static bool make_map(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
+                     uint64_t stride_bytes, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {d0, d1};
+  cuuint64_t strides[1] = {stride_bytes};
+  cuuint32_t box[2] = {b0, b1};
+  cuuint32_t es[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Library-owned scratch for the split row sums: one growable buffer per device.
+constexpr int kMaxDev = 64;
+static std::mutex g_scratch_mu;
+static void *g_scratch[kMaxDev];
+static size_t g_scratch_bytes[kMaxDev];
+
+static void *scratch_get(size_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_bytes[dev] < bytes) {
+    if (g_scratch[dev] != nullptr) {
+      // earlier launches may still read the old buffer
+      if (cudaDeviceSynchronize() != cudaSuccess) return nullptr;
+      cudaFree(g_scratch[dev]);
+      g_scratch[dev] = nullptr;
+      g_scratch_bytes[dev] = 0;
+    }
+    size_t cap = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
+    void *p = nullptr;
+    if (cudaMalloc(&p, cap) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    g_scratch[dev] = p;
+    g_scratch_bytes[dev] = cap;
+  }
+  return g_scratch[dev];
+}
+
+template <int BITS>
+static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
+                        const uint16_t *S, int64_t lds, cudaStream_t st, int *status) {
+  using C = pg::Cfg<BITS>;
+  const int G = w->k / 64;
+  CUtensorMap tmX, tmW, tmS;
+  if (!make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)w->k, (uint64_t)m, (uint64_t)ldx * 2, pg::BK,
+                pg::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return QL_ERR_CUDA;
+  if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, w->wq, (uint64_t)w->k * BITS / 32, (uint64_t)w->n,
+                (uint64_t)w->k * BITS / 8, pg::BK * BITS / 32, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return QL_ERR_CUDA;
+  if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, (uint64_t)(3 * G), (uint64_t)m, (uint64_t)lds * 2,
+                pg::BK, pg::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return QL_ERR_CUDA;
+  static bool attr_set[kMaxDev] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDev && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(pg::pgemm_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc) !=
+        cudaSuccess)
+      return QL_ERR_LAUNCH;
+    attr_set[dev] = true;
+  }
+  pg::Params p;
+  p.scales = w->scales;
+  p.biases = w->biases;
+  p.Y = Y;
+  p.ldy = ldy;
+  p.M = m;
+  p.N = w->n;
+  p.G = G;
+  p.NBB = (int)(lds / pg::BK);
+  p.status = status;
+  p.budget_ns = wait_budget_ns();
+  dim3 grid((unsigned)((w->n + pg::BN - 1) / pg::BN), (unsigned)((m + pg::BM - 1) / pg::BM));
+  pg::pgemm_kernel<BITS><<<grid, pg::kThreads, C::kAlloc, st>>>(tmX, tmW, tmS, p);
+  if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+  return QL_OK;
+}
+
+int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy, cudaStream_t st,
+              int *status) {
+  const int G = w->k / 64;
+  const int64_t lds = ((3 * (int64_t)G + 63) / 64) * 64;  // row pitch of the split sums (elements)
+  uint16_t *S = static_cast<uint16_t *>(scratch_get((size_t)m * lds * 2));
+  if (S == nullptr) return QL_ERR_NOMEM;
+  const int64_t total = (int64_t)m * G;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 8192) blocks = 8192;
+  pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
+  if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+  switch (w->bits) {
+    case 4: return launch_pgemm<4>(w, X, m, ldx, Y, ldy, S, lds, st, status);
+    case 6: return launch_pgemm<6>(w, X, m, ldx, Y, ldy, S, lds, st, status);
+    default: return launch_pgemm<8>(w, X, m, ldx, Y, ldy, S, lds, st, status);
+  }
+}
+
+}  // namespace qlk

@@ -1,0 +1,224 @@
+"""Python binding of libqlinear.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (include/qlinear.h)
+and does nothing but check tensor placement, allocate outputs with PyTorch and pass
+device pointers and the current CUDA stream.  All arithmetic runs in the library's
+sm_103a kernels; if the library is missing this module raises on import - there is
+no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqlinear.so")
+
+QL_OK = 0
+QL_ERR_NULL = -1
+QL_ERR_SHAPE = -2
+QL_ERR_BITS = -3
+QL_ERR_GROUP = -4
+QL_ERR_ROWS = -5
+QL_ERR_ALIGN = -6
+QL_ERR_ARCH = -7
+QL_ERR_LAUNCH = -8
+QL_ERR_TIMEOUT = -9
+QL_ERR_CUDA = -10
+QL_ERR_NOMEM = -11
+
+
+class QlinearError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {code} ({qlinear_strerror(code)})")
+
+
+class ql_weight(ctypes.Structure):
+    _fields_ = [("wq", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("n", ctypes.c_int32), ("k", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("group", ctypes.c_int32)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -m weight_only_bit_mlx_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, U64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+    W = ctypes.POINTER(ql_weight)
+    sig = {
+        "qlinear_mv": (ctypes.c_int, [W, P, P, P]),
+        "qlinear_mv_rows": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
+        "qffn_swiglu_mv": (ctypes.c_int, [W, W, P, I32, I64, P, I64, P]),
+        "qattn_proj_mv": (ctypes.c_int, [W, W, W, W, P, I32, I64, P, P, P, P, P]),
+        "qlinear_pgemm": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
+        "qswiglu": (ctypes.c_int, [P, P, I32, I32, I64, P, I64, P]),
+        "qlinear_last_error": (ctypes.c_int, [P]),
+        "qlinear_set_wait_budget_ns": (U64, [U64]),
+        "qlinear_wait_probe": (ctypes.c_int, [U64, P]),
+        "qlinear_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "qlinear_version": (ctypes.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+# ----------------------------------------------------------------------------------
+# weights
+# ----------------------------------------------------------------------------------
+class QWeight:
+    """A quantized weight on the device, as stored.
+
+    ``wq``: int32 tensor [n, k*bits/32] (the uint32 words' bits); ``scales`` and
+    ``biases``: bfloat16 tensors [n, k/64].
+    """
+
+    def __init__(self, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, k: int, bits: int,
+                 group: int = 64):
+        self.wq, self.scales, self.biases = wq, scales, biases
+        self.n, self.k, self.bits, self.group = int(wq.shape[0]), int(k), int(bits), int(group)
+        for t in (wq, scales, biases):
+            if not t.is_contiguous():
+                raise ValueError("weight tensors must be contiguous")
+        self.c = ql_weight(wq.data_ptr(), scales.data_ptr(), biases.data_ptr(), self.n, self.k, self.bits,
+                           self.group)
+
+    @classmethod
+    def from_numpy(cls, d: dict, device="cuda") -> "QWeight":
+        """From a dict with uint32 ``wq``, uint16 (bf16 bits) ``scales``/``biases``, ``k``, ``bits``."""
+        wq = torch.from_numpy(np.ascontiguousarray(d["wq"]).view(np.int32)).to(device)
+        sc = torch.from_numpy(np.ascontiguousarray(d["scales"]).view(np.int16)).to(device).view(torch.bfloat16)
+        bi = torch.from_numpy(np.ascontiguousarray(d["biases"]).view(np.int16)).to(device).view(torch.bfloat16)
+        return cls(wq, sc, bi, d["k"], d["bits"])
+
+    def rows(self, lo: int, hi: int) -> "QWeight":
+        """Rows lo..hi-1 of the weight (views, no copy)."""
+        return QWeight(self.wq[lo:hi], self.scales[lo:hi], self.biases[lo:hi], self.k, self.bits, self.group)
+
+
+def bf16_from_bits(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """A bfloat16 device tensor with the given uint16 bit patterns."""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    """uint16 bit patterns of a bfloat16 tensor (copied to the host)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(code: int, where: str):
+    if code != QL_OK:
+        raise QlinearError(code, where)
+
+
+def _act(x: torch.Tensor, k: int) -> tuple[torch.Tensor, int, int]:
+    if x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise ValueError("activations must be a CUDA bfloat16 tensor")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if x.shape[1] != k or x.stride(1) != 1:
+        raise ValueError(f"activations must be [rows, {k}] with unit column stride")
+    return x, int(x.shape[0]), int(x.stride(0))
+
+
+# ----------------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ----------------------------------------------------------------------------------
+def qlinear_mv(w: QWeight, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    x, rows, _ = _act(x, w.k)
+    if rows != 1:
+        raise ValueError("qlinear_mv takes one activation row")
+    if y is None:
+        y = torch.empty(w.n, dtype=torch.float32, device=x.device)
+    _check(LIB.qlinear_mv(ctypes.byref(w.c), x.data_ptr(), y.data_ptr(), _stream(stream)), "qlinear_mv")
+    return y
+
+
+def qlinear_mv_rows(w: QWeight, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    x, rows, ldx = _act(x, w.k)
+    if y is None:
+        y = torch.empty(rows, w.n, dtype=torch.float32, device=x.device)
+    _check(LIB.qlinear_mv_rows(ctypes.byref(w.c), x.data_ptr(), rows, ldx, y.data_ptr(), y.stride(0),
+                               _stream(stream)), "qlinear_mv_rows")
+    return y
+
+
+def qffn_swiglu_mv(w1: QWeight, w3: QWeight, x: torch.Tensor, h: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    x, rows, ldx = _act(x, w1.k)
+    if h is None:
+        h = torch.empty(rows, w1.n, dtype=torch.bfloat16, device=x.device)
+    _check(LIB.qffn_swiglu_mv(ctypes.byref(w1.c), ctypes.byref(w3.c), x.data_ptr(), rows, ldx, h.data_ptr(),
+                              h.stride(0), _stream(stream)), "qffn_swiglu_mv")
+    return h
+
+
+def qattn_proj_mv(wq: QWeight, wk: QWeight, wv: QWeight, wg: QWeight, x: torch.Tensor, outs=None,
+                  stream=None):
+    x, rows, ldx = _act(x, wq.k)
+    if outs is None:
+        outs = [torch.empty(rows, w.n, dtype=torch.float32, device=x.device) for w in (wq, wk, wv, wg)]
+    q, k, v, g = outs
+    _check(LIB.qattn_proj_mv(ctypes.byref(wq.c), ctypes.byref(wk.c), ctypes.byref(wv.c), ctypes.byref(wg.c),
+                             x.data_ptr(), rows, ldx, q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(),
+                             _stream(stream)), "qattn_proj_mv")
+    return q, k, v, g
+
+
+def qlinear_pgemm(w: QWeight, X: torch.Tensor, Y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if X.dtype != torch.bfloat16 or not X.is_cuda or X.dim() != 2 or X.shape[1] != w.k or X.stride(1) != 1:
+        raise ValueError(f"X must be a CUDA bfloat16 [m, {w.k}] tensor with unit column stride")
+    m = int(X.shape[0])
+    if Y is None:
+        Y = torch.empty(m, w.n, dtype=torch.float32, device=X.device)
+    _check(LIB.qlinear_pgemm(ctypes.byref(w.c), X.data_ptr(), m, X.stride(0), Y.data_ptr(), Y.stride(0),
+                             _stream(stream)), "qlinear_pgemm")
+    return Y
+
+
+def qswiglu(a: torch.Tensor, c: torch.Tensor, h: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if a.shape != c.shape or a.dtype != torch.float32 or c.dtype != torch.float32 or a.stride() != c.stride():
+        raise ValueError("a and c must be float32 tensors of one shape and layout")
+    a2 = a.view(1, -1) if a.dim() == 1 else a
+    c2 = c.view(1, -1) if c.dim() == 1 else c
+    rows, n = int(a2.shape[0]), int(a2.shape[1])
+    if h is None:
+        h = torch.empty(rows, n, dtype=torch.bfloat16, device=a.device)
+    _check(LIB.qswiglu(a2.data_ptr(), c2.data_ptr(), rows, n, a2.stride(0), h.data_ptr(), h.stride(0),
+                       _stream(stream)), "qswiglu")
+    return h
+
+
+def qlinear_last_error(stream=None) -> int:
+    return int(LIB.qlinear_last_error(_stream(stream)))
+
+
+def qlinear_set_wait_budget_ns(ns: int) -> int:
+    return int(LIB.qlinear_set_wait_budget_ns(int(ns)))
+
+
+def qlinear_wait_probe(budget_ns: int, stream=None):
+    _check(LIB.qlinear_wait_probe(int(budget_ns), _stream(stream)), "qlinear_wait_probe")
+
+
+def qlinear_strerror(code: int) -> str:
+    return LIB.qlinear_strerror(int(code)).decode()
+
+
+def qlinear_version() -> int:
+    return int(LIB.qlinear_version())
