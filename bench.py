@@ -53,6 +53,12 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--bits", type=int, default=4, choices=[4, 6, 8])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, choices=["pgemm", "ffn", "mv"],
+                    help="run only one kernel (for profiler captures): warm-up launches, then --steps launches")
+    ap.add_argument("--m", type=int, default=PROMPT, help="--case pgemm: rows of X")
+    ap.add_argument("--n", type=int, default=D_FF, help="--case: output channels")
+    ap.add_argument("--k", type=int, default=D_MODEL, help="--case: input channels")
+    ap.add_argument("--rows", type=int, default=1, help="--case ffn/mv: activation rows")
     return ap.parse_args()
 
 
@@ -464,9 +470,59 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_case(args):
+    """One kernel on one shape: --warmup launches, then --steps timed launches."""
+    import torch
+    from weight_only_bit_mlx_gb300 import qlinear as q
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    bits, n, k = args.bits, args.n, args.k
+
+    def w():
+        wq = torch.randint(-2**31, 2**31 - 1, (n, k * bits // 32), generator=gen, dtype=torch.int32, device=dev)
+        s = (torch.rand(n, k // 64, generator=gen, device=dev) * 0.015 + 0.005).to(torch.bfloat16)
+        b = (torch.rand(n, k // 64, generator=gen, device=dev) * 0.2 - 0.1).to(torch.bfloat16)
+        return q.QWeight(wq, s, b, k, bits)
+
+    if args.case == "pgemm":
+        wt = w()
+        X = torch.randn(args.m, k, generator=gen, device=dev).to(torch.bfloat16)
+        Y = torch.empty(args.m, n, device=dev)
+        fn, unit, work = (lambda: q.qlinear_pgemm(wt, X, Y)), "TFLOP/s", 2.0 * args.m * n * k
+    elif args.case == "ffn":
+        w1, w3 = w(), w()
+        x = torch.randn(args.rows, k, generator=gen, device=dev).to(torch.bfloat16)
+        h = torch.empty(args.rows, n, dtype=torch.bfloat16, device=dev)
+        fn, unit = (lambda: q.qffn_swiglu_mv(w1, w3, x, h)), "GB/s"
+        work = 2 * weight_bytes(n, k, bits) + args.rows * (k * 2 + n * 2)
+    else:
+        wt = w()
+        x = torch.randn(args.rows, k, generator=gen, device=dev).to(torch.bfloat16)
+        y = torch.empty(args.rows, n, device=dev)
+        fn, unit = (lambda: q.qlinear_mv_rows(wt, x, y)), "GB/s"
+        work = weight_bytes(n, k, bits) + args.rows * (k * 2 + n * 4)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    print(json.dumps({"case": args.case, "bits": bits, "m": args.m, "n": n, "k": k, "rows": args.rows,
+                      "us_per_launch": ms * 1e3, unit: work / (ms * 1e-3) / scale,
+                      "status": q.qlinear_last_error()}), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.case is not None:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
