@@ -61,7 +61,8 @@ enum {
   QL_ERR_LAUNCH = -8,   /* the kernel launch failed (cudaGetLastError after launch) */
   QL_ERR_TIMEOUT = -9,  /* a bounded device-side wait gave up (reported by qlinear_last_error) */
   QL_ERR_CUDA = -10,    /* another CUDA runtime error (device query, tensor-map encoding) */
-  QL_ERR_NOMEM = -11    /* the library could not allocate its scratch buffer */
+  QL_ERR_NOMEM = -11,   /* the library could not allocate its scratch buffer */
+  QL_ERR_TOO_LARGE = -12 /* the problem does not fit the fixed scratch of qlinear_pgemm_noalloc */
 };
 
 /* One quantized weight matrix, as stored.  All pointers are device pointers. */
@@ -136,6 +137,31 @@ int qattn_proj_mv(const ql_weight *wq, const ql_weight *wk, const ql_weight *wv,
  */
 int qlinear_pgemm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, float *Y,
                   int64_t ldy, void *stream);
+
+/*
+ * qlinear_pgemm_noalloc - qlinear_pgemm for callers that cannot allocate device
+ * memory when they call: code whose device memory belongs to another allocator or
+ * is held to a fixed budget, and code that must not pay the device-wide
+ * synchronization of growing qlinear_pgemm's scratch buffer (which frees and
+ * reallocates it).  The source pages have no counterpart; this is a deployment
+ * variant of the same computation, bit-equal to qlinear_pgemm on the same inputs.
+ *   Arguments, layouts and errors are those of qlinear_pgemm.  The split row sums
+ *   live in one file-scope static device array of 1,048,576 bf16 values (2 MiB),
+ *   which every GPU that loads the library holds until the process exits.
+ *   Limit: m * round_up(3*k/64, 64) <= 1,048,576 (for example m <= 8192 at k = 2048,
+ *   m <= 2730 at k = 8192); larger problems return QL_ERR_TOO_LARGE before anything
+ *   is enqueued.  The call itself allocates nothing (no cudaMalloc, cudaFree or
+ *   allocating library routine).
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current and caches it; make that first
+ *   call before any stream capture.
+ *   Sharing: all calls on a device use the same array, which keeps the last call's
+ *   contents.  Nothing in it needs to start at zero (each call writes every value it
+ *   reads before reading it), but calls that overlap on the GPU - on different
+ *   streams, or from different host threads - race on it and must be ordered.
+ */
+int qlinear_pgemm_noalloc(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, float *Y,
+                          int64_t ldy, void *stream);
 
 /*
  * qswiglu - h[r][i] = bf16(silu(a[r][i]) * c[r][i]) (float32 math, nearest-even

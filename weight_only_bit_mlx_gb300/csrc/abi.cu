@@ -209,6 +209,22 @@ int qlinear_pgemm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx,
   return pgemm_run(w, X, m, ldx, Y, ldy, static_cast<cudaStream_t>(stream), status);
 }
 
+// Same checks as qlinear_pgemm, then the fixed-scratch variant (allocates nothing).
+int qlinear_pgemm_noalloc(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, float *Y, int64_t ldy,
+                          void *stream) {
+  int e = check_weight(w);
+  if (e) return e;
+  if (m < 0) return QL_ERR_SHAPE;
+  if (m == 0) return QL_OK;
+  if (X == nullptr || Y == nullptr) return QL_ERR_NULL;
+  if (!aligned(X, 16) || (ldx % 8) != 0 || ldx < w->k || ldy < w->n || !aligned(Y, 4)) return QL_ERR_ALIGN;
+  const int64_t lds = ((3 * (int64_t)(w->k / 64) + 63) / 64) * 64;
+  if ((int64_t)m * lds > pgemm_noalloc_max_elems()) return QL_ERR_TOO_LARGE;
+  int *status = nullptr;
+  if ((e = device_setup(&status))) return e;
+  return pgemm_run_noalloc(w, X, m, ldx, Y, ldy, static_cast<cudaStream_t>(stream), status);
+}
+
 int qswiglu(const float *a, const float *c, int32_t rows, int32_t n, int64_t lda, uint16_t *h, int64_t ldh,
             void *stream) {
   if (a == nullptr || c == nullptr || h == nullptr) return QL_ERR_NULL;
@@ -259,6 +275,7 @@ const char *qlinear_strerror(int code) {
     case QL_ERR_TIMEOUT: return "a bounded device-side wait gave up";
     case QL_ERR_CUDA: return "CUDA runtime error";
     case QL_ERR_NOMEM: return "could not allocate scratch memory";
+    case QL_ERR_TOO_LARGE: return "m * round_up(3*k/64, 64) exceeds the 1,048,576-value fixed scratch";
     default: return "unknown qlinear status";
   }
 }

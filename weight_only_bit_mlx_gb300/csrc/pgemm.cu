@@ -594,6 +594,62 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   return QL_OK;
 }
 
+// ---- the same GEMM with a fixed, statically allocated scratch ---------------------
+// For callers that must not allocate device memory at call time: code whose device
+// memory is owned by another allocator or held to a fixed budget, and code that must
+// not stall on the device-wide synchronization that growing (freeing and
+// reallocating) a scratch buffer costs.  The split row sums then live in this
+// file-scope array instead of the library's growable buffer.  Every GPU that loads
+// the library holds the array until the process exits.
+constexpr int64_t kNoAllocScratchElems = int64_t(1) << 20;  // 1,048,576 bf16 values = 2 MiB
+static __device__ __align__(256) uint16_t g_noalloc_scratch[kNoAllocScratchElems];
+
+static std::mutex g_noalloc_mu;
+static uint16_t *g_noalloc_addr[kMaxDev];
+
+// Device address of the static array for the current device.  The name of a
+// __device__ array in host code is only a host-side stand-in, so the address is
+// looked up once per device, with that device current, and cached.
+static int noalloc_scratch_addr(uint16_t **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return QL_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return QL_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = static_cast<uint16_t *>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return QL_OK;
+}
+
+int64_t pgemm_noalloc_max_elems() { return kNoAllocScratchElems; }
+
+int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
+                      cudaStream_t st, int *status) {
+  const int G = w->k / 64;
+  const int64_t lds = ((3 * (int64_t)G + 63) / 64) * 64;
+  if ((int64_t)m * lds > kNoAllocScratchElems) return QL_ERR_TOO_LARGE;
+  uint16_t *S = nullptr;
+  int e = noalloc_scratch_addr(&S);
+  if (e) return e;
+  // every scratch value the GEMM reads is written by this pre-pass first, so nothing
+  // left by an earlier call needs clearing
+  const int64_t total = (int64_t)m * G;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 8192) blocks = 8192;
+  pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
+  if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+  switch (w->bits) {
+    case 4: return launch_pgemm<4>(w, X, m, ldx, Y, ldy, S, lds, st, status);
+    case 6: return launch_pgemm<6>(w, X, m, ldx, Y, ldy, S, lds, st, status);
+    default: return launch_pgemm<8>(w, X, m, ldx, Y, ldy, S, lds, st, status);
+  }
+}
+
 int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy, cudaStream_t st,
               int *status) {
   const int G = w->k / 64;

@@ -29,6 +29,7 @@ QL_ERR_LAUNCH = -8
 QL_ERR_TIMEOUT = -9
 QL_ERR_CUDA = -10
 QL_ERR_NOMEM = -11
+QL_ERR_TOO_LARGE = -12
 
 
 class QlinearError(RuntimeError):
@@ -55,6 +56,7 @@ def _load() -> ctypes.CDLL:
         "qffn_swiglu_mv": (ctypes.c_int, [W, W, P, I32, I64, P, I64, P]),
         "qattn_proj_mv": (ctypes.c_int, [W, W, W, W, P, I32, I64, P, P, P, P, P]),
         "qlinear_pgemm": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
+        "qlinear_pgemm_noalloc": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
         "qswiglu": (ctypes.c_int, [P, P, I32, I32, I64, P, I64, P]),
         "qlinear_last_error": (ctypes.c_int, [P]),
         "qlinear_set_wait_budget_ns": (U64, [U64]),
@@ -188,6 +190,16 @@ def qlinear_pgemm(w: QWeight, X: torch.Tensor, Y: torch.Tensor | None = None, st
         Y = torch.empty(m, w.n, dtype=torch.float32, device=X.device)
     _check(LIB.qlinear_pgemm(ctypes.byref(w.c), X.data_ptr(), m, X.stride(0), Y.data_ptr(), Y.stride(0),
                              _stream(stream)), "qlinear_pgemm")
+    return Y
+
+
+def qlinear_pgemm_noalloc(w: QWeight, X: torch.Tensor, Y: torch.Tensor, stream=None) -> torch.Tensor:
+    """qlinear_pgemm with the library's fixed static scratch: the library allocates
+    nothing, so the caller passes the output buffer too."""
+    if X.dtype != torch.bfloat16 or not X.is_cuda or X.dim() != 2 or X.shape[1] != w.k or X.stride(1) != 1:
+        raise ValueError(f"X must be a CUDA bfloat16 [m, {w.k}] tensor with unit column stride")
+    _check(LIB.qlinear_pgemm_noalloc(ctypes.byref(w.c), X.data_ptr(), int(X.shape[0]), X.stride(0), Y.data_ptr(),
+                                     Y.stride(0), _stream(stream)), "qlinear_pgemm_noalloc")
     return Y
 
 
