@@ -101,6 +101,16 @@ __global__ void swiglu_kernel(const float *a, const float *c, int rows, int n, i
   }
 }
 
+// Contiguous rows and 16-byte aligned data: four elements per thread step.
+__global__ void swiglu_vec4_kernel(const float4 *a, const float4 *c, int64_t n4, uint2 *h) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 av = a[i], cv = c[i];
+    const uint32_t h0 = swiglu_bf16(av.x, cv.x), h1 = swiglu_bf16(av.y, cv.y);
+    const uint32_t h2 = swiglu_bf16(av.z, cv.z), h3 = swiglu_bf16(av.w, cv.w);
+    h[i] = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+  }
+}
+
 // One thread waits on a barrier nothing will ever complete; the bounded wait gives
 // up after budget_ns and records QL_ERR_TIMEOUT.
 __global__ void wait_probe_kernel(int *status, uint64_t budget_ns) {
@@ -128,9 +138,12 @@ int qlinear_mv_rows(const ql_weight *w, const uint16_t *x, int32_t rows, int64_t
   if ((e = check_x(x, rows, ldx, w->k))) return e;
   if (y == nullptr) return QL_ERR_NULL;
   if (rows > 1 && ldy < w->n) return QL_ERR_ALIGN;
-  if ((e = device_setup(nullptr))) return e;
+  int *status = nullptr;
+  if ((e = device_setup(&status))) return e;
   MvParams p;
   std::memset(&p, 0, sizeof(p));
+  p.status = status;
+  p.budget_ns = wait_budget_ns();
   p.m[0] = make_mat(w, y, ldy);
   p.x = x;
   p.ldx = ldx;
@@ -154,9 +167,12 @@ int qffn_swiglu_mv(const ql_weight *w1, const ql_weight *w3, const uint16_t *x, 
   if ((e = check_x(x, rows, ldx, w1->k))) return e;
   if (h == nullptr) return QL_ERR_NULL;
   if (rows > 1 && ldh < w1->n) return QL_ERR_ALIGN;
-  if ((e = device_setup(nullptr))) return e;
+  int *status = nullptr;
+  if ((e = device_setup(&status))) return e;
   MvParams p;
   std::memset(&p, 0, sizeof(p));
+  p.status = status;
+  p.budget_ns = wait_budget_ns();
   p.m[0] = make_mat(w1, h, ldh);
   p.m[1] = make_mat(w3, h, ldh);
   p.x = x;
@@ -180,9 +196,12 @@ int qattn_proj_mv(const ql_weight *wq, const ql_weight *wk, const ql_weight *wv,
     if (ws[i]->k != wq->k) return QL_ERR_SHAPE;
   }
   if ((e = check_x(x, rows, ldx, wq->k))) return e;
-  if ((e = device_setup(nullptr))) return e;
+  int *status = nullptr;
+  if ((e = device_setup(&status))) return e;
   MvParams p;
   std::memset(&p, 0, sizeof(p));
+  p.status = status;
+  p.budget_ns = wait_budget_ns();
   int tiles = 0;
   for (int i = 0; i < 4; ++i) {
     p.m[i] = make_mat(ws[i], outs[i], ws[i]->n);
@@ -233,9 +252,19 @@ int qswiglu(const float *a, const float *c, int32_t rows, int32_t n, int64_t lda
   int e;
   if ((e = device_setup(nullptr))) return e;
   const int64_t total = (int64_t)rows * n;
-  int blocks = (int)((total + 255) / 256);
-  if (blocks > 4096) blocks = 4096;
-  swiglu_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a, c, rows, n, lda, h, ldh);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((rows == 1 || (lda == n && ldh == n)) && total % 4 == 0 && aligned(a, 16) && aligned(c, 16) &&
+      aligned(h, 8)) {
+    const int64_t n4 = total / 4;
+    int blocks = (int)((n4 + 255) / 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    swiglu_vec4_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4 *>(a), reinterpret_cast<const float4 *>(c),
+                                               n4, reinterpret_cast<uint2 *>(h));
+  } else {
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    swiglu_kernel<<<blocks, 256, 0, st>>>(a, c, rows, n, lda, h, ldh);
+  }
   return launch_status(cudaGetLastError());
 }
 

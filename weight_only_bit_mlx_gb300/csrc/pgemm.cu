@@ -19,11 +19,11 @@
 // each output from its own row and column, tiles out of range are zero-filled by
 // TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
 //
-// Warp roles (one CTA per 128 x 128 output tile, 448 threads):
+// Warp roles (one CTA per 128 x 128 output tile, 576 threads):
 //   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block)
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2-5   converters: packed codes -> bf16 (SWIZZLE_128B K-major), scales -> fp32
-//   warps 6-13  epilogue: TMEM -> registers, scale chain, bias add, store
+//   warps 2-9   converters: packed codes -> bf16 (SWIZZLE_128B K-major), scales -> fp32
+//   warps 10-17 epilogue: TMEM -> registers, scale chain, bias add, store
 //               (two warps per TMEM lane quarter, 64 columns each)
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
 // QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees TMEM and returns.
@@ -46,16 +46,22 @@ constexpr int BN = 128;
 constexpr int BK = 64;
 constexpr int kStages = 4;   // TMA stages (X/S tile + packed W tile)
 constexpr int kBStages = 3;  // converted bf16 W tiles
-constexpr int kScStages = 4; // fp32 scale rows
-constexpr int kConvWarps = 4;
+constexpr int kScStages = 8; // fp32 scale rows (deep enough to need no release barrier, see converters)
+constexpr int kConvWarps = 8;  // two per SM sub-partition; a thread converts half a row
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each owning half the columns
-constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
+constexpr int kRoleWarps = 2;  // producer, MMA issuer
+constexpr int kThreads = (kRoleWarps + kConvWarps + kEpiWarps) * 32;
+constexpr int kConvBase = kRoleWarps * 32;                  // first converter thread
+constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;          // first epilogue warp
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytes = BN * BK * 2;
 constexpr int kTmemCols = 2 * BN;
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
+constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
+constexpr int kPf = 4;       // k blocks of scale/bias prefetch
+static_assert(kScStages > kBStages + 2, "scale ring must outlast the MMA/epilogue lag");
 
 template <int BITS> struct Cfg {
   static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
@@ -64,9 +70,14 @@ template <int BITS> struct Cfg {
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffW = kOffB + kBStages * kBBytes;
   static constexpr int kOffSc = kOffW + kStages * kWBytes;
-  static constexpr int kOffBar = kOffSc + kScStages * BN * 4;
-  // barriers: tma_full, tma_empty, b_full, b_empty, acc_full[2], acc_empty[2], sc_full, sc_empty, mma_done
-  static constexpr int kNumBars = 2 * kStages + 2 * kBStages + 4 + 2 * kScStages + 1;
+  // biases of the tile's rows, bf16, boxes of 8 groups: [kBiasG / 8][BN][8]
+  static constexpr int kOffBias = kOffSc + kScStages * BN * 4;
+  // scale boxes streamed by TMA, bf16 [2][BN][8]
+  static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
+  static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
+  // barriers: tma_full, tma_empty, b_full, b_empty, acc_full[2], acc_empty[2], sc_full,
+  //           scb_full[2], scb_empty[2], bias_full, mma_done
+  static constexpr int kNumBars = 2 * kStages + 2 * kBStages + 4 + kScStages + 4 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -75,6 +86,8 @@ template <int BITS> struct Cfg {
 struct Params {
   const uint16_t *scales;
   const uint16_t *biases;
+  int sc_tma;  // scales arrive as TMA boxes of 8 groups (k % 512 == 0, 16-byte aligned)
+  int bi_tma;  // biases arrive as TMA boxes too (additionally k <= 64 * kBiasG)
   float *Y;
   int64_t ldy;
   int M, N, G, NBB;
@@ -151,11 +164,42 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// (d0, d1) = (a0, a1) * (b0, b1) + (d0, d1), each rounded to nearest (packed fp32 fma)
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rd, {%0, %1};"
+      "\n\tfma.rn.f32x2 rd, ra, rb, rd;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ uint4 lds128(const void *p) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(smem_addr(p)));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(const void *p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
   return v;
 }
 
@@ -177,8 +221,8 @@ __device__ __forceinline__ uint32_t window32(const uint32_t (&w)[NW], int off) {
 
 // One packed row of one k block (64 codes) -> 8 chunks of 8 bf16 codes, chunk c
 // holding k = 8c .. 8c+7 in natural order.
-template <int BITS>
-__device__ __forceinline__ uint4 convert_chunk(const uint32_t (&w)[BK * BITS / 32], int c) {
+template <int BITS, int NW>
+__device__ __forceinline__ uint4 convert_chunk(const uint32_t (&w)[NW], int c) {
   uint4 o;
   if constexpr (BITS == 4) {
     const uint32_t x = w[c], x4 = x >> 4;
@@ -199,7 +243,8 @@ __device__ __forceinline__ uint4 convert_chunk(const uint32_t (&w)[BK * BITS / 3
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     pgemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ Params p) {
+                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmSc,
+                 const __grid_constant__ CUtensorMap tmBi, const __grid_constant__ Params p) {
   using C = Cfg<BITS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -215,8 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *acc_full = b_empty + kBStages;
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *sc_full = acc_empty + 2;
-  uint64_t *sc_empty = sc_full + kScStages;
-  uint64_t *mma_done = sc_empty + kScStages;
+  uint64_t *scb_full = sc_full + kScStages;
+  uint64_t *scb_empty = scb_full + 2;
+  uint64_t *bias_full = scb_empty + 2;
+  uint64_t *mma_done = bias_full + 1;
+  uint16_t *sbias = reinterpret_cast<uint16_t *>(smem + C::kOffBias);
+  uint16_t *scbox = reinterpret_cast<uint16_t *>(smem + C::kOffScBox);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -229,13 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) { mbar_init(&tma_full[i], 1); mbar_init(&tma_empty[i], 1 + kConvThreads); }
     for (int i = 0; i < kBStages; ++i) { mbar_init(&b_full[i], kConvThreads); mbar_init(&b_empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kEpiThreads); }
-    for (int i = 0; i < kScStages; ++i) { mbar_init(&sc_full[i], kConvThreads); mbar_init(&sc_empty[i], kEpiThreads); }
+    for (int i = 0; i < kScStages; ++i) mbar_init(&sc_full[i], kConvThreads);
+    for (int i = 0; i < 2; ++i) { mbar_init(&scb_full[i], 1); mbar_init(&scb_empty[i], kConvThreads); }
+    mbar_init(bias_full, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmS);
+    if (p.sc_tma) prefetch_tmap(&tmSc);
+    if (p.bi_tma) prefetch_tmap(&tmBi);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -257,7 +310,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued = 0;
+      if (p.bi_tma) {
+        // every bias of the tile's rows, once (read only by the bias blocks at the end)
+        const int nbox = (G + 7) / 8;
+        mbar_arrive_expect_tx(bias_full, (uint32_t)(nbox * BN * 16));
+        for (int i = 0; i < nbox; ++i) tma_load_2d(sbias + i * BN * 8, &tmBi, bias_full, 8 * i, n0);
+      }
+      int sc_boxes = 0;
       for (int kb = 0; kb < KB; ++kb) {
+        if (p.sc_tma && kb < G && (kb & 7) == 0) {
+          // scales of blocks kb .. kb+7 for the tile's rows, two boxes in flight
+          const int j = kb >> 3, slot = j & 1;
+          if (!mbar_wait_bounded(&scb_empty[slot], ((uint32_t)(j >> 1) & 1u) ^ 1u, budget, abort_flag)) {
+            give_up();
+            break;
+          }
+          mbar_arrive_expect_tx(&scb_full[slot], (uint32_t)(BN * 16));
+          tma_load_2d(scbox + slot * BN * 8, &tmSc, &scb_full[slot], kb, n0);
+          sc_boxes = j + 1;
+        }
         const int s = kb % kStages;
         const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
         if (!mbar_wait_bounded(&tma_empty[s], ph ^ 1u, budget, abort_flag)) { give_up(); break; }
@@ -271,6 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = kb + 1;
       }
+      // drain the scale and bias boxes too
+      for (int j = (sc_boxes > 2 ? sc_boxes - 2 : 0); j < sc_boxes; ++j)
+        (void)mbar_wait_bounded(&scb_full[j & 1], (uint32_t)(j >> 1) & 1u, kDrainBudgetNs, nullptr);
+      if (p.bi_tma) (void)mbar_wait_bounded(bias_full, 0u, kDrainBudgetNs, nullptr);
       // drain: every copy this CTA started must land before its shared memory goes away
       for (int s = 0; s < kStages && s < issued; ++s) {
         const int uses = (issued - 1 - s) / kStages + 1;
@@ -312,77 +387,131 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait_bounded(mma_done, 0u, kDrainBudgetNs, nullptr);
       }
     }
-  } else if (warp < 2 + kConvWarps) {
+  } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ converters
-    const int ct = threadIdx.x - 64;  // 0..127: one row of the W tile
+    const int cthr = threadIdx.x - kConvBase;  // 0..255
+    const int ct = cthr & (BN - 1);      // row of the W tile
+    const int chalf = cthr >> 7;         // chunks 4*chalf .. 4*chalf+3 of the row
+    const bool lead = chalf == 0;        // the thread that also moves the row's scale and bias
     const int n = n0 + ct;
     const bool nvalid = n < p.N;
     const uint16_t *srow = p.scales + (size_t)(nvalid ? n : 0) * G;
     const uint16_t *brow = p.biases + (size_t)(nvalid ? n : 0) * G;
-    uint32_t s_next = nvalid ? ldg_u16(srow) : 0u;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % kStages, sb = kb % kBStages;
-      uint32_t s_cur = s_next;
-      if (kb + 1 < G) s_next = nvalid ? ldg_u16(srow + kb + 1) : 0u;
-      if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / kStages) & 1u, budget, abort_flag)) { give_up(); break; }
-      if (!mbar_wait_bounded(&b_empty[sb], ((uint32_t)(kb / kBStages) & 1u) ^ 1u, budget, abort_flag)) {
-        give_up();
-        break;
-      }
-      uint8_t *brow_s = sB + sb * kBBytes + ct * 128;
-      const int sw = ct & 7;
-      if (kb < G) {
-        constexpr int NW = BK * BITS / 32;
-        uint32_t w[NW];
-        const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes;
+    const bool bias_smem = G <= kBiasG;
+    // Without TMA boxes (k % 512 != 0), the lead thread loads its row's scale and bias
+    // itself, kPf blocks ahead; the loop is unrolled by kPf so that each ring slot
+    // stays in place while its load is in flight.
+    uint32_t sr[kPf], br[kPf];
 #pragma unroll
-        for (int i = 0; i < NW / 4; ++i) {
-          uint4 v = lds128(wp + 16 * i);
-          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    for (int i = 0; i < kPf; ++i) {
+      sr[i] = (lead && !p.sc_tma && nvalid && i < G) ? ldg_u16(srow + i) : 0u;
+      br[i] = (lead && !p.bi_tma && bias_smem && nvalid && i < G) ? ldg_u16(brow + i) : 0u;
+    }
+    bool alive = true;
+    for (int kb0 = 0; kb0 < KB && alive; kb0 += kPf) {
+#pragma unroll
+      for (int u = 0; u < kPf; ++u) {
+        const int kb = kb0 + u;
+        if (kb >= KB || !alive) break;
+        const int s = kb % kStages, sb = kb % kBStages;
+        uint32_t s_cur = 0u, b_cur = 0u;
+        if (kb < G) {
+          if (!p.sc_tma) {
+            s_cur = sr[u];
+            sr[u] = (lead && nvalid && kb + kPf < G) ? ldg_u16(srow + kb + kPf) : 0u;
+          } else {
+            const int j = kb >> 3, slot = j & 1;
+            if ((kb & 7) == 0 &&
+                !mbar_wait_bounded(&scb_full[slot], (uint32_t)(j >> 1) & 1u, budget, abort_flag)) {
+              give_up();
+              alive = false;
+              break;
+            }
+            s_cur = scbox[(slot * BN + ct) * 8 + (kb & 7)];
+            if ((kb & 7) == 7 || kb == G - 1) mbar_arrive(&scb_empty[slot]);
+          }
+          if (!p.bi_tma && bias_smem) {
+            b_cur = br[u];
+            br[u] = (lead && nvalid && kb + kPf < G) ? ldg_u16(brow + kb + kPf) : 0u;
+          }
         }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) sts128(brow_s + ((c ^ sw) << 4), convert_chunk<BITS>(w, c));
-        const int sc = kb % kScStages;
-        if (!mbar_wait_bounded(&sc_empty[sc], ((uint32_t)(kb / kScStages) & 1u) ^ 1u, budget, abort_flag)) {
+        if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / kStages) & 1u, budget, abort_flag) ||
+            !mbar_wait_bounded(&b_empty[sb], ((uint32_t)(kb / kBStages) & 1u) ^ 1u, budget, abort_flag)) {
           give_up();
+          alive = false;
           break;
         }
-        sSc[sc * BN + ct] = bf16_to_f32(s_cur);
-        fence_proxy_async();
-        mbar_arrive(&b_full[sb]);
-        mbar_arrive(&sc_full[sc]);
-        mbar_arrive(&tma_empty[s]);
-      } else {
-        // bias block: column t of block jb is k' = 64*jb + t of the [part][group]
-        // layout; its B value is bias[n][k' mod G] (zero past 3G)
-        const int base = (kb - G) * BK;
+        uint8_t *brow_s = sB + sb * kBBytes + ct * 128;
+        const int sw = ct & 7;
+        if (kb < G) {
+          constexpr int NW = BK * BITS / 64;  // words of half a row
+          uint32_t w[NW];
+          const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes + chalf * (C::kRowBytes / 2);
+          if constexpr ((NW % 4) == 0) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t h[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            int j = base + 8 * c + e;
-            uint32_t v = 0u;
-            if (nvalid && j < 3 * G) {
-              if (j >= G) j -= G;
-              if (j >= G) j -= G;
-              v = ldg_u16(brow + j);
+            for (int i = 0; i < NW / 4; ++i) {
+              uint4 v = lds128(wp + 16 * i);
+              w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
             }
-            h[e] = v;
+          } else {
+#pragma unroll
+            for (int i = 0; i < NW / 2; ++i) {
+              uint2 v = lds64(wp + 8 * i);
+              w[2 * i] = v.x; w[2 * i + 1] = v.y;
+            }
           }
-          uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-          sts128(brow_s + ((c ^ sw) << 4), o);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int cc = 4 * chalf + c;
+            sts128(brow_s + ((cc ^ sw) << 4), convert_chunk<BITS, NW>(w, c));
+          }
+          if (lead && !p.bi_tma && bias_smem) sbias[((kb >> 3) * BN + ct) * 8 + (kb & 7)] = (uint16_t)b_cur;
+          // Scale slot kb % kScStages was last read by the epilogue for block
+          // kb - kScStages.  Passing b_empty for this block means the MMA of block
+          // kb - kBStages finished, which waited for the epilogue to release block
+          // kb - kBStages - 2; kScStages > kBStages + 2 keeps the slot free.
+          if (lead) sSc[(kb % kScStages) * BN + ct] = bf16_to_f32(s_cur);
+          fence_proxy_async();
+          mbar_arrive(&b_full[sb]);
+          mbar_arrive(&sc_full[kb % kScStages]);
+          mbar_arrive(&tma_empty[s]);
+        } else {
+          // bias block: column t of block jb is k' = 64*jb + t of the [part][group]
+          // layout; its B value is bias[n][k' mod G] (zero past 3G)
+          if (kb == G && p.bi_tma && !mbar_wait_bounded(bias_full, 0u, budget, abort_flag)) {
+            give_up();
+            alive = false;
+            break;
+          }
+          const int base = (kb - G) * BK;
+#pragma unroll
+          for (int c = 4 * chalf; c < 4 * chalf + 4; ++c) {
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              int j = base + 8 * c + e;
+              uint32_t v = 0u;
+              if (nvalid && j < 3 * G) {
+                if (j >= G) j -= G;
+                if (j >= G) j -= G;
+                v = bias_smem ? (uint32_t)sbias[((j >> 3) * BN + ct) * 8 + (j & 7)] : ldg_u16(brow + j);
+              }
+              h[e] = v;
+            }
+            uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+            sts128(brow_s + ((c ^ sw) << 4), o);
+          }
+          fence_proxy_async();
+          mbar_arrive(&b_full[sb]);
+          mbar_arrive(&tma_empty[s]);
         }
-        fence_proxy_async();
-        mbar_arrive(&b_full[sb]);
-        mbar_arrive(&tma_empty[s]);
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     constexpr int CW = BN / 2;  // columns owned by one thread
     const int q = warp & 3;     // TMEM lane quarter this warp may access
-    const int half = (warp - (2 + kConvWarps)) / 4;
+    const int half = (warp - kEpiWarp0) / 4;
     const int row = 32 * q + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(half * CW);
     float y[CW];
@@ -400,22 +529,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float4 *sc4 = reinterpret_cast<const float4 *>(sSc + sc * BN + half * CW);
+      // 8-column chunks; the next chunk's TMEM load is in flight while one is used
+      uint32_t ra[8], rb[8];
+      tmem_ld8_nowait(lane_base + (uint32_t)(buf * BN), ra);
+      tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < CW / 16; ++j) {
-        uint32_t r[16];
-        tmem_ld16(lane_base + (uint32_t)(buf * BN + 16 * j), r);
+      for (int ch = 0; ch < CW / 8; ++ch) {
+        uint32_t(&cur)[8] = (ch & 1) ? rb : ra;
+        uint32_t(&nxt)[8] = (ch & 1) ? ra : rb;
+        if (ch + 1 < CW / 8) tmem_ld8_nowait(lane_base + (uint32_t)(buf * BN + 8 * (ch + 1)), nxt);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 s4 = sc4[4 * j + i];
-          y[16 * j + 4 * i + 0] = __fmaf_rn(s4.x, __uint_as_float(r[4 * i + 0]), y[16 * j + 4 * i + 0]);
-          y[16 * j + 4 * i + 1] = __fmaf_rn(s4.y, __uint_as_float(r[4 * i + 1]), y[16 * j + 4 * i + 1]);
-          y[16 * j + 4 * i + 2] = __fmaf_rn(s4.z, __uint_as_float(r[4 * i + 2]), y[16 * j + 4 * i + 2]);
-          y[16 * j + 4 * i + 3] = __fmaf_rn(s4.w, __uint_as_float(r[4 * i + 3]), y[16 * j + 4 * i + 3]);
+        for (int i = 0; i < 2; ++i) {
+          const float4 s4 = sc4[2 * ch + i];
+          float *yy = &y[8 * ch + 4 * i];
+          ffma2(yy[0], yy[1], s4.x, s4.y, __uint_as_float(cur[4 * i]), __uint_as_float(cur[4 * i + 1]));
+          ffma2(yy[2], yy[3], s4.z, s4.w, __uint_as_float(cur[4 * i + 2]), __uint_as_float(cur[4 * i + 3]));
         }
+        if (ch + 1 < CW / 8) tmem_wait_ld();
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
-      mbar_arrive(&sc_empty[sc]);
     }
     if (ok) {
       bool w_ok = mbar_wait_bounded(&acc_full[G & 1], (uint32_t)(G >> 1) & 1u, budget, abort_flag);
@@ -558,7 +691,7 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
                         const uint16_t *S, int64_t lds, cudaStream_t st, int *status) {
   using C = pg::Cfg<BITS>;
   const int G = w->k / 64;
-  CUtensorMap tmX, tmW, tmS;
+  CUtensorMap tmX, tmW, tmS, tmSc, tmBi;
   if (!make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)w->k, (uint64_t)m, (uint64_t)ldx * 2, pg::BK,
                 pg::BM, CU_TENSOR_MAP_SWIZZLE_128B))
     return QL_ERR_CUDA;
@@ -568,6 +701,16 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, (uint64_t)(3 * G), (uint64_t)m, (uint64_t)lds * 2,
                 pg::BK, pg::BM, CU_TENSOR_MAP_SWIZZLE_128B))
     return QL_ERR_CUDA;
+  // scales/biases as TMA boxes of 8 groups when their rows are 16-byte aligned
+  const bool sb_ok = (G % 8) == 0 && (reinterpret_cast<uintptr_t>(w->scales) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(w->biases) & 15) == 0;
+  const bool sc_tma = sb_ok && make_map(&tmSc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w->scales, (uint64_t)G,
+                                        (uint64_t)w->n, (uint64_t)G * 2, 8, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+  const bool bi_tma = sc_tma && G <= pg::kBiasG &&
+                      make_map(&tmBi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w->biases, (uint64_t)G, (uint64_t)w->n,
+                               (uint64_t)G * 2, 8, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!sc_tma) tmSc = tmX;  // never read
+  if (!bi_tma) tmBi = tmX;  // never read
   static bool attr_set[kMaxDev] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -580,6 +723,8 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   pg::Params p;
   p.scales = w->scales;
   p.biases = w->biases;
+  p.sc_tma = sc_tma ? 1 : 0;
+  p.bi_tma = bi_tma ? 1 : 0;
   p.Y = Y;
   p.ldy = ldy;
   p.M = m;
@@ -589,7 +734,7 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   p.status = status;
   p.budget_ns = wait_budget_ns();
   dim3 grid((unsigned)((w->n + pg::BN - 1) / pg::BN), (unsigned)((m + pg::BM - 1) / pg::BM));
-  pg::pgemm_kernel<BITS><<<grid, pg::kThreads, C::kAlloc, st>>>(tmX, tmW, tmS, p);
+  pg::pgemm_kernel<BITS><<<grid, pg::kThreads, C::kAlloc, st>>>(tmX, tmW, tmS, tmSc, tmBi, p);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   return QL_OK;
 }

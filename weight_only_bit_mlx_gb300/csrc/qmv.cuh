@@ -6,8 +6,7 @@
 
 namespace qlk {
 
-constexpr int kMvGpw = 2;         // 64-wide groups per warp slice
-constexpr int kMvMaxWarps = 8;    // warps (k-slices) per CTA
+constexpr int kMvWarps = 4;       // warps per CTA (each owns a slice of the CTA's k chunk)
 constexpr int kMvMaxCluster = 8;  // CTAs per cluster along k
 
 enum { kMvPlain = 0, kMvFfn = 1, kMvAttn = 2 };
@@ -28,15 +27,18 @@ struct MvParams {
   int64_t ldx;
   int rows;
   int k;
+  int *status;           // device status word (bounded waits record QL_ERR_TIMEOUT)
+  int sb_bulk;           // scales/biases rows are 16-byte aligned: copied in bulk
+  uint64_t budget_ns;    // bound of every device-side wait
   // filled by launch_mv from k and bits
   int groups;
   int wpr;
-  int slices;
-  int cs;
+  int span_g;            // groups per CTA (processed in chunks of the per-bits span)
+  int cs;                // CTAs per cluster along k
 };
 
-// k-decomposition used by every decode launch (function of k only)
-void mv_geometry(int k, int &groups, int &slices, int &nwarps, int &cs);
+// k-decomposition used by every decode launch (a function of k and bits only)
+void mv_geometry(int k, int bits, int &groups, int &span_g, int &nwarps, int &cs);
 
 // Enqueue one decode launch over `tiles` 16-row tiles.
 cudaError_t launch_mv(MvParams &p, int mode, int bits, int tiles, cudaStream_t st);
