@@ -1,5 +1,5 @@
 // pgemm.cu - prompt-window GEMM over MLX affine 4/6/8-bit group-64 weights on the
-// sm_103a tensor cores (TMA -> in-SMEM exact dequant -> tcgen05.mma -> TMEM).
+// sm_103a tensor cores (TMA -> exact dequant into tensor memory -> tcgen05.mma).
 //
 // TensorFold PR #1696 (later revision), "What it adds" > "Prompt GEMM": prompt
 // windows take a GEMM that dequantizes the 4-bit weights as it loads each weight
@@ -7,24 +7,32 @@
 // order, so a row's sum does not depend on how the prompt is cut.
 //
 // For output Y[m][n] with 64-wide blocks b = 0..G-1:
-//   P_b[m][n] = sum_{j in b} X[m][j] * q[n][j]      tcgen05.mma, bf16 x bf16 -> fp32
-//               (codes converted exactly to bf16 in shared memory; fresh TMEM
-//                accumulator per block, double-buffered)
+//   P_b[n][m] = sum_{j in b} q[n][j] * X[m][j]      tcgen05.mma, bf16 x bf16 -> fp32
+//               A = codes of 128 weight rows converted exactly to bf16 and written
+//                   straight into tensor memory (tcgen05.st); B = the X tile, staged
+//                   by TMA in shared memory; fresh accumulator per block,
+//                   double-buffered in tensor memory
 //   y = fma(scale[n][b], P_b, y)  for b = 0..G-1 in order      (epilogue registers)
 //   Y = y + sum_b bias[n][b] * S_b[m]                            (added last)
 // with S_b[m] = sum_{j in b} X[m][j] computed by a pre-pass in fp32 and split
 // exactly into three bf16 parts, so the bias term is one more small tcgen05
 // contraction (k' = 3G) instead of a second fma per element and block.
+// The accumulator holds output channels in tensor-memory lanes, so an epilogue
+// thread owns one channel: one scale per block, and the 32 lanes of a warp store 32
+// consecutive channels of a row (coalesced).
 // Every quantity of row m depends only on X[m][:] and W: the tensor core computes
 // each output from its own row and column, tiles out of range are zero-filled by
 // TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
 //
-// Warp roles (one CTA per 128 x 128 output tile, 576 threads):
-//   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block)
+// Warp roles (one CTA per 128-channel x 128-row output tile, 576 threads):
+//   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block;
+//               scale and bias boxes)
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2-9   converters: packed codes -> bf16 (SWIZZLE_128B K-major), scales -> fp32
-//   warps 10-17 epilogue: TMEM -> registers, scale chain, bias add, store
-//               (two warps per TMEM lane quarter, 64 columns each)
+//   warps 2-9   converters: packed codes -> bf16 in tensor memory, scales -> fp32
+//               (a warp writes the tensor-memory lanes of its quarter; two warps per
+//               quarter, each half of a row)
+//   warps 10-17 epilogue: tensor memory -> registers, scale chain, bias add, store
+//               (two warps per lane quarter, 64 rows of X each)
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
 // QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -41,43 +49,45 @@ namespace qlk {
 
 namespace pg {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BM = 128;  // rows of X per tile (MMA N)
+constexpr int BN = 128;  // output channels per tile (MMA M, tensor-memory lanes)
 constexpr int BK = 64;
-constexpr int kStages = 4;   // TMA stages (X/S tile + packed W tile)
-constexpr int kBStages = 3;  // converted bf16 W tiles
-constexpr int kScStages = 8; // fp32 scale rows (deep enough to need no release barrier, see converters)
-constexpr int kConvWarps = 8;  // two per SM sub-partition; a thread converts half a row
-constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each owning half the columns
+constexpr int kScStages = 8;  // fp32 scale rows (deep enough to need no release barrier, see converters)
+constexpr int kConvWarps = 8;
+constexpr int kEpiWarps = 8;
 constexpr int kRoleWarps = 2;  // producer, MMA issuer
 constexpr int kThreads = (kRoleWarps + kConvWarps + kEpiWarps) * 32;
-constexpr int kConvBase = kRoleWarps * 32;                  // first converter thread
-constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;          // first epilogue warp
+constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kABytes = BM * BK * 2;
-constexpr int kBBytes = BN * BK * 2;
-constexpr int kTmemCols = 2 * BN;
+constexpr int kXBytes = BM * BK * 2;
+// tensor-memory columns: two accumulators of BM columns, kABufs A buffers of BK/2 columns
+constexpr int kABufs = 4;  // converted weight blocks the converters may run ahead of the MMA
+constexpr int kColAcc = 0;
+constexpr int kColA = 2 * BM;
+constexpr int kTmemCols = 512;
+static_assert(kColA + kABufs * (BK / 2) <= kTmemCols, "tensor memory budget");
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
-constexpr int kPf = 4;       // k blocks of scale/bias prefetch
-static_assert(kScStages > kBStages + 2, "scale ring must outlast the MMA/epilogue lag");
+constexpr int kPf = 4;       // k blocks of scale/bias prefetch (no-TMA path)
+static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
 
 template <int BITS> struct Cfg {
   static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
   static constexpr int kWBytes = BN * kRowBytes;         // packed W tile
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + kStages * kABytes;
-  static constexpr int kOffW = kOffB + kBStages * kBBytes;
+  // TMA stages in flight (X/S tile + packed W tile): as many as shared memory holds
+  static constexpr int kStages = BITS == 8 ? 7 : 8;
+  static constexpr int kOffX = 0;
+  static constexpr int kOffW = kOffX + kStages * kXBytes;
   static constexpr int kOffSc = kOffW + kStages * kWBytes;
   // biases of the tile's rows, bf16, boxes of 8 groups: [kBiasG / 8][BN][8]
   static constexpr int kOffBias = kOffSc + kScStages * BN * 4;
   // scale boxes streamed by TMA, bf16 [2][BN][8]
   static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
   static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
-  // barriers: tma_full, tma_empty, b_full, b_empty, acc_full[2], acc_empty[2], sc_full,
-  //           scb_full[2], scb_empty[2], bias_full, mma_done
-  static constexpr int kNumBars = 2 * kStages + 2 * kBStages + 4 + kScStages + 4 + 1 + 1;
+  // barriers: tma_full, tma_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
+  //           sc_full, scb_full[2], scb_empty[2], bias_full, mma_done
+  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -124,12 +134,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -140,38 +151,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
 
 __device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -180,6 +159,18 @@ __device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // (d0, d1) = (a0, a1) * (b0, b1) + (d0, d1), each rounded to nearest (packed fp32 fma)
 __device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
@@ -203,12 +194,6 @@ __device__ __forceinline__ uint2 lds64(const void *p) {
   return v;
 }
 
-__device__ __forceinline__ void sts128(void *p, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(p)), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-
 // bits [off, off + 32) of a little-endian array of 32-bit words (off is a constant
 // after unrolling; the word after the last is never needed for the fields used)
 template <int NW>
@@ -219,24 +204,21 @@ __device__ __forceinline__ uint32_t window32(const uint32_t (&w)[NW], int off) {
   return __funnelshift_r(w[i], hi, s);
 }
 
-// One packed row of one k block (64 codes) -> 8 chunks of 8 bf16 codes, chunk c
-// holding k = 8c .. 8c+7 in natural order.
+// Chunk c (8 codes, k = 8c .. 8c+7 of the held words) -> four bf16 pairs in k order.
 template <int BITS, int NW>
-__device__ __forceinline__ uint4 convert_chunk(const uint32_t (&w)[NW], int c) {
-  uint4 o;
+__device__ __forceinline__ void convert_chunk(const uint32_t (&w)[NW], int c, uint32_t *o) {
   if constexpr (BITS == 4) {
     const uint32_t x = w[c], x4 = x >> 4;
-    o.x = q4_pair(x, x4, 0); o.y = q4_pair(x, x4, 1); o.z = q4_pair(x, x4, 2); o.w = q4_pair(x, x4, 3);
+    o[0] = q4_pair(x, x4, 0); o[1] = q4_pair(x, x4, 1); o[2] = q4_pair(x, x4, 2); o[3] = q4_pair(x, x4, 3);
   } else if constexpr (BITS == 8) {
-    o.x = q8_pair(w[2 * c], 0); o.y = q8_pair(w[2 * c], 1);
-    o.z = q8_pair(w[2 * c + 1], 0); o.w = q8_pair(w[2 * c + 1], 1);
+    o[0] = q8_pair(w[2 * c], 0); o[1] = q8_pair(w[2 * c], 1);
+    o[2] = q8_pair(w[2 * c + 1], 0); o[3] = q8_pair(w[2 * c + 1], 1);
   } else {
-    o.x = q6_pair(window32(w, 48 * c));
-    o.y = q6_pair(window32(w, 48 * c + 12));
-    o.z = q6_pair(window32(w, 48 * c + 24));
-    o.w = q6_pair(window32(w, 48 * c + 36));
+    o[0] = q6_pair(window32(w, 48 * c));
+    o[1] = q6_pair(window32(w, 48 * c + 12));
+    o[2] = q6_pair(window32(w, 48 * c + 24));
+    o[3] = q6_pair(window32(w, 48 * c + 36));
   }
-  return o;
 }
 
 // ---- the GEMM kernel -------------------------------------------------------------
@@ -248,24 +230,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<BITS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sA = smem + C::kOffA;
-  uint8_t *sB = smem + C::kOffB;
+  uint8_t *sX = smem + C::kOffX;
   uint8_t *sW = smem + C::kOffW;
   float *sSc = reinterpret_cast<float *>(smem + C::kOffSc);
+  uint16_t *sbias = reinterpret_cast<uint16_t *>(smem + C::kOffBias);
+  uint16_t *scbox = reinterpret_cast<uint16_t *>(smem + C::kOffScBox);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint64_t *tma_full = bars;
-  uint64_t *tma_empty = tma_full + kStages;
-  uint64_t *b_full = tma_empty + kStages;
-  uint64_t *b_empty = b_full + kBStages;
-  uint64_t *acc_full = b_empty + kBStages;
+  uint64_t *tma_empty = tma_full + C::kStages;
+  uint64_t *a_full = tma_empty + C::kStages;
+  uint64_t *a_empty = a_full + kABufs;
+  uint64_t *acc_full = a_empty + kABufs;
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *sc_full = acc_empty + 2;
   uint64_t *scb_full = sc_full + kScStages;
   uint64_t *scb_empty = scb_full + 2;
   uint64_t *bias_full = scb_empty + 2;
   uint64_t *mma_done = bias_full + 1;
-  uint16_t *sbias = reinterpret_cast<uint16_t *>(smem + C::kOffBias);
-  uint16_t *scbox = reinterpret_cast<uint16_t *>(smem + C::kOffScBox);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -275,11 +256,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t budget = p.budget_ns;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(&tma_full[i], 1); mbar_init(&tma_empty[i], 1 + kConvThreads); }
-    for (int i = 0; i < kBStages; ++i) { mbar_init(&b_full[i], kConvThreads); mbar_init(&b_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kEpiThreads); }
+    for (int i = 0; i < C::kStages; ++i) { mbar_init(&tma_full[i], 1); mbar_init(&tma_empty[i], 1 + kConvThreads); }
+    for (int i = 0; i < kABufs; ++i) {
+      mbar_init(&a_full[i], kConvThreads);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiThreads);
+      mbar_init(&scb_full[i], 1);
+      mbar_init(&scb_empty[i], kConvThreads);
+    }
     for (int i = 0; i < kScStages; ++i) mbar_init(&sc_full[i], kConvThreads);
-    for (int i = 0; i < 2; ++i) { mbar_init(&scb_full[i], 1); mbar_init(&scb_empty[i], kConvThreads); }
     mbar_init(bias_full, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -311,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int issued = 0;
       if (p.bi_tma) {
-        // every bias of the tile's rows, once (read only by the bias blocks at the end)
+        // every bias of the tile's channels, once (read only by the bias blocks at the end)
         const int nbox = (G + 7) / 8;
         mbar_arrive_expect_tx(bias_full, (uint32_t)(nbox * BN * 16));
         for (int i = 0; i < nbox; ++i) tma_load_2d(sbias + i * BN * 8, &tmBi, bias_full, 8 * i, n0);
@@ -319,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int sc_boxes = 0;
       for (int kb = 0; kb < KB; ++kb) {
         if (p.sc_tma && kb < G && (kb & 7) == 0) {
-          // scales of blocks kb .. kb+7 for the tile's rows, two boxes in flight
+          // scales of blocks kb .. kb+7 for the tile's channels, two boxes in flight
           const int j = kb >> 3, slot = j & 1;
           if (!mbar_wait_bounded(&scb_empty[slot], ((uint32_t)(j >> 1) & 1u) ^ 1u, budget, abort_flag)) {
             give_up();
@@ -329,39 +317,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(scbox + slot * BN * 8, &tmSc, &scb_full[slot], kb, n0);
           sc_boxes = j + 1;
         }
-        const int s = kb % kStages;
-        const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+        const int s = kb % C::kStages;
+        const uint32_t ph = (uint32_t)(kb / C::kStages) & 1u;
         if (!mbar_wait_bounded(&tma_empty[s], ph ^ 1u, budget, abort_flag)) { give_up(); break; }
         if (kb < G) {
-          mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kABytes + C::kWBytes));
-          tma_load_2d(sA + s * kABytes, &tmX, &tma_full[s], kb * BK, m0);
+          mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
+          tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
           tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
         } else {
-          mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kABytes);
-          tma_load_2d(sA + s * kABytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
+          mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kXBytes);
+          tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
         }
         issued = kb + 1;
       }
-      // drain the scale and bias boxes too
+      // drain: every copy this CTA started must land before its shared memory goes away
       for (int j = (sc_boxes > 2 ? sc_boxes - 2 : 0); j < sc_boxes; ++j)
         (void)mbar_wait_bounded(&scb_full[j & 1], (uint32_t)(j >> 1) & 1u, kDrainBudgetNs, nullptr);
       if (p.bi_tma) (void)mbar_wait_bounded(bias_full, 0u, kDrainBudgetNs, nullptr);
-      // drain: every copy this CTA started must land before its shared memory goes away
-      for (int s = 0; s < kStages && s < issued; ++s) {
-        const int uses = (issued - 1 - s) / kStages + 1;
+      for (int s = 0; s < C::kStages && s < issued; ++s) {
+        const int uses = (issued - 1 - s) / C::kStages + 1;
         (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      constexpr uint32_t idesc = idesc_bf16(BN, BM);
       bool any = false;
       for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % kStages, sb = kb % kBStages;
+        const int s = kb % C::kStages, ab = kb % kABufs;
         const int a = kb < G ? kb : G;
-        if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / kStages) & 1u, budget, abort_flag)) { give_up(); break; }
-        if (!mbar_wait_bounded(&b_full[sb], (uint32_t)(kb / kBStages) & 1u, budget, abort_flag)) { give_up(); break; }
+        if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / C::kStages) & 1u, budget, abort_flag)) { give_up(); break; }
+        if (!mbar_wait_bounded(&a_full[ab], (uint32_t)(kb / kABufs) & 1u, budget, abort_flag)) { give_up(); break; }
         if (kb <= G) {
           if (!mbar_wait_bounded(&acc_empty[a & 1], ((uint32_t)(a >> 1) & 1u) ^ 1u, budget, abort_flag)) {
             give_up();
@@ -369,17 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)((a & 1) * BN);
-        const uint64_t ad = sw128_desc(smem_addr(sA + s * kABytes));
-        const uint64_t bd = sw128_desc(smem_addr(sB + sb * kBBytes));
+        const uint32_t d = tmem_base + (uint32_t)(kColAcc + (a & 1) * BM);
+        const uint32_t at = tmem_base + (uint32_t)(kColA + ab * (BK / 2));
+        const uint64_t bd = sw128_desc(smem_addr(sX + s * kXBytes));
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint32_t acc = (kk > 0 || kb > G) ? 1u : 0u;
-          mma_bf16(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
+          mma_bf16_ts(d, at + (uint32_t)(8 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
         }
         any = true;
         mma_commit(&tma_empty[s]);
-        mma_commit(&b_empty[sb]);
+        mma_commit(&a_empty[ab]);
         if (kb < G || kb == KB - 1) mma_commit(&acc_full[a & 1]);
       }
       if (any) {
@@ -389,18 +376,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ converters
-    const int cthr = threadIdx.x - kConvBase;  // 0..255
-    const int ct = cthr & (BN - 1);      // row of the W tile
-    const int chalf = cthr >> 7;         // chunks 4*chalf .. 4*chalf+3 of the row
-    const bool lead = chalf == 0;        // the thread that also moves the row's scale and bias
+    const int q = warp & 3;                         // tensor-memory lane quarter of this warp
+    const int chalf = (warp - kRoleWarps) >> 2;     // half of the row: chunks 4*chalf .. 4*chalf+3
+    const int ct = 32 * q + lane;                   // channel (row of the W tile) = tensor-memory lane
+    const bool lead = chalf == 0;                   // also moves the channel's scale and bias
+    const uint32_t a_lane = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(kColA + 16 * chalf);
     const int n = n0 + ct;
     const bool nvalid = n < p.N;
     const uint16_t *srow = p.scales + (size_t)(nvalid ? n : 0) * G;
     const uint16_t *brow = p.biases + (size_t)(nvalid ? n : 0) * G;
     const bool bias_smem = G <= kBiasG;
-    // Without TMA boxes (k % 512 != 0), the lead thread loads its row's scale and bias
-    // itself, kPf blocks ahead; the loop is unrolled by kPf so that each ring slot
-    // stays in place while its load is in flight.
+    // Without TMA boxes (k % 512 != 0), the lead thread loads its channel's scale and
+    // bias itself, kPf blocks ahead; the loop is unrolled by kPf so that each ring
+    // slot stays in place while its load is in flight.
     uint32_t sr[kPf], br[kPf];
 #pragma unroll
     for (int i = 0; i < kPf; ++i) {
@@ -413,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < kPf; ++u) {
         const int kb = kb0 + u;
         if (kb >= KB || !alive) break;
-        const int s = kb % kStages, sb = kb % kBStages;
+        const int s = kb % C::kStages, ab = kb % kABufs;
         uint32_t s_cur = 0u, b_cur = 0u;
         if (kb < G) {
           if (!p.sc_tma) {
@@ -435,14 +423,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             br[u] = (lead && nvalid && kb + kPf < G) ? ldg_u16(brow + kb + kPf) : 0u;
           }
         }
-        if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / kStages) & 1u, budget, abort_flag) ||
-            !mbar_wait_bounded(&b_empty[sb], ((uint32_t)(kb / kBStages) & 1u) ^ 1u, budget, abort_flag)) {
+        if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / C::kStages) & 1u, budget, abort_flag) ||
+            !mbar_wait_bounded(&a_empty[ab], ((uint32_t)(kb / kABufs) & 1u) ^ 1u, budget, abort_flag)) {
           give_up();
           alive = false;
           break;
         }
-        uint8_t *brow_s = sB + sb * kBBytes + ct * 128;
-        const int sw = ct & 7;
+        tc_fence_after();
+        uint32_t o[16];
         if (kb < G) {
           constexpr int NW = BK * BITS / 64;  // words of half a row
           uint32_t w[NW];
@@ -461,59 +449,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int cc = 4 * chalf + c;
-            sts128(brow_s + ((cc ^ sw) << 4), convert_chunk<BITS, NW>(w, c));
-          }
+          for (int c = 0; c < 4; ++c) convert_chunk<BITS, NW>(w, c, o + 4 * c);
           if (lead && !p.bi_tma && bias_smem) sbias[((kb >> 3) * BN + ct) * 8 + (kb & 7)] = (uint16_t)b_cur;
           // Scale slot kb % kScStages was last read by the epilogue for block
-          // kb - kScStages.  Passing b_empty for this block means the MMA of block
-          // kb - kBStages finished, which waited for the epilogue to release block
-          // kb - kBStages - 2; kScStages > kBStages + 2 keeps the slot free.
+          // kb - kScStages.  Passing a_empty for this block means the MMA of block
+          // kb - kABufs finished, which waited for the epilogue to release block
+          // kb - kABufs - 2; kScStages >= kABufs + 3 keeps the slot free.
           if (lead) sSc[(kb % kScStages) * BN + ct] = bf16_to_f32(s_cur);
-          fence_proxy_async();
-          mbar_arrive(&b_full[sb]);
-          mbar_arrive(&sc_full[kb % kScStages]);
-          mbar_arrive(&tma_empty[s]);
         } else {
           // bias block: column t of block jb is k' = 64*jb + t of the [part][group]
-          // layout; its B value is bias[n][k' mod G] (zero past 3G)
+          // layout; its A value is bias[n][k' mod G] (zero past 3G)
           if (kb == G && p.bi_tma && !mbar_wait_bounded(bias_full, 0u, budget, abort_flag)) {
             give_up();
             alive = false;
             break;
           }
-          const int base = (kb - G) * BK;
+          const int base = (kb - G) * BK + 32 * chalf;
 #pragma unroll
-          for (int c = 4 * chalf; c < 4 * chalf + 4; ++c) {
-            uint32_t h[8];
+          for (int e = 0; e < 16; ++e) {
+            uint32_t h2[2];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              int j = base + 8 * c + e;
+            for (int hh = 0; hh < 2; ++hh) {
+              int j = base + 2 * e + hh;
               uint32_t v = 0u;
               if (nvalid && j < 3 * G) {
                 if (j >= G) j -= G;
                 if (j >= G) j -= G;
                 v = bias_smem ? (uint32_t)sbias[((j >> 3) * BN + ct) * 8 + (j & 7)] : ldg_u16(brow + j);
               }
-              h[e] = v;
+              h2[hh] = v;
             }
-            uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-            sts128(brow_s + ((c ^ sw) << 4), o);
+            o[e] = h2[0] | (h2[1] << 16);
           }
-          fence_proxy_async();
-          mbar_arrive(&b_full[sb]);
-          mbar_arrive(&tma_empty[s]);
         }
+        tmem_st16(a_lane + (uint32_t)(ab * (BK / 2)), o);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&a_full[ab]);
+        if (kb < G) mbar_arrive(&sc_full[kb % kScStages]);
+        mbar_arrive(&tma_empty[s]);
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    constexpr int CW = BN / 2;  // columns owned by one thread
-    const int q = warp & 3;     // TMEM lane quarter this warp may access
+    constexpr int CW = BM / 2;  // rows of X owned by one thread
+    const int q = warp & 3;     // tensor-memory lane quarter this warp may access
     const int half = (warp - kEpiWarp0) / 4;
-    const int row = 32 * q + lane;
-    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(half * CW);
+    const int ch_row = 32 * q + lane;  // output channel of this thread within the tile
+    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(kColAcc + half * CW);
     float y[CW];
 #pragma unroll
     for (int i = 0; i < CW; ++i) y[i] = 0.0f;
@@ -528,23 +511,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const float4 *sc4 = reinterpret_cast<const float4 *>(sSc + sc * BN + half * CW);
+      const float sv = sSc[sc * BN + ch_row];
       // 8-column chunks; the next chunk's TMEM load is in flight while one is used
       uint32_t ra[8], rb[8];
-      tmem_ld8_nowait(lane_base + (uint32_t)(buf * BN), ra);
+      tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM), ra);
       tmem_wait_ld();
 #pragma unroll
       for (int ch = 0; ch < CW / 8; ++ch) {
         uint32_t(&cur)[8] = (ch & 1) ? rb : ra;
         uint32_t(&nxt)[8] = (ch & 1) ? ra : rb;
-        if (ch + 1 < CW / 8) tmem_ld8_nowait(lane_base + (uint32_t)(buf * BN + 8 * (ch + 1)), nxt);
+        if (ch + 1 < CW / 8) tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * (ch + 1)), nxt);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float4 s4 = sc4[2 * ch + i];
-          float *yy = &y[8 * ch + 4 * i];
-          ffma2(yy[0], yy[1], s4.x, s4.y, __uint_as_float(cur[4 * i]), __uint_as_float(cur[4 * i + 1]));
-          ffma2(yy[2], yy[3], s4.z, s4.w, __uint_as_float(cur[4 * i + 2]), __uint_as_float(cur[4 * i + 3]));
-        }
+        for (int i = 0; i < 4; ++i)
+          ffma2(y[8 * ch + 2 * i], y[8 * ch + 2 * i + 1], sv, sv, __uint_as_float(cur[2 * i]),
+                __uint_as_float(cur[2 * i + 1]));
         if (ch + 1 < CW / 8) tmem_wait_ld();
       }
       tc_fence_before();
@@ -561,27 +541,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int buf = G & 1;
 #pragma unroll
-      for (int j = 0; j < CW / 16; ++j) {
-        uint32_t r[16];
-        tmem_ld16(lane_base + (uint32_t)(buf * BN + 16 * j), r);
+      for (int ch = 0; ch < CW / 8; ++ch) {
+        uint32_t r[8];
+        tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * ch), r);
+        tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[16 * j + i] = __fadd_rn(y[16 * j + i], __uint_as_float(r[i]));
+        for (int i = 0; i < 8; ++i) y[8 * ch + i] = __fadd_rn(y[8 * ch + i], __uint_as_float(r[i]));
       }
       tc_fence_before();
-      const int m = m0 + row;
-      const int nb = n0 + half * CW;
-      if (m < p.M) {
-        float *yrow = p.Y + (size_t)m * p.ldy + nb;
-        const bool vec = (nb + CW <= p.N) && ((reinterpret_cast<uintptr_t>(yrow) & 15u) == 0);
-        if (vec) {
+      // one channel per thread: lanes of a warp write 32 consecutive channels of a row
+      const int n = n0 + ch_row;
+      if (n < p.N) {
+        const int mb = m0 + half * CW;
+        float *ycol = p.Y + (size_t)mb * p.ldy + n;
 #pragma unroll
-          for (int i = 0; i < CW / 4; ++i)
-            reinterpret_cast<float4 *>(yrow)[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < CW; ++i)
-            if (nb + i < p.N) yrow[i] = y[i];
-        }
+        for (int i = 0; i < CW; ++i)
+          if (mb + i < p.M) ycol[(size_t)i * p.ldy] = y[i];
       }
     }
   }

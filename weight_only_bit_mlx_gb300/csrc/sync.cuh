@@ -1,9 +1,9 @@
 // sync.cuh - shared-memory barrier helpers with bounded waits (sm_103a).
 //
-// Every wait in the library's kernels goes through mbar_wait_bounded(): it polls
-// with mbarrier.try_wait (which itself suspends the thread for a short, hardware-
-// chosen time) and gives up once `budget_ns` of %globaltimer time has passed, or
-// when another warp of the CTA has already given up (shared abort flag).  A kernel
+// Every wait in the library's kernels goes through mbar_wait_bounded(): it sleeps in
+// mbarrier.try_wait with a suspend-time hint (the thread wakes when the phase
+// completes) and gives up once `budget_ns` of %globaltimer time has passed, or when
+// another warp of the CTA has already given up (shared abort flag).  A kernel
 // whose wait gives up records QL_ERR_TIMEOUT in the status word and returns; no
 // wait in this library can spin forever.
 #pragma once
@@ -44,29 +44,42 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+__device__ __forceinline__ bool mbar_test_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(addr), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
+// Suspends the thread until the phase completes or about kSuspendNs have passed.
+constexpr uint32_t kSuspendNs = 100000;
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the barrier's phase with parity `parity` has completed.  Returns false
 // (without having waited for it) if the budget ran out or *abort became nonzero.
+// A completed phase costs one non-blocking test; otherwise the thread sleeps in
+// mbarrier.try_wait (woken when the phase completes) instead of spinning, so waiting
+// warps take no issue slots from the warps doing work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t budget_ns,
                                                   const volatile int *abort) {
   const uint32_t addr = smem_addr(bar);
-  if (mbar_try_wait(addr, parity)) return true;
+  if (mbar_test_wait(addr, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(addr, parity)) return true;
-    if ((it & 15u) == 0u) {
-      if (abort != nullptr && *abort != 0) return false;
-      if (globaltimer_ns() - t0 > budget_ns) return false;
-    }
+    if (abort != nullptr && *abort != 0) return false;
+    if (globaltimer_ns() - t0 > budget_ns) return false;
   }
 }
 
