@@ -90,6 +90,18 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t w, uint32_t w4, int t) {
   return fma_bf16x2(v, kBf16One2, kBf16Neg128x2);
 }
 
+// 4-bit, offset form: codes t and t+4 of word w (t = 0..3) as the bf16 pair
+// (1 + q_t/16, 1 + q_{t+4}/16).  A bf16 in [1, 2) has a unit in the last place of
+// 2^-7, so a 4-bit code placed in mantissa bits 3..6 of 1.0 gives 1 + q/16 exactly;
+// one shift and one mask-or per pair, no arithmetic.  A dot product with these
+// values is S + P/16 (S = sum of the activations, P = sum q*x), so
+// sum (s*q + b) x = 16s * dot + (b - 16s) * S.
+constexpr uint32_t kBf16One2Mask4 = 0x00780078u;  // mantissa bits 3..6 of both halves
+__device__ __forceinline__ uint32_t q4_off_pair(uint32_t w, int t) {
+  const uint32_t v = t == 0 ? (w << 3) : (w >> (4 * t - 3));
+  return (v & kBf16One2Mask4) | kBf16One2;
+}
+
 // 6-bit: a 12-bit field f (two 6-bit codes, lower code in bits 0..5)
 __device__ __forceinline__ uint32_t q6_pair(uint32_t f) {
   uint32_t v = (f & 0x3Fu) | ((f << 10) & 0x003F0000u) | kBf16Magic2;
@@ -114,10 +126,12 @@ __device__ __forceinline__ uint32_t bits96_at(uint32_t w0, uint32_t w1, uint32_t
   return w2 >> (off - 64);
 }
 
-// D = A(16x16 bf16, row) * B(16x8 bf16, col) + C, fp32 accumulate
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + C, fp32 accumulate.  A pure function
+// of its registers (not volatile), so the compiler may interleave independent MMAs
+// with the loads and conversions of other groups.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                                uint32_t b1, const float (&c)[4]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])

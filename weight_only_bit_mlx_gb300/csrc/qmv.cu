@@ -9,21 +9,27 @@
 // Work decomposition (a function of k and bits only, never of the number of rows R,
 // of n or of the fused/unfused choice):
 //   * a CTA owns a 16-row tile of W (both w1 and w3 in the fused FFN) and a k-span;
-//     CTAs of a cluster split k into spans, a span is processed in chunks of
-//     span_g<BITS>() groups (2048 k for 4-bit, 1024 k for 6/8-bit);
-//   * each of the 4 warps owns Geo::kGpw consecutive groups of the chunk.  Its lanes
-//     start one bulk copy (cp.async.bulk) per weight row of the slice - contiguous
-//     runs of 192-256 bytes straight from HBM into shared memory, so the weight
-//     stream leaves the SM as few large requests, all issued at kernel start;
-//   * scales and biases are staged in shared memory as fp32; activations (the only
-//     input a preceding kernel may write) are bulk-copied in after
-//     griddepcontrol.wait, so with programmatic dependent launch the weight stream of
-//     this kernel overlaps the tail of the previous one;
-//   * per group the codes are converted exactly to bf16 and multiplied on the tensor
-//     cores with mma.sync m16n8k16 (rows of W as A, activation rows as B):
-//       P_g = sum_{j in g} q_j x_j      (fresh fp32 accumulator per group)
-//       S_g = sum_{j in g} x_j          (same MMA with A = 1)
-//       y   = fma(scale_g, P_g, y);  y = fma(bias_g, S_g, y)   (groups in order)
+//     CTAs of a cluster split k into spans;
+//   * the span is cut into kNch chunks of kGpc groups; a copy warp starts, chunk by
+//     chunk, one bulk copy (cp.async.bulk) per weight row of the chunk, straight
+//     from HBM into shared memory, each chunk completing its own mbarrier, so the
+//     compute warps start on chunk 0 while later chunks are still streaming in and
+//     the weight stream leaves the SM as large requests issued at kernel start;
+//   * scales and biases go in by bulk copy with chunk 0 (one copy for the whole tile
+//     when a CTA spans the full k), activations (the only input a preceding kernel
+//     may write) are loaded by the compute warps after griddepcontrol.wait, so with
+//     programmatic dependent launch the weight stream of this kernel overlaps the
+//     tail of the previous one;
+//   * compute warp w owns kGpw consecutive groups of every chunk.  Per group the
+//     codes are converted exactly to bf16 and multiplied on the tensor cores with
+//     mma.sync m16n8k16 (rows of W as A, activation rows as B), a fresh fp32
+//     accumulator per group, and the affine step follows in group order:
+//       6/8-bit:  P_g = sum_{j in g} q_j x_j;          y = fma(s, P_g, y); y = fma(b, S_g, y)
+//       4-bit:    D_g = sum_{j in g} (1 + q_j/16) x_j; y = fma(16s, D_g, y); y = fma(b - 16s, S_g, y)
+//     (the 4-bit codes go into the mantissa of 1.0, two instructions per bf16 pair;
+//     D_g = S_g + P_g/16, so both forms are s*P_g + b*S_g).  S_g = sum_{j in g} x_j
+//     is computed once per activation row and group while the activations are
+//     staged, in a fixed order;
 //   * warp partials are added in warp order through shared memory, CTA partials in
 //     rank order through distributed shared memory.  No atomics, no scratch memory.
 // The tensor core computes every output column (activation row) from that column's
@@ -39,16 +45,20 @@ namespace cg = cooperative_groups;
 namespace qlk {
 
 template <int BITS> struct Geo;
+#ifndef QL_MV_NCH
+#define QL_MV_NCH 1
+#endif
+constexpr int kNch = QL_MV_NCH;  // chunks per span (one mbarrier each)
 template <> struct Geo<4> {
-  static constexpr int kLw = 2;     // words per lane per row per group
-  static constexpr int kGpw = 8;    // groups per warp slice
+  static constexpr int kLw = 2;             // words per lane per row per group
+  static constexpr int kGpw = 8 / kNch;     // groups per compute warp per chunk
 };
-template <> struct Geo<6> { static constexpr int kLw = 3; static constexpr int kGpw = 4; };
-template <> struct Geo<8> { static constexpr int kLw = 4; static constexpr int kGpw = 4; };
-template <int BITS> __host__ __device__ constexpr int gbytes() { return 8 * BITS; }                           // bytes per row per group
-template <int BITS> __host__ __device__ constexpr int span_g() { return kMvWarps * Geo<BITS>::kGpw; }          // groups per chunk
+template <> struct Geo<6> { static constexpr int kLw = 3; static constexpr int kGpw = 4 / kNch; };
+template <> struct Geo<8> { static constexpr int kLw = 4; static constexpr int kGpw = 4 / kNch; };
+template <int BITS> __host__ __device__ constexpr int gbytes() { return 8 * BITS; }                  // bytes per row per group
+template <int BITS> __host__ __device__ constexpr int gpc() { return kMvWarps * Geo<BITS>::kGpw; }  // groups per chunk
+template <int BITS> __host__ __device__ constexpr int span_g() { return kNch * gpc<BITS>(); }        // groups per span
 template <int BITS> __host__ __device__ constexpr int wpitch() { return span_g<BITS>() * gbytes<BITS>() + 32; }  // padded row pitch
-__host__ __device__ constexpr int xpitch(int sg) { return sg * 64 + 8; }                                       // bf16 elements
 
 int mv_span_g(int bits) { return bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6>() : span_g<8>()); }
 
@@ -58,15 +68,15 @@ int mv_span_g(int bits) { return bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6
 // fragments use the same mapping, so they are plain 16-byte reads of x.
 template <int BITS>
 __device__ __forceinline__ void lds_lane_words(const uint8_t *p, uint32_t (&w)[Geo<BITS>::kLw]) {
-  const uint32_t a = smem_addr(p);
   if constexpr (BITS == 4) {
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(a));
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    w[0] = v.x; w[1] = v.y;
   } else if constexpr (BITS == 8) {
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(a));
+    const uint4 v = *reinterpret_cast<const uint4 *>(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
   } else {
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(a));
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[1]) : "r"(a + 4));
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[2]) : "r"(a + 8));
+    const uint32_t *q = reinterpret_cast<const uint32_t *>(p);
+    w[0] = q[0]; w[1] = q[1]; w[2] = q[2];
   }
 }
 
@@ -89,14 +99,6 @@ __device__ __forceinline__ uint32_t u4get(const uint4 &v, int j) {
   return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-__device__ __forceinline__ uint4 lds_v4(const void *p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_addr(p)));
-  return v;
-}
-
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_addr(dst)),
@@ -104,51 +106,70 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                : "memory");
 }
 
+constexpr int kMvThreads = (kMvWarps + 1) * 32;  // compute warps + one copy warp
+constexpr int kMvComputeThreads = kMvWarps * 32;
+constexpr int kBarCompute = 1;                   // named barrier of the compute warps
+constexpr uint64_t kMvDrainNs = 2000000000ull;
+
 // Shared-memory layout of one CTA (dynamic, 128-byte aligned):
-//   wsm [NMAT][16][wpitch]                   weight rows of the chunk (one bulk copy per row)
-//   sbs [NMAT][2][16][span] bf16             scales, biases of the chunk
-//   red [kMvWarps][NV][32] fp32              warp partials
-//   csum[NV][32] fp32                        CTA partial (read by cluster rank 0)
-//   bars[2]                                  weights+scales barrier, activation barrier
-//   xs  [rows][xpitch] bf16                  activations of the chunk
+//   wsm [NMAT][16][wpitch]             weight rows of the span (one bulk copy per row and chunk);
+//                                      after the last group it holds the warp partials
+//                                      red[kMvWarps][NV][32] and the CTA partial csum[NV][32]
+//   sbf [NMAT][span][16] float2        per (group, row): (16s, b - 16s) for 4-bit, (s, b) else
+//   bars[kNch]                         one per chunk
+// Activations never pass through shared memory: each lane loads the 16-byte pieces
+// its MMA fragments take straight from global memory (L1/L2).
 template <int BITS, int NB, int MODE> struct MvLayout {
   static constexpr int NMAT = (MODE == kMvFfn) ? 2 : 1;
   static constexpr int NV = NMAT * NB * 4;
   static constexpr int kW = 0;
-  static constexpr int kSb = kW + NMAT * 16 * wpitch<BITS>();
-  static constexpr int kRed = kSb + NMAT * 2 * 16 * span_g<BITS>() * 2;
-  static constexpr int kCsum = kRed + kMvWarps * NV * 32 * 4;
-  static constexpr int kBar = kCsum + NV * 32 * 4;
-  static constexpr int kX = ((kBar + 2 * 8) + 127) / 128 * 128;
-  static int bytes(int rows) { return kX + rows * xpitch(span_g<BITS>()) * 2; }
+  static constexpr int kWBytes = NMAT * 16 * wpitch<BITS>();
+  static constexpr int kRed = 0;                                // aliases wsm
+  static constexpr int kCsum = kRed + kMvWarps * NV * 32 * 4;   // aliases wsm
+  static_assert(kCsum + NV * 32 * 4 <= kWBytes, "partials must fit in the weight area");
+  static constexpr int kSbf = kWBytes;
+  static constexpr int kBar = kSbf + NMAT * span_g<BITS>() * 16 * 8;
+  static constexpr int kBytes = kBar + kNch * 8;
 };
 
+// activation fragment of lane (g4, c) for one group: x[row][64g + 16c .. +16) as two
+// 16-byte pieces; 4-bit takes each 8-value block in the order x0 x4 x1 x5 x2 x6 x3 x7
+template <bool kOff>
+__device__ __forceinline__ void load_x_frag(const uint16_t *px, uint4 &a, uint4 &b) {
+  a = ldg_v4(px);
+  b = ldg_v4(px + 8);
+  if constexpr (kOff) {
+    a = make_uint4(__byte_perm(a.x, a.z, 0x5410), __byte_perm(a.x, a.z, 0x7632), __byte_perm(a.y, a.w, 0x5410),
+                   __byte_perm(a.y, a.w, 0x7632));
+    b = make_uint4(__byte_perm(b.x, b.z, 0x5410), __byte_perm(b.x, b.z, 0x7632), __byte_perm(b.y, b.w, 0x5410),
+                   __byte_perm(b.y, b.w, 0x7632));
+  }
+}
+
 template <int BITS, int NB, int MODE>
-__global__ void __launch_bounds__(kMvWarps * 32) qmv_kernel(const __grid_constant__ MvParams p) {
+__global__ void __launch_bounds__(kMvThreads) qmv_kernel(const __grid_constant__ MvParams p) {
   using Lay = MvLayout<BITS, NB, MODE>;
   constexpr int NMAT = Lay::NMAT;
   constexpr int NV = Lay::NV;
   constexpr int LW = Geo<BITS>::kLw;
   constexpr int GPW = Geo<BITS>::kGpw;
+  constexpr int GPC = gpc<BITS>();
   constexpr int SPAN = span_g<BITS>();
   constexpr int GB = gbytes<BITS>();
   constexpr int WP = wpitch<BITS>();
-  constexpr int XP = xpitch(SPAN);
+  constexpr bool kOff = BITS == 4;  // offset-form conversion (1 + q/16)
   extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t *sbs = reinterpret_cast<uint16_t *>(smem + Lay::kSb);
+  float2 *sbf = reinterpret_cast<float2 *>(smem + Lay::kSbf);
   float *red = reinterpret_cast<float *>(smem + Lay::kRed);
   float *csum = reinterpret_cast<float *>(smem + Lay::kCsum);
-  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
-  uint64_t *xbar = wbar + 1;
-  uint16_t *xs = reinterpret_cast<uint16_t *>(smem + Lay::kX);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
+  uint8_t *wsm = smem + Lay::kW;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = p.cs > 1 ? (int)cluster.block_rank() : 0;
   const int tile_g = blockIdx.x / p.cs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
   const int g4 = lane >> 2, c = lane & 3;
-  uint8_t *wsm = smem + Lay::kW;
 
   int mi = 0, tile = tile_g;
   if constexpr (MODE == kMvAttn) {
@@ -158,168 +179,213 @@ __global__ void __launch_bounds__(kMvWarps * 32) qmv_kernel(const __grid_constan
   const int n = p.m[mi].n;
   const size_t row_bytes = (size_t)p.groups * GB;
 
-  // this CTA's k-span: groups [gs0, gs1), in chunks of SPAN groups
+  // this CTA's k-span: groups [gs0, gs1), in spans of SPAN groups
   const int gs0 = rank * p.span_g, gs1 = min(p.groups, gs0 + p.span_g);
 
   if (threadIdx.x == 0) {
-    mbar_init(wbar, 1);
-    mbar_init(xbar, 1);
+    for (int i = 0; i < kNch; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
 
   float y[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) y[i] = 0.0f;
   const uint32_t ones[4] = {kBf16One2, kBf16One2, kBf16One2, kBf16One2};
   uint32_t phase = 0;
+  bool ok = true;
+  int armed = 0;  // chunks of the last span whose copies were started (copy warp)
 
   for (int ch0 = gs0; ch0 < gs1; ch0 += SPAN) {
     const int ch1 = min(gs1, ch0 + SPAN);
-    const int gw0 = ch0 + warp * GPW;  // this warp's slice
-    const int gcnt = max(0, min(GPW, ch1 - gw0));
-    // ---- 1. weights (and, with 16-byte aligned rows, scales and biases) of the
-    //         chunk: warp 0 starts one bulk copy per row, HBM -> smem, at once
-    const int cg_n = ch1 - ch0;
-    if (warp == 0) {
+    const int ng = ch1 - ch0;
+    if (warp == kMvWarps) {
+      // ---- copy warp: chunk by chunk, one bulk copy per weight row of the chunk
       const int t = lane >> 4, r = lane & 15;
       const int row = tile * 16 + r;
       const bool mine = lane < NMAT * 16 && row < n;
-      const uint32_t wb = (uint32_t)(cg_n * GB), sbb = (uint32_t)(cg_n * 2);
-      uint32_t bytes = mine ? wb + (p.sb_bulk ? 2u * sbb : 0u) : 0u;
+      if (ch0 != gs0 && lane == 0) {
+        // the previous span's copies have landed (its consumers waited for them, unless
+        // a wait gave up) before this span's copies reuse the buffers and barriers
+        for (int cc = 0; cc < armed; ++cc) (void)mbar_wait_bounded(&bars[cc], phase ^ 1u, kMvDrainNs, nullptr);
+        fence_proxy_async_smem();
+      }
+      armed = 0;
+      for (int cc = 0; cc < kNch; ++cc) {
+        const int ga = ch0 + cc * GPC;
+        if (ga >= ch1) break;
+        const int gb = min(ch1, ga + GPC);
+        const uint32_t wb = (uint32_t)((gb - ga) * GB);
+        uint32_t bytes = mine ? wb : 0u;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-      if (lane == 0) {
-        if (ch0 != gs0) fence_proxy_async_smem();
-        mbar_arrive_expect_tx(wbar, bytes);
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[cc], bytes);
+        __syncwarp();
+        if (mine) {
+          const uint8_t *src = reinterpret_cast<const uint8_t *>(p.m[mi + t].wq) + (size_t)row * row_bytes +
+                               (size_t)ga * GB;
+          bulk_g2s(wsm + (t * 16 + r) * WP + (ga - ch0) * GB, src, wb, &bars[cc]);
+        }
+        armed = cc + 1;
       }
-      __syncwarp();
-      if (mine) {
-        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.m[mi + t].wq) + (size_t)row * row_bytes +
-                             (size_t)ch0 * GB;
-        bulk_g2s(wsm + (t * 16 + r) * WP, src, wb, wbar);
-        if (p.sb_bulk) {
-          const size_t off = (size_t)row * p.groups + ch0;
-          bulk_g2s(sbs + ((t * 2 + 0) * 16 + r) * SPAN, p.m[mi + t].s + off, sbb, wbar);
-          bulk_g2s(sbs + ((t * 2 + 1) * 16 + r) * SPAN, p.m[mi + t].b + off, sbb, wbar);
+    } else {
+      // ---- compute warps
+      const int tid = threadIdx.x;  // 0 .. kMvComputeThreads-1
+      // Scales and biases of the span (not written by a preceding kernel, so read
+      // before the dependency wait) -> fp32 factor pairs.  16-byte vectors of 8
+      // groups when the rows allow it, else one value at a time.
+      if (p.sb_bulk) {
+        const int v8 = ng >> 3;  // vectors per row
+        for (int e = tid; e < NMAT * 16 * v8; e += kMvComputeThreads) {
+          const int t = e / (16 * v8), rr = (e / v8) % 16, v = e % v8;
+          const int row = tile * 16 + rr;
+          uint4 sv = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
+          if (row < n) {
+            const size_t off = (size_t)row * p.groups + ch0 + 8 * v;
+            sv = ldg_v4(p.m[mi + t].s + off);
+            bv = ldg_v4(p.m[mi + t].b + off);
+          }
+          const uint32_t ss[4] = {sv.x, sv.y, sv.z, sv.w}, bb[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+          for (int q2 = 0; q2 < 8; ++q2) {
+            const float s1 = bf16_to_f32((ss[q2 >> 1] >> (16 * (q2 & 1))) & 0xFFFFu);
+            const float b1 = bf16_to_f32((bb[q2 >> 1] >> (16 * (q2 & 1))) & 0xFFFFu);
+            float2 f;
+            if constexpr (kOff) f = make_float2(s1 * 16.0f, __fsub_rn(b1, s1 * 16.0f));
+            else f = make_float2(s1, b1);
+            sbf[(t * SPAN + 8 * v + q2) * 16 + rr] = f;
+          }
+        }
+      } else {
+        for (int e = tid; e < NMAT * 16 * ng; e += kMvComputeThreads) {
+          const int t = e / (16 * ng), rr = (e / ng) % 16, gg = e % ng;
+          const int row = tile * 16 + rr;
+          float s1 = 0.0f, b1 = 0.0f;
+          if (row < n) {
+            const size_t off = (size_t)row * p.groups + ch0 + gg;
+            s1 = bf16_to_f32(ldg_u16(p.m[mi + t].s + off));
+            b1 = bf16_to_f32(ldg_u16(p.m[mi + t].b + off));
+          }
+          float2 f;
+          if constexpr (kOff) f = make_float2(s1 * 16.0f, __fsub_rn(b1, s1 * 16.0f));
+          else f = make_float2(s1, b1);
+          sbf[(t * SPAN + gg) * 16 + rr] = f;
+        }
+      }
+      // Activations: a preceding kernel may write them, so they are read only after
+      // the programmatic-dependency wait.
+      if (ch0 == gs0) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+      }
+      named_bar_sync(kBarCompute, kMvComputeThreads);  // factor pairs visible
+      bool xv[NB];
+#pragma unroll
+      for (int h = 0; h < NB; ++h) xv[h] = (8 * h + g4) < p.rows;
+      for (int cc = 0; cc < kNch; ++cc) {
+        const int ga = ch0 + cc * GPC;
+        if (ga >= ch1) break;
+        const int gw0 = ga + warp * GPW;  // this warp's groups of the chunk
+        const int gcnt = max(0, min(GPW, ch1 - gw0));
+        // the first group's activations are in flight while the chunk's weights land
+        uint4 Xa[NB], Xb[NB];
+#pragma unroll
+        for (int h = 0; h < NB; ++h) {
+          Xa[h] = make_uint4(0, 0, 0, 0);
+          Xb[h] = make_uint4(0, 0, 0, 0);
+          if (xv[h] && gcnt > 0)
+            load_x_frag<kOff>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)gw0 * 64 + 16 * c, Xa[h], Xb[h]);
+        }
+        if (ok) ok = mbar_wait_bounded(&bars[cc], phase, p.budget_ns, nullptr);
+        if (!ok) continue;  // keep every barrier below matched; the status word records why
+#pragma unroll
+        for (int gi = 0; gi < GPW; ++gi) {
+          if (gi < gcnt) {
+            const int gl = gw0 + gi - ch0;  // group index within the span
+            uint4 X0[NB], X1[NB];
+#pragma unroll
+            for (int h = 0; h < NB; ++h) {
+              X0[h] = Xa[h];
+              X1[h] = Xb[h];
+              if (xv[h] && gi + 1 < gcnt)  // next group's activations
+                load_x_frag<kOff>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi + 1) * 64 + 16 * c, Xa[h],
+                                  Xb[h]);
+            }
+            // S of the group for this lane's two output columns (A = 1)
+            float S[NB][4];
+#pragma unroll
+            for (int h = 0; h < NB; ++h) {
+              S[h][0] = S[h][1] = S[h][2] = S[h][3] = 0.0f;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) mma_bf16_16816(S[h], ones, u4get(X0[h], j), u4get(X1[h], j), S[h]);
+            }
+#pragma unroll
+            for (int t = 0; t < NMAT; ++t) {
+              uint32_t W0[LW], W1[LW];
+              lds_lane_words<BITS>(wsm + (t * 16 + g4) * WP + gl * GB + c * 4 * LW, W0);
+              lds_lane_words<BITS>(wsm + (t * 16 + g4 + 8) * WP + gl * GB + c * 4 * LW, W1);
+              float P[NB][4];
+#pragma unroll
+              for (int h = 0; h < NB; ++h) P[h][0] = P[h][1] = P[h][2] = P[h][3] = 0.0f;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t a[4];
+                if constexpr (kOff) {
+                  a[0] = q4_off_pair(W0[0], j);
+                  a[1] = q4_off_pair(W1[0], j);
+                  a[2] = q4_off_pair(W0[1], j);
+                  a[3] = q4_off_pair(W1[1], j);
+                } else {
+                  lane_pairs<BITS>(W0, j, a[0], a[2]);
+                  lane_pairs<BITS>(W1, j, a[1], a[3]);
+                }
+#pragma unroll
+                for (int h = 0; h < NB; ++h) mma_bf16_16816(P[h], a, u4get(X0[h], j), u4get(X1[h], j), P[h]);
+              }
+              // (scale-like, bias-like) factors of rows g4 and g4 + 8
+              const float2 f0 = sbf[(t * SPAN + gl) * 16 + g4];
+              const float2 f1 = sbf[(t * SPAN + gl) * 16 + g4 + 8];
+#pragma unroll
+              for (int h = 0; h < NB; ++h) {
+                float *yy = &y[(t * NB + h) * 4];
+                yy[0] = __fmaf_rn(f0.x, P[h][0], yy[0]); yy[0] = __fmaf_rn(f0.y, S[h][0], yy[0]);
+                yy[1] = __fmaf_rn(f0.x, P[h][1], yy[1]); yy[1] = __fmaf_rn(f0.y, S[h][1], yy[1]);
+                yy[2] = __fmaf_rn(f1.x, P[h][2], yy[2]); yy[2] = __fmaf_rn(f1.y, S[h][0], yy[2]);
+                yy[3] = __fmaf_rn(f1.x, P[h][3], yy[3]); yy[3] = __fmaf_rn(f1.y, S[h][1], yy[3]);
+              }
+            }
+          }
         }
       }
     }
-    if (ch0 != gs0) __syncthreads();  // the previous chunk's activations are fully read
-    // ---- 2. scales and biases the slow way (rows not 16-byte aligned)
-    if (!p.sb_bulk) {
-      if (ch0 != gs0) __syncthreads();
-      for (int e = threadIdx.x; e < NMAT * 16 * cg_n; e += blockDim.x) {
-        const int t = e / (16 * cg_n), rr = (e / cg_n) % 16, gg = e % cg_n;
-        const int row = tile * 16 + rr;
-        uint16_t sv = 0, bv = 0;
-        if (row < n) {
-          const size_t off = (size_t)row * p.groups + ch0 + gg;
-          sv = (uint16_t)ldg_u16(p.m[mi + t].s + off);
-          bv = (uint16_t)ldg_u16(p.m[mi + t].b + off);
-        }
-        sbs[((t * 2 + 0) * 16 + rr) * SPAN + gg] = sv;
-        sbs[((t * 2 + 1) * 16 + rr) * SPAN + gg] = bv;
-      }
-    }
-    // ---- 3. activations: a preceding kernel may write them, so they are read only
-    //         after the programmatic-dependency wait; one bulk copy per row
-    if (ch0 == gs0) {
-      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-    }
-    __syncthreads();  // scales/biases visible; barriers initialised
-    if (threadIdx.x == 0) {
-      fence_proxy_async_smem();
-      const uint32_t xb = (uint32_t)(ch1 - ch0) * 128u;
-      mbar_arrive_expect_tx(xbar, xb * (uint32_t)p.rows);
-      for (int r = 0; r < p.rows; ++r)
-        bulk_g2s(xs + r * XP, p.x + (size_t)r * p.ldx + (size_t)ch0 * 64, xb, xbar);
-    }
-    bool ok = mbar_wait_bounded(xbar, phase, p.budget_ns, nullptr) &&
-              mbar_wait_bounded(wbar, phase, p.budget_ns, nullptr);
     phase ^= 1u;
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) {
-      if (threadIdx.x == 0) record_status(p.status, kErrTimeout);
-      break;
-    }
-    // ---- 4. per group: exact-code MMAs, then the affine step in group order
-    bool xv[NB];
-#pragma unroll
-    for (int h = 0; h < NB; ++h) xv[h] = (8 * h + g4) < p.rows;
-#pragma unroll
-    for (int gi = 0; gi < GPW; ++gi) {
-      if (gi < gcnt) {
-        const int gl = gw0 + gi - ch0;  // group index within the chunk
-        uint4 X0[NB], X1[NB];
-#pragma unroll
-        for (int h = 0; h < NB; ++h) {
-          if (xv[h]) {
-            const uint16_t *px = xs + (8 * h + g4) * XP + gl * 64 + 16 * c;
-            X0[h] = lds_v4(px);
-            X1[h] = lds_v4(px + 8);
-          } else {
-            X0[h] = make_uint4(0, 0, 0, 0);
-            X1[h] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        float S[NB][4];
-#pragma unroll
-        for (int h = 0; h < NB; ++h) {
-          S[h][0] = S[h][1] = S[h][2] = S[h][3] = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mma_bf16_16816(S[h], ones, u4get(X0[h], j), u4get(X1[h], j), S[h]);
-        }
-#pragma unroll
-        for (int t = 0; t < NMAT; ++t) {
-          uint32_t W0[LW], W1[LW];
-          lds_lane_words<BITS>(wsm + (t * 16 + g4) * WP + gl * GB + c * 4 * LW, W0);
-          lds_lane_words<BITS>(wsm + (t * 16 + g4 + 8) * WP + gl * GB + c * 4 * LW, W1);
-          float P[NB][4];
-#pragma unroll
-          for (int h = 0; h < NB; ++h) P[h][0] = P[h][1] = P[h][2] = P[h][3] = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t a[4];
-            lane_pairs<BITS>(W0, j, a[0], a[2]);
-            lane_pairs<BITS>(W1, j, a[1], a[3]);
-#pragma unroll
-            for (int h = 0; h < NB; ++h) mma_bf16_16816(P[h], a, u4get(X0[h], j), u4get(X1[h], j), P[h]);
-          }
-          const float2 sb0 = make_float2(bf16_to_f32(sbs[((t * 2 + 0) * 16 + g4) * SPAN + gl]),
-                                         bf16_to_f32(sbs[((t * 2 + 1) * 16 + g4) * SPAN + gl]));
-          const float2 sb1 = make_float2(bf16_to_f32(sbs[((t * 2 + 0) * 16 + g4 + 8) * SPAN + gl]),
-                                         bf16_to_f32(sbs[((t * 2 + 1) * 16 + g4 + 8) * SPAN + gl]));
-#pragma unroll
-          for (int h = 0; h < NB; ++h) {
-            float *yy = &y[(t * NB + h) * 4];
-            yy[0] = __fmaf_rn(sb0.x, P[h][0], yy[0]); yy[0] = __fmaf_rn(sb0.y, S[h][0], yy[0]);
-            yy[1] = __fmaf_rn(sb0.x, P[h][1], yy[1]); yy[1] = __fmaf_rn(sb0.y, S[h][1], yy[1]);
-            yy[2] = __fmaf_rn(sb1.x, P[h][2], yy[2]); yy[2] = __fmaf_rn(sb1.y, S[h][0], yy[2]);
-            yy[3] = __fmaf_rn(sb1.x, P[h][3], yy[3]); yy[3] = __fmaf_rn(sb1.y, S[h][1], yy[3]);
-          }
-        }
-      }
-    }
-    __syncthreads();  // every warp is done with the chunk before it is refilled
+    if (ch1 < gs1) __syncthreads();  // the span's buffers are fully read before the next span refills them
   }
+  if (!ok && lane == 0) record_status(p.status, kErrTimeout);
 
-  // ---- partials: warps in order, then cluster ranks in order
+  // ---- partials: warps in order, then cluster ranks in order.  The partials reuse
+  //      the weight area, so every compute warp is past its last group first.
+  if (warp < kMvWarps) {
+    named_bar_sync(kBarCompute, kMvComputeThreads);
 #pragma unroll
-  for (int i = 0; i < NV; ++i) red[(warp * NV + i) * 32 + lane] = y[i];
-  __syncthreads();
-  for (int v = threadIdx.x; v < NV * 32; v += blockDim.x) {
-    const int i = v >> 5, ln = v & 31;
-    float acc = red[i * 32 + ln];
-    for (int w = 1; w < nwarps; ++w) acc = __fadd_rn(acc, red[(w * NV + i) * 32 + ln]);
-    csum[i * 32 + ln] = acc;
+    for (int i = 0; i < NV; ++i) red[(warp * NV + i) * 32 + lane] = y[i];
+    named_bar_sync(kBarCompute, kMvComputeThreads);
+    for (int v = threadIdx.x; v < NV * 32; v += kMvComputeThreads) {
+      const int i = v >> 5, ln = v & 31;
+      float acc = red[i * 32 + ln];
+#pragma unroll
+      for (int w = 1; w < kMvWarps; ++w) acc = __fadd_rn(acc, red[(w * NV + i) * 32 + ln]);
+      csum[i * 32 + ln] = acc;
+    }
+  } else if (lane == 0 && armed > 0) {
+    // every copy this CTA started must land before its shared memory goes away
+    for (int cc = 0; cc < armed; ++cc) (void)mbar_wait_bounded(&bars[cc], phase ^ 1u, kMvDrainNs, nullptr);
   }
   if (p.cs > 1) cluster.sync();
   else __syncthreads();
   if (rank == 0) {
     constexpr int NO = NB * 4;  // outputs per lane per matrix
-    for (int v = threadIdx.x; v < NO * 32; v += blockDim.x) {
+    for (int v = threadIdx.x; v < NO * 32; v += kMvThreads) {
       const int i = v >> 5, ln = v & 31;
       float acc[NMAT];
 #pragma unroll
@@ -347,21 +413,26 @@ __global__ void __launch_bounds__(kMvWarps * 32) qmv_kernel(const __grid_constan
 }
 
 template <int BITS, int NB, int MODE>
-static cudaError_t launch_t(const MvParams &p, int nwarps, int tiles, cudaStream_t st) {
+static cudaError_t launch_t(const MvParams &p, int tiles, cudaStream_t st) {
   using Lay = MvLayout<BITS, NB, MODE>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(qmv_kernel<BITS, NB, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay::bytes(16));
+                                         Lay::kBytes);
+    if (e != cudaSuccess) return e;
+    // every decode kernel asks for the largest shared-memory carveout, so CTAs of
+    // consecutive launches (programmatic dependent launch) can share an SM
+    e = cudaFuncSetAttribute(qmv_kernel<BITS, NB, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * p.cs));
-  cfg.blockDim = dim3((unsigned)(nwarps * 32));
-  cfg.dynamicSmemBytes = (size_t)Lay::bytes(p.rows);
+  cfg.blockDim = dim3((unsigned)kMvThreads);
+  cfg.dynamicSmemBytes = (size_t)Lay::kBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -376,12 +447,12 @@ static cudaError_t launch_t(const MvParams &p, int nwarps, int tiles, cudaStream
 }
 
 template <int MODE>
-static cudaError_t launch_mode(const MvParams &p, int bits, int nwarps, int tiles, cudaStream_t st) {
+static cudaError_t launch_mode(const MvParams &p, int bits, int tiles, cudaStream_t st) {
   const bool two = p.rows > 8;
   switch (bits) {
-    case 4: return two ? launch_t<4, 2, MODE>(p, nwarps, tiles, st) : launch_t<4, 1, MODE>(p, nwarps, tiles, st);
-    case 6: return two ? launch_t<6, 2, MODE>(p, nwarps, tiles, st) : launch_t<6, 1, MODE>(p, nwarps, tiles, st);
-    default: return two ? launch_t<8, 2, MODE>(p, nwarps, tiles, st) : launch_t<8, 1, MODE>(p, nwarps, tiles, st);
+    case 4: return two ? launch_t<4, 2, MODE>(p, tiles, st) : launch_t<4, 1, MODE>(p, tiles, st);
+    case 6: return two ? launch_t<6, 2, MODE>(p, tiles, st) : launch_t<6, 1, MODE>(p, tiles, st);
+    default: return two ? launch_t<8, 2, MODE>(p, tiles, st) : launch_t<8, 1, MODE>(p, tiles, st);
   }
 }
 
@@ -411,9 +482,9 @@ cudaError_t launch_mv(MvParams &p, int mode, int bits, int tiles, cudaStream_t s
     sb = sb && (reinterpret_cast<uintptr_t>(p.m[i].s) % 16) == 0 && (reinterpret_cast<uintptr_t>(p.m[i].b) % 16) == 0;
   p.sb_bulk = sb ? 1 : 0;
   switch (mode) {
-    case kMvFfn: return launch_mode<kMvFfn>(p, bits, nwarps, tiles, st);
-    case kMvAttn: return launch_mode<kMvAttn>(p, bits, nwarps, tiles, st);
-    default: return launch_mode<kMvPlain>(p, bits, nwarps, tiles, st);
+    case kMvFfn: return launch_mode<kMvFfn>(p, bits, tiles, st);
+    case kMvAttn: return launch_mode<kMvAttn>(p, bits, tiles, st);
+    default: return launch_mode<kMvPlain>(p, bits, tiles, st);
   }
 }
 

@@ -83,6 +83,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
+// Named hardware barrier over `nthreads` threads (warps wait without issuing).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void record_status(int *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
