@@ -49,12 +49,14 @@ template <int BITS> struct Geo;
 #define QL_MV_NCH 1
 #endif
 constexpr int kNch = QL_MV_NCH;  // chunks per span (one mbarrier each)
+// spans of 32 groups (4-bit) or 16 groups (6/8-bit), split over the compute warps and chunks
 template <> struct Geo<4> {
-  static constexpr int kLw = 2;             // words per lane per row per group
-  static constexpr int kGpw = 8 / kNch;     // groups per compute warp per chunk
+  static constexpr int kLw = 2;                          // words per lane per row per group
+  static constexpr int kGpw = 32 / (kMvWarps * kNch);    // groups per compute warp per chunk
 };
-template <> struct Geo<6> { static constexpr int kLw = 3; static constexpr int kGpw = 4 / kNch; };
-template <> struct Geo<8> { static constexpr int kLw = 4; static constexpr int kGpw = 4 / kNch; };
+template <> struct Geo<6> { static constexpr int kLw = 3; static constexpr int kGpw = 16 / (kMvWarps * kNch); };
+template <> struct Geo<8> { static constexpr int kLw = 4; static constexpr int kGpw = 16 / (kMvWarps * kNch); };
+static_assert(Geo<6>::kGpw >= 1, "every compute warp owns at least one group per chunk");
 template <int BITS> __host__ __device__ constexpr int gbytes() { return 8 * BITS; }                  // bytes per row per group
 template <int BITS> __host__ __device__ constexpr int gpc() { return kMvWarps * Geo<BITS>::kGpw; }  // groups per chunk
 template <int BITS> __host__ __device__ constexpr int span_g() { return kNch * gpc<BITS>(); }        // groups per span
@@ -114,22 +116,30 @@ constexpr uint64_t kMvDrainNs = 2000000000ull;
 // Shared-memory layout of one CTA (dynamic, 128-byte aligned):
 //   wsm [NMAT][16][wpitch]             weight rows of the span (one bulk copy per row and chunk);
 //                                      after the last group it holds the warp partials
-//                                      red[kMvWarps][NV][32] and the CTA partial csum[NV][32]
+//                                      red[kMvWarps][NV][32] and, without a cluster, the
+//                                      CTA partial csum[NV][32]
 //   sbf [NMAT][span][16] float2        per (group, row): (16s, b - 16s) for 4-bit, (s, b) else
 //   bars[kNch]                         one per chunk
+//   cpart[cs][NV][32] fp32             with a cluster of cs > 1 CTAs: every rank's CTA
+//                                      partial (only rank 0's copy is read); a region of
+//                                      its own, since other ranks write it while this
+//                                      CTA may still be reading its weights
 // Activations never pass through shared memory: each lane loads the 16-byte pieces
 // its MMA fragments take straight from global memory (L1/L2).
 template <int BITS, int NB, int MODE> struct MvLayout {
   static constexpr int NMAT = (MODE == kMvFfn) ? 2 : 1;
   static constexpr int NV = NMAT * NB * 4;
   static constexpr int kW = 0;
-  static constexpr int kWBytes = NMAT * 16 * wpitch<BITS>();
   static constexpr int kRed = 0;                                // aliases wsm
   static constexpr int kCsum = kRed + kMvWarps * NV * 32 * 4;   // aliases wsm
-  static_assert(kCsum + NV * 32 * 4 <= kWBytes, "partials must fit in the weight area");
+  static constexpr int kPartBytes = kCsum + NV * 32 * 4;
+  static constexpr int kWBytes = NMAT * 16 * wpitch<BITS>() > kPartBytes ? NMAT * 16 * wpitch<BITS>() : kPartBytes;
   static constexpr int kSbf = kWBytes;
   static constexpr int kBar = kSbf + NMAT * span_g<BITS>() * 16 * 8;
-  static constexpr int kBytes = kBar + kNch * 8;
+  static constexpr int kCpart = (kBar + kNch * 8 + 15) / 16 * 16;
+  static constexpr int kBytes = kCpart;  // without a cluster
+  static int bytes(int cs) { return cs > 1 ? kCpart + cs * NV * 32 * 4 : kBytes; }
+  static int max_bytes() { return bytes(kMvMaxCluster); }
 };
 
 // activation fragment of lane (g4, c) for one group: x[row][64g + 16c .. +16) as two
@@ -161,7 +171,7 @@ __global__ void __launch_bounds__(kMvThreads) qmv_kernel(const __grid_constant__
   extern __shared__ __align__(128) uint8_t smem[];
   float2 *sbf = reinterpret_cast<float2 *>(smem + Lay::kSbf);
   float *red = reinterpret_cast<float *>(smem + Lay::kRed);
-  float *csum = reinterpret_cast<float *>(smem + Lay::kCsum);
+  float *csum = reinterpret_cast<float *>(smem + (p.cs > 1 ? Lay::kCpart : Lay::kCsum));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
   uint8_t *wsm = smem + Lay::kW;
 
@@ -305,11 +315,20 @@ __global__ void __launch_bounds__(kMvThreads) qmv_kernel(const __grid_constant__
             uint4 X0[NB], X1[NB];
 #pragma unroll
             for (int h = 0; h < NB; ++h) {
-              X0[h] = Xa[h];
-              X1[h] = Xb[h];
-              if (xv[h] && gi + 1 < gcnt)  // next group's activations
-                load_x_frag<kOff>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi + 1) * 64 + 16 * c, Xa[h],
-                                  Xb[h]);
+              if (NB == 1 || gi == 0) {
+                // one activation row block: the next group's fragments are loaded a
+                // group ahead; with two blocks they are loaded when used (registers)
+                X0[h] = Xa[h];
+                X1[h] = Xb[h];
+                if (NB == 1 && xv[h] && gi + 1 < gcnt)
+                  load_x_frag<kOff>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi + 1) * 64 + 16 * c, Xa[h],
+                                    Xb[h]);
+              } else if (xv[h]) {
+                load_x_frag<kOff>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi) * 64 + 16 * c, X0[h], X1[h]);
+              } else {
+                X0[h] = make_uint4(0, 0, 0, 0);
+                X1[h] = make_uint4(0, 0, 0, 0);
+              }
             }
             // S of the group for this lane's two output columns (A = 1)
             float S[NB][4];
@@ -364,18 +383,22 @@ __global__ void __launch_bounds__(kMvThreads) qmv_kernel(const __grid_constant__
   if (!ok && lane == 0) record_status(p.status, kErrTimeout);
 
   // ---- partials: warps in order, then cluster ranks in order.  The partials reuse
-  //      the weight area, so every compute warp is past its last group first.
+  //      the weight area, so every compute warp is past its last group first.  In a
+  //      cluster each rank writes its CTA partial into slot `rank` of rank 0's cpart
+  //      (distributed shared memory); after one cluster barrier rank 0 adds the slots
+  //      in rank order and the other ranks may exit (nobody reads their shared memory).
   if (warp < kMvWarps) {
     named_bar_sync(kBarCompute, kMvComputeThreads);
 #pragma unroll
     for (int i = 0; i < NV; ++i) red[(warp * NV + i) * 32 + lane] = y[i];
     named_bar_sync(kBarCompute, kMvComputeThreads);
+    float *dst = (p.cs > 1 ? cluster.map_shared_rank(csum, 0) : csum) + rank * NV * 32;
     for (int v = threadIdx.x; v < NV * 32; v += kMvComputeThreads) {
       const int i = v >> 5, ln = v & 31;
       float acc = red[i * 32 + ln];
 #pragma unroll
       for (int w = 1; w < kMvWarps; ++w) acc = __fadd_rn(acc, red[(w * NV + i) * 32 + ln]);
-      csum[i * 32 + ln] = acc;
+      dst[i * 32 + ln] = acc;
     }
   } else if (lane == 0 && armed > 0) {
     // every copy this CTA started must land before its shared memory goes away
@@ -391,9 +414,8 @@ __global__ void __launch_bounds__(kMvThreads) qmv_kernel(const __grid_constant__
 #pragma unroll
       for (int t = 0; t < NMAT; ++t) acc[t] = csum[(t * NO + i) * 32 + ln];
       for (int r = 1; r < p.cs; ++r) {
-        const float *rs = cluster.map_shared_rank(csum, r);
 #pragma unroll
-        for (int t = 0; t < NMAT; ++t) acc[t] = __fadd_rn(acc[t], rs[(t * NO + i) * 32 + ln]);
+        for (int t = 0; t < NMAT; ++t) acc[t] = __fadd_rn(acc[t], csum[r * NV * 32 + (t * NO + i) * 32 + ln]);
       }
       // value i of lane ln: half h = i / 4, element e = i % 4
       const int h = i >> 2, e = i & 3;
@@ -409,7 +431,6 @@ __global__ void __launch_bounds__(kMvThreads) qmv_kernel(const __grid_constant__
       }
     }
   }
-  if (p.cs > 1) cluster.sync();
 }
 
 template <int BITS, int NB, int MODE>
@@ -420,7 +441,7 @@ static cudaError_t launch_t(const MvParams &p, int tiles, cudaStream_t st) {
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(qmv_kernel<BITS, NB, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay::kBytes);
+                                         Lay::max_bytes());
     if (e != cudaSuccess) return e;
     // every decode kernel asks for the largest shared-memory carveout, so CTAs of
     // consecutive launches (programmatic dependent launch) can share an SM
@@ -432,7 +453,7 @@ static cudaError_t launch_t(const MvParams &p, int tiles, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * p.cs));
   cfg.blockDim = dim3((unsigned)kMvThreads);
-  cfg.dynamicSmemBytes = (size_t)Lay::kBytes;
+  cfg.dynamicSmemBytes = (size_t)Lay::bytes(p.cs);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -6,7 +6,10 @@
 
 namespace qlk {
 
-constexpr int kMvWarps = 4;       // warps per CTA (each owns a slice of the CTA's k chunk)
+#ifndef QL_MV_WARPS
+#define QL_MV_WARPS 8
+#endif
+constexpr int kMvWarps = QL_MV_WARPS;  // compute warps per CTA (each owns a slice of the CTA's k-span)
 constexpr int kMvMaxCluster = 8;  // CTAs per cluster along k
 
 enum { kMvPlain = 0, kMvFfn = 1, kMvAttn = 2 };
