@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--n", type=int, default=D_FF, help="--case: output channels")
     ap.add_argument("--k", type=int, default=D_MODEL, help="--case: input channels")
     ap.add_argument("--rows", type=int, default=1, help="--case ffn/mv: activation rows")
+    ap.add_argument("--copies", type=int, default=1,
+                    help="--case ffn/mv: distinct weight copies cycled through (> L2 with enough copies)")
     return ap.parse_args()
 
 
@@ -491,16 +493,28 @@ def run_case(args):
         Y = torch.empty(args.m, n, device=dev)
         fn, unit, work = (lambda: q.qlinear_pgemm(wt, X, Y)), "TFLOP/s", 2.0 * args.m * n * k
     elif args.case == "ffn":
-        w1, w3 = w(), w()
+        pairs = [(w(), w()) for _ in range(args.copies)]
         x = torch.randn(args.rows, k, generator=gen, device=dev).to(torch.bfloat16)
         h = torch.empty(args.rows, n, dtype=torch.bfloat16, device=dev)
-        fn, unit = (lambda: q.qffn_swiglu_mv(w1, w3, x, h)), "GB/s"
+        it = [0]
+
+        def fn():
+            w1, w3 = pairs[it[0] % len(pairs)]
+            it[0] += 1
+            q.qffn_swiglu_mv(w1, w3, x, h)
+        unit = "GB/s"
         work = 2 * weight_bytes(n, k, bits) + args.rows * (k * 2 + n * 2)
     else:
-        wt = w()
+        ws = [w() for _ in range(args.copies)]
         x = torch.randn(args.rows, k, generator=gen, device=dev).to(torch.bfloat16)
         y = torch.empty(args.rows, n, device=dev)
-        fn, unit = (lambda: q.qlinear_mv_rows(wt, x, y)), "GB/s"
+        it = [0]
+
+        def fn():
+            wt = ws[it[0] % len(ws)]
+            it[0] += 1
+            q.qlinear_mv_rows(wt, x, y)
+        unit = "GB/s"
         work = weight_bytes(n, k, bits) + args.rows * (k * 2 + n * 4)
     for _ in range(args.warmup):
         fn()
@@ -514,6 +528,7 @@ def run_case(args):
     ms = e0.elapsed_time(e1) / max(1, args.steps)
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     print(json.dumps({"case": args.case, "bits": bits, "m": args.m, "n": n, "k": k, "rows": args.rows,
+                      "copies": args.copies,
                       "us_per_launch": ms * 1e3, unit: work / (ms * 1e-3) / scale,
                       "status": q.qlinear_last_error()}), flush=True)
 
