@@ -24,14 +24,16 @@
 // each output from its own row and column, tiles out of range are zero-filled by
 // TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
 //
-// Warp roles (one CTA per 128-channel x 128-row output tile, 576 threads):
+// Warp roles (one CTA per 128-channel x 128-row output tile, 608 threads):
 //   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block;
 //               scale and bias boxes)
-//   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2-9   converters: packed codes -> bf16 in tensor memory, scales -> fp32
+//   warps 1-2   MMA issuers (one thread each): warp 1 the even k blocks and
+//               accumulator 0, warp 2 the odd ones and accumulator 1 (the bias blocks
+//               go to the owner of accumulator G % 2); warp 1 also allocates TMEM
+//   warps 3-10  converters: packed codes -> bf16 in tensor memory, scales -> fp32
 //               (a warp writes the tensor-memory lanes of its quarter; two warps per
 //               quarter, each half of a row)
-//   warps 10-17 epilogue: tensor memory -> registers, scale chain, bias add, store
+//   warps 11-18 epilogue: tensor memory -> registers, scale chain, bias add, store
 //               (two warps per lane quarter, 64 rows of X each)
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
 // QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees TMEM and returns.
@@ -55,7 +57,7 @@ constexpr int BK = 64;
 constexpr int kScStages = 8;  // fp32 scale rows (deep enough to need no release barrier, see converters)
 constexpr int kConvWarps = 8;
 constexpr int kEpiWarps = 8;
-constexpr int kRoleWarps = 2;  // producer, MMA issuer
+constexpr int kRoleWarps = 3;  // producer, two MMA issuers
 constexpr int kThreads = (kRoleWarps + kConvWarps + kEpiWarps) * 32;
 constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;
 constexpr int kConvThreads = kConvWarps * 32;
@@ -86,8 +88,8 @@ template <int BITS> struct Cfg {
   static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
   static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
   // barriers: tma_full, tma_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
-  //           sc_full, scb_full[2], scb_empty[2], bias_full, mma_done
-  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 1 + 1;
+  //           sc_full, scb_full[2], scb_empty[2], bias_full, mma_done[2]
+  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 1 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -269,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kScStages; ++i) mbar_init(&sc_full[i], kConvThreads);
     mbar_init(bias_full, 1);
-    mbar_init(mma_done, 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
@@ -339,14 +342,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer `par` (warp 1: 0, warp 2: 1) owns the main blocks kb with kb % 2 == par and
+    // accumulator par; the bias blocks all chain into accumulator G % 2 and belong to its
+    // owner.  Each issuer's barrier waits and commits overlap the other's MMAs.
+    const int par = warp - 1;
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BN, BM);
       bool any = false;
       for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % C::kStages, ab = kb % kABufs;
         const int a = kb < G ? kb : G;
+        if ((a & 1) != par) continue;
+        const int s = kb % C::kStages, ab = kb % kABufs;
         if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / C::kStages) & 1u, budget, abort_flag)) { give_up(); break; }
         if (!mbar_wait_bounded(&a_full[ab], (uint32_t)(kb / kABufs) & 1u, budget, abort_flag)) { give_up(); break; }
         if (kb <= G) {
@@ -370,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kb < G || kb == KB - 1) mma_commit(&acc_full[a & 1]);
       }
       if (any) {
-        mma_commit(mma_done);
-        (void)mbar_wait_bounded(mma_done, 0u, kDrainBudgetNs, nullptr);
+        mma_commit(&mma_done[par]);
+        (void)mbar_wait_bounded(&mma_done[par], 0u, kDrainBudgetNs, nullptr);
       }
     }
   } else if (warp < kEpiWarp0) {
