@@ -473,21 +473,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const int base = (kb - G) * BK + 32 * chalf;
+          if (bias_smem && (G % 8) == 0) {
+            // runs of 8 columns never cross a multiple of G: each is one 16-byte row
+            // of a staged bias box
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            uint32_t h2[2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              int j = base + 2 * e + hh;
-              uint32_t v = 0u;
+            for (int r = 0; r < 4; ++r) {
+              int j = base + 8 * r;
+              uint4 v = make_uint4(0u, 0u, 0u, 0u);
               if (nvalid && j < 3 * G) {
                 if (j >= G) j -= G;
                 if (j >= G) j -= G;
-                v = bias_smem ? (uint32_t)sbias[((j >> 3) * BN + ct) * 8 + (j & 7)] : ldg_u16(brow + j);
+                v = lds128(sbias + ((j >> 3) * BN + ct) * 8);
               }
-              h2[hh] = v;
+              o[4 * r] = v.x; o[4 * r + 1] = v.y; o[4 * r + 2] = v.z; o[4 * r + 3] = v.w;
             }
-            o[e] = h2[0] | (h2[1] << 16);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              uint32_t h2[2];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                int j = base + 2 * e + hh;
+                uint32_t v = 0u;
+                if (nvalid && j < 3 * G) {
+                  if (j >= G) j -= G;
+                  if (j >= G) j -= G;
+                  v = bias_smem ? (uint32_t)sbias[((j >> 3) * BN + ct) * 8 + (j & 7)] : ldg_u16(brow + j);
+                }
+                h2[hh] = v;
+              }
+              o[e] = h2[0] | (h2[1] << 16);
+            }
           }
         }
         tmem_st16(a_lane + (uint32_t)(ab * (BK / 2)), o);
