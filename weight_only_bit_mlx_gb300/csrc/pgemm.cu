@@ -9,14 +9,17 @@
 // For output Y[m][n] with 64-wide blocks b = 0..G-1:
 //   P_b[n][m] = sum_{j in b} q[n][j] * X[m][j]      tcgen05.mma, bf16 x bf16 -> fp32
 //               A = codes of 128 weight rows converted exactly to bf16 and written
-//                   straight into tensor memory (tcgen05.st); B = the X tile, staged
-//                   by TMA in shared memory; fresh accumulator per block,
-//                   double-buffered in tensor memory
+//                   into shared memory in the UMMA 128-byte-swizzle K-major layout;
+//               B = the X tile (256 rows), staged by TMA in shared memory; fresh
+//               accumulator per block, double-buffered in tensor memory
 //   y = fma(scale[n][b], P_b, y)  for b = 0..G-1 in order      (epilogue registers)
 //   Y = y + sum_b bias[n][b] * S_b[m]                            (added last)
 // with S_b[m] = sum_{j in b} X[m][j] computed by a pre-pass in fp32 and split
 // exactly into three bf16 parts, so the bias term is one more small tcgen05
 // contraction (k' = 3G) instead of a second fma per element and block.
+// The tile is 128 channels x 256 rows: tcgen05.mma at M = 128, N = 256, K = 16 runs
+// close to the tensor peak, while N = 128 (or A read from tensor memory) reaches
+// well under half of it on this part.
 // The accumulator holds output channels in tensor-memory lanes, so an epilogue
 // thread owns one channel: one scale per block, and the 32 lanes of a warp store 32
 // consecutive channels of a row (coalesced).
@@ -24,17 +27,15 @@
 // each output from its own row and column, tiles out of range are zero-filled by
 // TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
 //
-// Warp roles (one CTA per 128-channel x 128-row output tile, 608 threads):
+// Warp roles (one CTA per 128-channel x 256-row output tile, 704 threads):
 //   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block;
 //               scale and bias boxes)
-//   warps 1-2   MMA issuers (one thread each): warp 1 the even k blocks and
-//               accumulator 0, warp 2 the odd ones and accumulator 1 (the bias blocks
-//               go to the owner of accumulator G % 2); warp 1 also allocates TMEM
-//   warps 3-10  converters: packed codes -> bf16 in tensor memory, scales -> fp32
-//               (a warp writes the tensor-memory lanes of its quarter; two warps per
-//               quarter, each half of a row)
-//   warps 11-18 epilogue: tensor memory -> registers, scale chain, bias add, store
-//               (two warps per lane quarter, 64 rows of X each)
+//   warp 1      TMEM allocator (two accumulators of 256 columns) and the single
+//               thread that issues the MMAs
+//   warps 2-5   converters: one channel row per thread, packed codes -> bf16 A tile
+//               in shared memory, scales -> fp32
+//   warps 6-21  epilogue: tensor memory -> registers, scale chain, bias add, store
+//               (four warps per lane quarter, 64 rows of X each)
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
 // QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -51,48 +52,48 @@ namespace qlk {
 
 namespace pg {
 
-constexpr int BM = 128;  // rows of X per tile (MMA N)
+constexpr int BM = 256;  // rows of X per tile (MMA N)
 constexpr int BN = 128;  // output channels per tile (MMA M, tensor-memory lanes)
 constexpr int BK = 64;
 constexpr int kScStages = 8;  // fp32 scale rows (deep enough to need no release barrier, see converters)
-constexpr int kConvWarps = 8;
-constexpr int kEpiWarps = 8;
-constexpr int kRoleWarps = 3;  // producer, two MMA issuers
+constexpr int kConvWarps = 4;   // one channel row per thread
+constexpr int kEpiWarps = 16;   // four per tensor-memory lane quarter, 64 rows of X each
+constexpr int kRoleWarps = 2;   // producer, MMA issuer (and tensor-memory allocator)
 constexpr int kThreads = (kRoleWarps + kConvWarps + kEpiWarps) * 32;
 constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kXBytes = BM * BK * 2;
-// tensor-memory columns: two accumulators of BM columns, kABufs A buffers of BK/2 columns
-constexpr int kABufs = 4;  // converted weight blocks the converters may run ahead of the MMA
-constexpr int kColAcc = 0;
-constexpr int kColA = 2 * BM;
-constexpr int kTmemCols = 512;
-static_assert(kColA + kABufs * (BK / 2) <= kTmemCols, "tensor memory budget");
+constexpr int kEpiRows = BM / (kEpiWarps / 4);  // rows of X per epilogue thread
+constexpr int kXBytes = BM * BK * 2;            // X tile: BM rows x 64 bf16, 128-byte swizzle
+constexpr int kABytes = BN * BK * 2;            // converted W tile: 128 rows x 64 bf16, 128-byte swizzle
+constexpr int kABufs = 3;  // converted weight blocks the converters may run ahead of the MMA
+constexpr int kTmemCols = 512;  // two accumulators of BM fp32 columns
+static_assert(2 * BM <= kTmemCols, "tensor memory budget");
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
-constexpr int kPf = 4;       // k blocks of scale/bias prefetch (no-TMA path)
+constexpr int kPf = 2;       // k blocks of scale/bias prefetch (no-TMA path)
 static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
 
 template <int BITS> struct Cfg {
   static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
   static constexpr int kWBytes = BN * kRowBytes;         // packed W tile
-  // TMA stages in flight (X/S tile + packed W tile): as many as shared memory holds
-  static constexpr int kStages = BITS == 8 ? 7 : 8;
+  static constexpr int kStages = 3;                      // TMA stages in flight (X/S tile + packed W tile)
   static constexpr int kOffX = 0;
   static constexpr int kOffW = kOffX + kStages * kXBytes;
-  static constexpr int kOffSc = kOffW + kStages * kWBytes;
+  static constexpr int kOffA = (kOffW + kStages * kWBytes + 1023) / 1024 * 1024;
+  static constexpr int kOffSc = kOffA + kABufs * kABytes;
   // biases of the tile's rows, bf16, boxes of 8 groups: [kBiasG / 8][BN][8]
   static constexpr int kOffBias = kOffSc + kScStages * BN * 4;
   // scale boxes streamed by TMA, bf16 [2][BN][8]
   static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
   static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
   // barriers: tma_full, tma_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
-  //           sc_full, scb_full[2], scb_empty[2], bias_full, mma_done[2]
-  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 1 + 2;
+  //           sc_full, scb_full[2], scb_empty[2], bias_full, mma_done
+  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kBytes = kOffMisc + 16;  // tmem address, abort flag
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
 struct Params {
@@ -144,6 +145,20 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -234,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sX = smem + C::kOffX;
   uint8_t *sW = smem + C::kOffW;
+  uint8_t *sA = smem + C::kOffA;
   float *sSc = reinterpret_cast<float *>(smem + C::kOffSc);
   uint16_t *sbias = reinterpret_cast<uint16_t *>(smem + C::kOffBias);
   uint16_t *scbox = reinterpret_cast<uint16_t *>(smem + C::kOffScBox);
@@ -271,8 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kScStages; ++i) mbar_init(&sc_full[i], kConvThreads);
     mbar_init(bias_full, 1);
-    mbar_init(&mma_done[0], 1);
-    mbar_init(&mma_done[1], 1);
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
@@ -342,19 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
       }
     }
-  } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers
-    // Issuer `par` (warp 1: 0, warp 2: 1) owns the main blocks kb with kb % 2 == par and
-    // accumulator par; the bias blocks all chain into accumulator G % 2 and belong to its
-    // owner.  Each issuer's barrier waits and commits overlap the other's MMAs.
-    const int par = warp - 1;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BN, BM);
       bool any = false;
       for (int kb = 0; kb < KB; ++kb) {
-        const int a = kb < G ? kb : G;
-        if ((a & 1) != par) continue;
         const int s = kb % C::kStages, ab = kb % kABufs;
+        const int a = kb < G ? kb : G;
         if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / C::kStages) & 1u, budget, abort_flag)) { give_up(); break; }
         if (!mbar_wait_bounded(&a_full[ab], (uint32_t)(kb / kABufs) & 1u, budget, abort_flag)) { give_up(); break; }
         if (kb <= G) {
@@ -364,13 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(kColAcc + (a & 1) * BM);
-        const uint32_t at = tmem_base + (uint32_t)(kColA + ab * (BK / 2));
+        const uint32_t d = tmem_base + (uint32_t)((a & 1) * BM);
+        const uint64_t ad = sw128_desc(smem_addr(sA + ab * kABytes));
         const uint64_t bd = sw128_desc(smem_addr(sX + s * kXBytes));
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint32_t acc = (kk > 0 || kb > G) ? 1u : 0u;
-          mma_bf16_ts(d, at + (uint32_t)(8 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
+          mma_bf16_ss(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
         }
         any = true;
         mma_commit(&tma_empty[s]);
@@ -378,30 +388,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kb < G || kb == KB - 1) mma_commit(&acc_full[a & 1]);
       }
       if (any) {
-        mma_commit(&mma_done[par]);
-        (void)mbar_wait_bounded(&mma_done[par], 0u, kDrainBudgetNs, nullptr);
+        mma_commit(mma_done);
+        (void)mbar_wait_bounded(mma_done, 0u, kDrainBudgetNs, nullptr);
       }
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ converters
-    const int q = warp & 3;                         // tensor-memory lane quarter of this warp
-    const int chalf = (warp - kRoleWarps) >> 2;     // half of the row: chunks 4*chalf .. 4*chalf+3
-    const int ct = 32 * q + lane;                   // channel (row of the W tile) = tensor-memory lane
-    const bool lead = chalf == 0;                   // also moves the channel's scale and bias
-    const uint32_t a_lane = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(kColA + 16 * chalf);
+    // Thread = one channel row of the tile.  Its 64 codes of the block become 32 exact
+    // bf16 pairs, written as eight 16-byte chunks of the row of the A tile in the
+    // UMMA 128-byte-swizzle K-major layout: 8-row groups 1024 bytes apart, rows 128
+    // bytes apart, chunk c of row r at position c ^ (r % 8).
+    const int ct = 32 * (warp & 3) + lane;  // channel (row of the W tile)
     const int n = n0 + ct;
     const bool nvalid = n < p.N;
     const uint16_t *srow = p.scales + (size_t)(nvalid ? n : 0) * G;
     const uint16_t *brow = p.biases + (size_t)(nvalid ? n : 0) * G;
     const bool bias_smem = G <= kBiasG;
-    // Without TMA boxes (k % 512 != 0), the lead thread loads its channel's scale and
-    // bias itself, kPf blocks ahead; the loop is unrolled by kPf so that each ring
-    // slot stays in place while its load is in flight.
+    const uint32_t a_row = smem_addr(sA) + (uint32_t)((ct >> 3) * 1024 + (ct & 7) * 128);
+    const uint32_t sw = (uint32_t)(ct & 7);
+    // Without TMA boxes (k % 512 != 0), the thread loads its channel's scale and bias
+    // itself, kPf blocks ahead; the loop is unrolled by kPf so that each ring slot
+    // stays in place while its load is in flight.
     uint32_t sr[kPf], br[kPf];
 #pragma unroll
     for (int i = 0; i < kPf; ++i) {
-      sr[i] = (lead && !p.sc_tma && nvalid && i < G) ? ldg_u16(srow + i) : 0u;
-      br[i] = (lead && !p.bi_tma && bias_smem && nvalid && i < G) ? ldg_u16(brow + i) : 0u;
+      sr[i] = (!p.sc_tma && nvalid && i < G) ? ldg_u16(srow + i) : 0u;
+      br[i] = (!p.bi_tma && bias_smem && nvalid && i < G) ? ldg_u16(brow + i) : 0u;
     }
     bool alive = true;
     for (int kb0 = 0; kb0 < KB && alive; kb0 += kPf) {
@@ -412,10 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = kb % C::kStages, ab = kb % kABufs;
         uint32_t s_cur = 0u, b_cur = 0u;
         if (kb < G) {
-          if (!p.sc_tma) {
-            s_cur = sr[u];
-            sr[u] = (lead && nvalid && kb + kPf < G) ? ldg_u16(srow + kb + kPf) : 0u;
-          } else {
+          if (p.sc_tma) {
             const int j = kb >> 3, slot = j & 1;
             if ((kb & 7) == 0 &&
                 !mbar_wait_bounded(&scb_full[slot], (uint32_t)(j >> 1) & 1u, budget, abort_flag)) {
@@ -425,10 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             s_cur = scbox[(slot * BN + ct) * 8 + (kb & 7)];
             if ((kb & 7) == 7 || kb == G - 1) mbar_arrive(&scb_empty[slot]);
+          } else {
+            s_cur = sr[u];
+            sr[u] = (nvalid && kb + kPf < G) ? ldg_u16(srow + kb + kPf) : 0u;
           }
           if (!p.bi_tma && bias_smem) {
             b_cur = br[u];
-            br[u] = (lead && nvalid && kb + kPf < G) ? ldg_u16(brow + kb + kPf) : 0u;
+            br[u] = (nvalid && kb + kPf < G) ? ldg_u16(brow + kb + kPf) : 0u;
           }
         }
         if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / C::kStages) & 1u, budget, abort_flag) ||
@@ -437,33 +449,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           alive = false;
           break;
         }
-        tc_fence_after();
-        uint32_t o[16];
+        const uint32_t dst = a_row + (uint32_t)(ab * kABytes);
         if (kb < G) {
-          constexpr int NW = BK * BITS / 64;  // words of half a row
+          constexpr int NW = BK * BITS / 32;  // words of the row
           uint32_t w[NW];
-          const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes + chalf * (C::kRowBytes / 2);
-          if constexpr ((NW % 4) == 0) {
+          const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes;
 #pragma unroll
-            for (int i = 0; i < NW / 4; ++i) {
-              uint4 v = lds128(wp + 16 * i);
-              w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < NW / 2; ++i) {
-              uint2 v = lds64(wp + 8 * i);
-              w[2 * i] = v.x; w[2 * i + 1] = v.y;
-            }
+          for (int i = 0; i < NW / 4; ++i) {
+            uint4 v = lds128(wp + 16 * i);
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) convert_chunk<BITS, NW>(w, c, o + 4 * c);
-          if (lead && !p.bi_tma && bias_smem) sbias[((kb >> 3) * BN + ct) * 8 + (kb & 7)] = (uint16_t)b_cur;
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[4];
+            convert_chunk<BITS, NW>(w, c, o);
+            sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+          }
+          if (!p.bi_tma && bias_smem) sbias[((kb >> 3) * BN + ct) * 8 + (kb & 7)] = (uint16_t)b_cur;
           // Scale slot kb % kScStages was last read by the epilogue for block
           // kb - kScStages.  Passing a_empty for this block means the MMA of block
           // kb - kABufs finished, which waited for the epilogue to release block
           // kb - kABufs - 2; kScStages >= kABufs + 3 keeps the slot free.
-          if (lead) sSc[(kb % kScStages) * BN + ct] = bf16_to_f32(s_cur);
+          sSc[(kb % kScStages) * BN + ct] = bf16_to_f32(s_cur);
         } else {
           // bias block: column t of block jb is k' = 64*jb + t of the [part][group]
           // layout; its A value is bias[n][k' mod G] (zero past 3G)
@@ -472,43 +479,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             alive = false;
             break;
           }
-          const int base = (kb - G) * BK + 32 * chalf;
-          if (bias_smem && (G % 8) == 0) {
-            // runs of 8 columns never cross a multiple of G: each is one 16-byte row
-            // of a staged bias box
+          const int base = (kb - G) * BK;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              int j = base + 8 * r;
-              uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[4] = {0u, 0u, 0u, 0u};
+            int j = base + 8 * c;
+            if (bias_smem && (G % 8) == 0) {
+              // a run of 8 columns never crosses a multiple of G: one 16-byte row of a
+              // staged bias box
               if (nvalid && j < 3 * G) {
                 if (j >= G) j -= G;
                 if (j >= G) j -= G;
-                v = lds128(sbias + ((j >> 3) * BN + ct) * 8);
+                const uint4 v = lds128(sbias + ((j >> 3) * BN + ct) * 8);
+                o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
               }
-              o[4 * r] = v.x; o[4 * r + 1] = v.y; o[4 * r + 2] = v.z; o[4 * r + 3] = v.w;
-            }
-          } else {
+            } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              uint32_t h2[2];
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                int j = base + 2 * e + hh;
+              for (int e = 0; e < 8; ++e) {
+                int jj = j + e;
                 uint32_t v = 0u;
-                if (nvalid && j < 3 * G) {
-                  if (j >= G) j -= G;
-                  if (j >= G) j -= G;
-                  v = bias_smem ? (uint32_t)sbias[((j >> 3) * BN + ct) * 8 + (j & 7)] : ldg_u16(brow + j);
+                if (nvalid && jj < 3 * G) {
+                  if (jj >= G) jj -= G;
+                  if (jj >= G) jj -= G;
+                  v = bias_smem ? (uint32_t)sbias[((jj >> 3) * BN + ct) * 8 + (jj & 7)] : ldg_u16(brow + jj);
                 }
-                h2[hh] = v;
+                o[e >> 1] |= v << (16 * (e & 1));
               }
-              o[e] = h2[0] | (h2[1] << 16);
             }
+            sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
           }
         }
-        tmem_st16(a_lane + (uint32_t)(ab * (BK / 2)), o);
-        tmem_wait_st();
-        tc_fence_before();
+        fence_proxy_async_smem();  // the A tile is read by the tensor core (async proxy)
         mbar_arrive(&a_full[ab]);
         if (kb < G) mbar_arrive(&sc_full[kb % kScStages]);
         mbar_arrive(&tma_empty[s]);
@@ -516,11 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    constexpr int CW = BM / 2;  // rows of X owned by one thread
-    const int q = warp & 3;     // tensor-memory lane quarter this warp may access
-    const int half = (warp - kEpiWarp0) / 4;
+    constexpr int CW = kEpiRows;  // rows of X owned by one thread
+    const int q = warp & 3;       // tensor-memory lane quarter this warp may access
+    const int slice = (warp - kEpiWarp0) >> 2;
     const int ch_row = 32 * q + lane;  // output channel of this thread within the tile
-    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(kColAcc + half * CW);
+    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(slice * CW);
     float y[CW];
 #pragma unroll
     for (int i = 0; i < CW; ++i) y[i] = 0.0f;
@@ -536,20 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float sv = sSc[sc * BN + ch_row];
-      // 8-column chunks; the next chunk's TMEM load is in flight while one is used
-      uint32_t ra[8], rb[8];
-      tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM), ra);
-      tmem_wait_ld();
 #pragma unroll
       for (int ch = 0; ch < CW / 8; ++ch) {
-        uint32_t(&cur)[8] = (ch & 1) ? rb : ra;
-        uint32_t(&nxt)[8] = (ch & 1) ? ra : rb;
-        if (ch + 1 < CW / 8) tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * (ch + 1)), nxt);
+        uint32_t r[8];
+        tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * ch), r);
+        tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          ffma2(y[8 * ch + 2 * i], y[8 * ch + 2 * i + 1], sv, sv, __uint_as_float(cur[2 * i]),
-                __uint_as_float(cur[2 * i + 1]));
-        if (ch + 1 < CW / 8) tmem_wait_ld();
+          ffma2(y[8 * ch + 2 * i], y[8 * ch + 2 * i + 1], sv, sv, __uint_as_float(r[2 * i]),
+                __uint_as_float(r[2 * i + 1]));
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
@@ -576,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one channel per thread: lanes of a warp write 32 consecutive channels of a row
       const int n = n0 + ch_row;
       if (n < p.N) {
-        const int mb = m0 + half * CW;
+        const int mb = m0 + slice * CW;
         float *ycol = p.Y + (size_t)mb * p.ldy + n;
 #pragma unroll
         for (int i = 0; i < CW; ++i)
