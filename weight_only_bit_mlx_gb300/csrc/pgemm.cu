@@ -1,5 +1,5 @@
 // pgemm.cu - prompt-window GEMM over MLX affine 4/6/8-bit group-64 weights on the
-// sm_103a tensor cores (TMA -> exact dequant into tensor memory -> tcgen05.mma).
+// sm_103a tensor cores (TMA -> exact dequant into shared memory -> tcgen05.mma).
 //
 // TensorFold PR #1696 (later revision), "What it adds" > "Prompt GEMM": prompt
 // windows take a GEMM that dequantizes the 4-bit weights as it loads each weight
