@@ -27,14 +27,16 @@
 // each output from its own row and column, tiles out of range are zero-filled by
 // TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
 //
-// Warp roles (one CTA per 128-channel x 256-row output tile, 704 threads):
+// Warp roles (one CTA per 128-channel x 256-row output tile, 736 threads):
 //   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block;
 //               scale and bias boxes)
-//   warp 1      TMEM allocator (two accumulators of 256 columns) and the single
-//               thread that issues the MMAs
-//   warps 2-5   converters: one channel row per thread, packed codes -> bf16 A tile
+//   warps 1-2   MMA issuers (one thread each): warp 1 the even k blocks and
+//               accumulator 0, warp 2 the odd ones and accumulator 1 (the bias blocks go
+//               to the owner of accumulator G % 2); warp 1 also allocates TMEM (two
+//               accumulators of 256 columns)
+//   warps 3-6   converters: one channel row per thread, packed codes -> bf16 A tile
 //               in shared memory, scales -> fp32
-//   warps 6-21  epilogue: tensor memory -> registers, scale chain, bias add, store
+//   warps 7-22  epilogue: tensor memory -> registers, scale chain, bias add, store
 //               (four warps per lane quarter, 64 rows of X each)
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
 // QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees TMEM and returns.
@@ -58,7 +60,7 @@ constexpr int BK = 64;
 constexpr int kScStages = 8;  // fp32 scale rows (deep enough to need no release barrier, see converters)
 constexpr int kConvWarps = 4;   // one channel row per thread
 constexpr int kEpiWarps = 16;   // four per tensor-memory lane quarter, 64 rows of X each
-constexpr int kRoleWarps = 2;   // producer, MMA issuer (and tensor-memory allocator)
+constexpr int kRoleWarps = 3;   // producer, two MMA issuers (the first also allocates tensor memory)
 constexpr int kThreads = (kRoleWarps + kConvWarps + kEpiWarps) * 32;
 constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;
 constexpr int kConvThreads = kConvWarps * 32;
@@ -70,14 +72,14 @@ constexpr int kABufs = 3;  // converted weight blocks the converters may run ahe
 constexpr int kTmemCols = 512;  // two accumulators of BM fp32 columns
 static_assert(2 * BM <= kTmemCols, "tensor memory budget");
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
-constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
+constexpr int kBiasG = 64;   // groups of bias staged in shared memory (k <= 4096); larger k reads global
 constexpr int kPf = 2;       // k blocks of scale/bias prefetch (no-TMA path)
 static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
 
 template <int BITS> struct Cfg {
   static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
   static constexpr int kWBytes = BN * kRowBytes;         // packed W tile
-  static constexpr int kStages = 3;                      // TMA stages in flight (X/S tile + packed W tile)
+  static constexpr int kStages = BITS == 8 ? 3 : 4;      // TMA stages in flight (X/S tile + packed W tile)
   static constexpr int kOffX = 0;
   static constexpr int kOffW = kOffX + kStages * kXBytes;
   static constexpr int kOffA = (kOffW + kStages * kWBytes + 1023) / 1024 * 1024;
@@ -88,8 +90,8 @@ template <int BITS> struct Cfg {
   static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
   static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
   // barriers: tma_full, tma_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
-  //           sc_full, scb_full[2], scb_empty[2], bias_full, mma_done
-  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 1 + 1;
+  //           sc_full, scb_full[2], scb_empty[2], bias_full, mma_done[2]
+  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 1 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;  // tmem address, abort flag
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -287,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kScStages; ++i) mbar_init(&sc_full[i], kConvThreads);
     mbar_init(bias_full, 1);
-    mbar_init(mma_done, 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
@@ -357,14 +360,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer `par` (warp 1: 0, warp 2: 1) owns the main blocks kb with kb % 2 == par and
+    // accumulator par; the bias blocks all chain into accumulator G % 2 and belong to its
+    // owner.  One issuer's barrier waits and commits overlap the other's MMAs.
+    const int par = warp - 1;
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BN, BM);
       bool any = false;
       for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % C::kStages, ab = kb % kABufs;
         const int a = kb < G ? kb : G;
+        if ((a & 1) != par) continue;
+        const int s = kb % C::kStages, ab = kb % kABufs;
         if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / C::kStages) & 1u, budget, abort_flag)) { give_up(); break; }
         if (!mbar_wait_bounded(&a_full[ab], (uint32_t)(kb / kABufs) & 1u, budget, abort_flag)) { give_up(); break; }
         if (kb <= G) {
@@ -388,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kb < G || kb == KB - 1) mma_commit(&acc_full[a & 1]);
       }
       if (any) {
-        mma_commit(mma_done);
-        (void)mbar_wait_bounded(mma_done, 0u, kDrainBudgetNs, nullptr);
+        mma_commit(&mma_done[par]);
+        (void)mbar_wait_bounded(&mma_done[par], 0u, kDrainBudgetNs, nullptr);
       }
     }
   } else if (warp < kEpiWarp0) {
