@@ -104,3 +104,27 @@ def test_row_independence_of_other_rows(q):
     X2[1::2] = X2[1::2] * 3.0
     Y2 = q.qlinear_pgemm(w, X2)
     assert torch.equal(Y[0::2], Y2[0::2])
+
+
+@pytest.mark.parametrize("bits,k", [(4, 6144), (6, 8192)])
+def test_several_tiles_per_cta_long_k(q, bits, k):
+    """More 128 x 256 tiles than SMs with a long k (5-6 bias blocks per tile): every
+    CTA walks several tiles, and the result must equal windows of 256 rows (one tile
+    each) bit for bit, with no timeout, and match the oracle on sampled rows."""
+    n, m = 2048, 4864  # 16 x 19 = 304 tiles
+    w = U.weight(n, k, bits, config_id=90, tensor_id=bits)
+    X = synth.make_x(m, k, config_id=90, tensor_id=1000 + bits)
+    wd, Xd = U.dev_weight(w), U.dev_x(X)
+    Y = q.qlinear_pgemm(wd, Xd)
+    torch.cuda.synchronize()
+    assert q.qlinear_last_error() == q.QL_OK
+    Yw = torch.empty_like(Y)
+    for lo in range(0, m, 256):
+        q.qlinear_pgemm(wd, Xd[lo:lo + 256], Y=Yw[lo:lo + 256])
+    torch.cuda.synchronize()
+    assert q.qlinear_last_error() == q.QL_OK
+    assert torch.equal(Yw, Y)
+    rows = np.random.default_rng(k).choice(m, size=24, replace=False)
+    rows.sort()
+    y64, A = orc.pgemm(X[rows], w)
+    U.assert_close(Y[torch.from_numpy(rows).cuda()], y64, A, f"pgemm several tiles bits={bits} k={k}")

@@ -13,10 +13,12 @@
 //               B = the X tile (256 rows), staged by TMA in shared memory; fresh
 //               accumulator per block, double-buffered in tensor memory
 //   y = fma(scale[n][b], P_b, y)  for b = 0..G-1 in order      (epilogue registers)
-//   Y = y + sum_b bias[n][b] * S_b[m]                            (added last)
+//   Y = (y + B_0) + B_1,  B_0 + B_1 = sum_b bias[n][b] * S_b[m]   (added last)
 // with S_b[m] = sum_{j in b} X[m][j] computed by a pre-pass in fp32 and split
 // exactly into three bf16 parts, so the bias term is one more small tcgen05
-// contraction (k' = 3G) instead of a second fma per element and block.
+// contraction (k' = 3G) instead of a second fma per element and block; its k blocks
+// alternate between the two accumulators like all others, giving two partial sums
+// B_0 (the part holding the first bias block) and B_1.
 // The tile is 128 channels x 256 rows: tcgen05.mma at M = 128, N = 256, K = 16 runs
 // close to the tensor peak, while N = 128 (or A read from tensor memory) reaches
 // well under half of it on this part.
@@ -30,10 +32,10 @@
 // Warp roles (one CTA per 128-channel x 256-row output tile, 736 threads):
 //   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block;
 //               scale and bias boxes)
-//   warps 1-2   MMA issuers (one thread each): warp 1 the even k blocks and
-//               accumulator 0, warp 2 the odd ones and accumulator 1 (the bias blocks go
-//               to the owner of accumulator G % 2); warp 1 also allocates TMEM (two
-//               accumulators of 256 columns)
+//   warps 1-2   MMA issuers (one thread each): warp 1 the even k blocks of the CTA's
+//               running block count and accumulator 0, warp 2 the odd ones and
+//               accumulator 1; warp 1 also allocates TMEM (two accumulators of 256
+//               columns)
 //   warps 3-6   converters: one channel row per thread, packed codes -> bf16 A tile
 //               in shared memory, scales -> fp32
 //   warps 7-22  epilogue: tensor memory -> registers, scale chain, bias add, store
@@ -68,7 +70,7 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiRows = BM / (kEpiWarps / 4);  // rows of X per epilogue thread
 constexpr int kXBytes = BM * BK * 2;            // X tile: BM rows x 64 bf16, 128-byte swizzle
 constexpr int kABytes = BN * BK * 2;            // converted W tile: 128 rows x 64 bf16, 128-byte swizzle
-constexpr int kABufs = 3;  // converted weight blocks the converters may run ahead of the MMA
+constexpr int kABufs = 5;  // converted weight blocks the converters may run ahead of the MMA
 constexpr int kTmemCols = 512;  // two accumulators of BM fp32 columns
 static_assert(2 * BM <= kTmemCols, "tensor memory budget");
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
@@ -79,7 +81,7 @@ static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converte
 template <int BITS> struct Cfg {
   static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
   static constexpr int kWBytes = BN * kRowBytes;         // packed W tile
-  static constexpr int kStages = BITS == 8 ? 3 : 4;      // TMA stages in flight (X/S tile + packed W tile)
+  static constexpr int kStages = 3;                      // TMA stages in flight (X/S tile + packed W tile)
   static constexpr int kOffX = 0;
   static constexpr int kOffW = kOffX + kStages * kXBytes;
   static constexpr int kOffA = (kOffW + kStages * kWBytes + 1023) / 1024 * 1024;
@@ -90,8 +92,8 @@ template <int BITS> struct Cfg {
   static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
   static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
   // barriers: tma_full, tma_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
-  //           sc_full, scb_full[2], scb_empty[2], bias_full, mma_done[2]
-  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 1 + 2;
+  //           sc_full, scb_full[2], scb_empty[2], bias_full, bias_empty, mma_done[2]
+  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;  // tmem address, abort flag
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -106,6 +108,7 @@ struct Params {
   float *Y;
   int64_t ldy;
   int M, N, G, NBB;
+  int tiles_n, tiles;  // 128-channel tiles per 256-row band; tiles in all
   int *status;
   uint64_t budget_ns;
 };
@@ -241,6 +244,11 @@ __device__ __forceinline__ void convert_chunk(const uint32_t (&w)[NW], int c, ui
 }
 
 // ---- the GEMM kernel -------------------------------------------------------------
+// Persistent: one CTA per SM walks the tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+// (128-channel tiles fastest, so CTAs working at the same time share 256-row bands of
+// X in L2).  Every role keeps running counters across tiles (k blocks g, main blocks
+// h, scale boxes, accumulator uses), so the next tile's copies, conversions and MMAs
+// overlap this tile's epilogue.
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     pgemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -266,12 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *scb_full = sc_full + kScStages;
   uint64_t *scb_empty = scb_full + 2;
   uint64_t *bias_full = scb_empty + 2;
-  uint64_t *mma_done = bias_full + 1;
+  uint64_t *bias_empty = bias_full + 1;
+  uint64_t *mma_done = bias_empty + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
   const int G = p.G, KB = p.G + p.NBB;
   const uint64_t budget = p.budget_ns;
 
@@ -289,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kScStages; ++i) mbar_init(&sc_full[i], kConvThreads);
     mbar_init(bias_full, 1);
+    mbar_init(bias_empty, kConvThreads);
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
     *abort_flag = 0;
@@ -318,82 +327,116 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      if (p.bi_tma) {
-        // every bias of the tile's channels, once (read only by the bias blocks at the end)
-        const int nbox = (G + 7) / 8;
-        mbar_arrive_expect_tx(bias_full, (uint32_t)(nbox * BN * 16));
-        for (int i = 0; i < nbox; ++i) tma_load_2d(sbias + i * BN * 8, &tmBi, bias_full, 8 * i, n0);
-      }
-      int sc_boxes = 0;
-      for (int kb = 0; kb < KB; ++kb) {
-        if (p.sc_tma && kb < G && (kb & 7) == 0) {
-          // scales of blocks kb .. kb+7 for the tile's channels, two boxes in flight
-          const int j = kb >> 3, slot = j & 1;
-          if (!mbar_wait_bounded(&scb_empty[slot], ((uint32_t)(j >> 1) & 1u) ^ 1u, budget, abort_flag)) {
+      int g = 0, box = 0, tj = 0, bias_sets = 0;
+      bool alive = true;
+      for (int t = blockIdx.x; t < p.tiles && alive; t += gridDim.x, ++tj) {
+        const int n0 = (t % p.tiles_n) * BN, m0 = (t / p.tiles_n) * BM;
+        if (p.bi_tma) {
+          // every bias of the tile's channels, once per tile (read only by its bias
+          // blocks), after the previous tile's bias blocks are converted
+          if (tj > 0 && !mbar_wait_bounded(bias_empty, (uint32_t)((tj - 1) & 1), budget, abort_flag)) {
             give_up();
             break;
           }
-          mbar_arrive_expect_tx(&scb_full[slot], (uint32_t)(BN * 16));
-          tma_load_2d(scbox + slot * BN * 8, &tmSc, &scb_full[slot], kb, n0);
-          sc_boxes = j + 1;
+          const int nbox = (G + 7) / 8;
+          mbar_arrive_expect_tx(bias_full, (uint32_t)(nbox * BN * 16));
+          for (int i = 0; i < nbox; ++i) tma_load_2d(sbias + i * BN * 8, &tmBi, bias_full, 8 * i, n0);
+          ++bias_sets;
         }
-        const int s = kb % C::kStages;
-        const uint32_t ph = (uint32_t)(kb / C::kStages) & 1u;
-        if (!mbar_wait_bounded(&tma_empty[s], ph ^ 1u, budget, abort_flag)) { give_up(); break; }
-        if (kb < G) {
-          mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
-          tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
-          tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
-        } else {
-          mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kXBytes);
-          tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (p.sc_tma && kb < G && (kb & 7) == 0) {
+            // scales of blocks kb .. kb+7 for the tile's channels, two boxes in flight
+            const int slot = box & 1;
+            if (!mbar_wait_bounded(&scb_empty[slot], ((uint32_t)(box >> 1) & 1u) ^ 1u, budget, abort_flag)) {
+              give_up();
+              alive = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&scb_full[slot], (uint32_t)(BN * 16));
+            tma_load_2d(scbox + slot * BN * 8, &tmSc, &scb_full[slot], kb, n0);
+            ++box;
+          }
+          const int s = g % C::kStages;
+          const uint32_t ph = (uint32_t)(g / C::kStages) & 1u;
+          if (!mbar_wait_bounded(&tma_empty[s], ph ^ 1u, budget, abort_flag)) {
+            give_up();
+            alive = false;
+            break;
+          }
+          if (kb < G) {
+            mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
+            tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
+            tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
+          } else {
+            mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kXBytes);
+            tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
+          }
+          ++g;
         }
-        issued = kb + 1;
       }
       // drain: every copy this CTA started must land before its shared memory goes away
-      for (int j = (sc_boxes > 2 ? sc_boxes - 2 : 0); j < sc_boxes; ++j)
+      for (int j = (box > 2 ? box - 2 : 0); j < box; ++j)
         (void)mbar_wait_bounded(&scb_full[j & 1], (uint32_t)(j >> 1) & 1u, kDrainBudgetNs, nullptr);
-      if (p.bi_tma) (void)mbar_wait_bounded(bias_full, 0u, kDrainBudgetNs, nullptr);
-      for (int s = 0; s < C::kStages && s < issued; ++s) {
-        const int uses = (issued - 1 - s) / C::kStages + 1;
+      if (bias_sets > 0) (void)mbar_wait_bounded(bias_full, (uint32_t)((bias_sets - 1) & 1), kDrainBudgetNs, nullptr);
+      for (int s = 0; s < C::kStages && s < g; ++s) {
+        const int uses = (g - 1 - s) / C::kStages + 1;
         (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
       }
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer `par` (warp 1: 0, warp 2: 1) owns the main blocks kb with kb % 2 == par and
-    // accumulator par; the bias blocks all chain into accumulator G % 2 and belong to its
-    // owner.  One issuer's barrier waits and commits overlap the other's MMAs.
+    // The k blocks of this CTA (all tiles, main and bias blocks) alternate between the
+    // two issuers and the two accumulators by their running index g: issuer par takes
+    // g % 2 == par into accumulator par.  A main block is one use of the accumulator;
+    // the bias blocks of a tile that fall to one issuer chain into one use (so each
+    // accumulator holds half of the bias contraction).  Strict alternation keeps each
+    // issuer at most one block ahead of the other, so no wait is ever more than one
+    // phase ahead of a barrier's last completion.
     const int par = warp - 1;
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BN, BM);
-      bool any = false;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int a = kb < G ? kb : G;
-        if ((a & 1) != par) continue;
-        const int s = kb % C::kStages, ab = kb % kABufs;
-        if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / C::kStages) & 1u, budget, abort_flag)) { give_up(); break; }
-        if (!mbar_wait_bounded(&a_full[ab], (uint32_t)(kb / kABufs) & 1u, budget, abort_flag)) { give_up(); break; }
-        if (kb <= G) {
-          if (!mbar_wait_bounded(&acc_empty[a & 1], ((uint32_t)(a >> 1) & 1u) ^ 1u, budget, abort_flag)) {
+      bool any = false, alive = true;
+      int g = 0, uses = 0;  // k blocks of this CTA so far; uses of accumulator par so far
+      for (int t = blockIdx.x; t < p.tiles && alive; t += gridDim.x) {
+        const int g0 = g;
+        // this issuer's first and last bias block of the tile
+        const int kb_first = G + ((g0 + G) % 2 == par ? 0 : 1);
+        const int kb_last = (g0 + KB - 1) % 2 == par ? KB - 1 : KB - 2;
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          if ((g & 1) != par) continue;
+          const int s = g % C::kStages, ab = g % kABufs;
+          if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
+              !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag)) {
             give_up();
+            alive = false;
             break;
           }
-        }
-        tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)((a & 1) * BM);
-        const uint64_t ad = sw128_desc(smem_addr(sA + ab * kABytes));
-        const uint64_t bd = sw128_desc(smem_addr(sX + s * kXBytes));
+          const bool opens = kb < G || kb == kb_first;   // a new use of the accumulator
+          const bool closes = kb < G || kb == kb_last;
+          if (opens) {  // the epilogue has read the accumulator's last use
+            if (!mbar_wait_bounded(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
+              give_up();
+              alive = false;
+              break;
+            }
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + (uint32_t)(par * BM);
+          const uint64_t ad = sw128_desc(smem_addr(sA + ab * kABytes));
+          const uint64_t bd = sw128_desc(smem_addr(sX + s * kXBytes));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint32_t acc = (kk > 0 || kb > G) ? 1u : 0u;
-          mma_bf16_ss(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t acc = (kk > 0 || !opens) ? 1u : 0u;
+            mma_bf16_ss(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
+          }
+          any = true;
+          mma_commit(&tma_empty[s]);
+          mma_commit(&a_empty[ab]);
+          if (closes) {
+            mma_commit(&acc_full[par]);
+            ++uses;
+          }
         }
-        any = true;
-        mma_commit(&tma_empty[s]);
-        mma_commit(&a_empty[ab]);
-        if (kb < G || kb == KB - 1) mma_commit(&acc_full[a & 1]);
       }
       if (any) {
         mma_commit(&mma_done[par]);
@@ -407,120 +450,132 @@ __global__ void __launch_bounds__(kThreads, 1)
     // UMMA 128-byte-swizzle K-major layout: 8-row groups 1024 bytes apart, rows 128
     // bytes apart, chunk c of row r at position c ^ (r % 8).
     const int ct = 32 * (warp & 3) + lane;  // channel (row of the W tile)
-    const int n = n0 + ct;
-    const bool nvalid = n < p.N;
-    const uint16_t *srow = p.scales + (size_t)(nvalid ? n : 0) * G;
-    const uint16_t *brow = p.biases + (size_t)(nvalid ? n : 0) * G;
     const bool bias_smem = G <= kBiasG;
     const uint32_t a_row = smem_addr(sA) + (uint32_t)((ct >> 3) * 1024 + (ct & 7) * 128);
     const uint32_t sw = (uint32_t)(ct & 7);
-    // Without TMA boxes (k % 512 != 0), the thread loads its channel's scale and bias
-    // itself, kPf blocks ahead; the loop is unrolled by kPf so that each ring slot
-    // stays in place while its load is in flight.
-    uint32_t sr[kPf], br[kPf];
-#pragma unroll
-    for (int i = 0; i < kPf; ++i) {
-      sr[i] = (!p.sc_tma && nvalid && i < G) ? ldg_u16(srow + i) : 0u;
-      br[i] = (!p.bi_tma && bias_smem && nvalid && i < G) ? ldg_u16(brow + i) : 0u;
-    }
     bool alive = true;
-    for (int kb0 = 0; kb0 < KB && alive; kb0 += kPf) {
+    int g = 0, h = 0, box = 0, tj = 0;  // k blocks, main blocks, scale boxes, tiles
+    for (int t = blockIdx.x; t < p.tiles && alive; t += gridDim.x, ++tj) {
+      const int n = (t % p.tiles_n) * BN + ct;
+      const bool nvalid = n < p.N;
+      const uint16_t *srow = p.scales + (size_t)(nvalid ? n : 0) * G;
+      const uint16_t *brow = p.biases + (size_t)(nvalid ? n : 0) * G;
+      // Without TMA boxes (k % 512 != 0), the thread loads its channel's scale and bias
+      // itself, kPf blocks ahead; the loop is unrolled by kPf so that each ring slot
+      // stays in place while its load is in flight.
+      uint32_t sr[kPf], br[kPf];
 #pragma unroll
-      for (int u = 0; u < kPf; ++u) {
-        const int kb = kb0 + u;
-        if (kb >= KB || !alive) break;
-        const int s = kb % C::kStages, ab = kb % kABufs;
-        uint32_t s_cur = 0u, b_cur = 0u;
-        if (kb < G) {
-          if (p.sc_tma) {
-            const int j = kb >> 3, slot = j & 1;
-            if ((kb & 7) == 0 &&
-                !mbar_wait_bounded(&scb_full[slot], (uint32_t)(j >> 1) & 1u, budget, abort_flag)) {
-              give_up();
-              alive = false;
-              break;
+      for (int i = 0; i < kPf; ++i) {
+        sr[i] = (!p.sc_tma && nvalid && i < G) ? ldg_u16(srow + i) : 0u;
+        br[i] = (!p.bi_tma && bias_smem && nvalid && i < G) ? ldg_u16(brow + i) : 0u;
+      }
+      for (int kb0 = 0; kb0 < KB && alive; kb0 += kPf) {
+#pragma unroll
+        for (int u = 0; u < kPf; ++u) {
+          const int kb = kb0 + u;
+          if (kb >= KB || !alive) break;
+          const int s = g % C::kStages, ab = g % kABufs;
+          uint32_t s_cur = 0u, b_cur = 0u;
+          if (kb < G) {
+            if (p.sc_tma) {
+              const int slot = box & 1;
+              if ((kb & 7) == 0 &&
+                  !mbar_wait_bounded(&scb_full[slot], (uint32_t)(box >> 1) & 1u, budget, abort_flag)) {
+                give_up();
+                alive = false;
+                break;
+              }
+              s_cur = scbox[(slot * BN + ct) * 8 + (kb & 7)];
+              if ((kb & 7) == 7 || kb == G - 1) {
+                mbar_arrive(&scb_empty[slot]);
+                ++box;
+              }
+            } else {
+              s_cur = sr[u];
+              sr[u] = (nvalid && kb + kPf < G) ? ldg_u16(srow + kb + kPf) : 0u;
             }
-            s_cur = scbox[(slot * BN + ct) * 8 + (kb & 7)];
-            if ((kb & 7) == 7 || kb == G - 1) mbar_arrive(&scb_empty[slot]);
-          } else {
-            s_cur = sr[u];
-            sr[u] = (nvalid && kb + kPf < G) ? ldg_u16(srow + kb + kPf) : 0u;
+            if (!p.bi_tma && bias_smem) {
+              b_cur = br[u];
+              br[u] = (nvalid && kb + kPf < G) ? ldg_u16(brow + kb + kPf) : 0u;
+            }
           }
-          if (!p.bi_tma && bias_smem) {
-            b_cur = br[u];
-            br[u] = (nvalid && kb + kPf < G) ? ldg_u16(brow + kb + kPf) : 0u;
-          }
-        }
-        if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(kb / C::kStages) & 1u, budget, abort_flag) ||
-            !mbar_wait_bounded(&a_empty[ab], ((uint32_t)(kb / kABufs) & 1u) ^ 1u, budget, abort_flag)) {
-          give_up();
-          alive = false;
-          break;
-        }
-        const uint32_t dst = a_row + (uint32_t)(ab * kABytes);
-        if (kb < G) {
-          constexpr int NW = BK * BITS / 32;  // words of the row
-          uint32_t w[NW];
-          const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes;
-#pragma unroll
-          for (int i = 0; i < NW / 4; ++i) {
-            uint4 v = lds128(wp + 16 * i);
-            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-          }
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t o[4];
-            convert_chunk<BITS, NW>(w, c, o);
-            sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
-          }
-          if (!p.bi_tma && bias_smem) sbias[((kb >> 3) * BN + ct) * 8 + (kb & 7)] = (uint16_t)b_cur;
-          // Scale slot kb % kScStages was last read by the epilogue for block
-          // kb - kScStages.  Passing a_empty for this block means the MMA of block
-          // kb - kABufs finished, which waited for the epilogue to release block
-          // kb - kABufs - 2; kScStages >= kABufs + 3 keeps the slot free.
-          sSc[(kb % kScStages) * BN + ct] = bf16_to_f32(s_cur);
-        } else {
-          // bias block: column t of block jb is k' = 64*jb + t of the [part][group]
-          // layout; its A value is bias[n][k' mod G] (zero past 3G)
-          if (kb == G && p.bi_tma && !mbar_wait_bounded(bias_full, 0u, budget, abort_flag)) {
+          if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
+              !mbar_wait_bounded(&a_empty[ab], ((uint32_t)(g / kABufs) & 1u) ^ 1u, budget, abort_flag)) {
             give_up();
             alive = false;
             break;
           }
-          const int base = (kb - G) * BK;
+          const uint32_t dst = a_row + (uint32_t)(ab * kABytes);
+          if (kb < G) {
+            constexpr int NW = BK * BITS / 32;  // words of the row
+            uint32_t w[NW];
+            const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t o[4] = {0u, 0u, 0u, 0u};
-            int j = base + 8 * c;
-            if (bias_smem && (G % 8) == 0) {
-              // a run of 8 columns never crosses a multiple of G: one 16-byte row of a
-              // staged bias box
-              if (nvalid && j < 3 * G) {
-                if (j >= G) j -= G;
-                if (j >= G) j -= G;
-                const uint4 v = lds128(sbias + ((j >> 3) * BN + ct) * 8);
-                o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                int jj = j + e;
-                uint32_t v = 0u;
-                if (nvalid && jj < 3 * G) {
-                  if (jj >= G) jj -= G;
-                  if (jj >= G) jj -= G;
-                  v = bias_smem ? (uint32_t)sbias[((jj >> 3) * BN + ct) * 8 + (jj & 7)] : ldg_u16(brow + jj);
-                }
-                o[e >> 1] |= v << (16 * (e & 1));
-              }
+            for (int i = 0; i < NW / 4; ++i) {
+              uint4 v = lds128(wp + 16 * i);
+              w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
             }
-            sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint32_t o[4];
+              convert_chunk<BITS, NW>(w, c, o);
+              sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+            }
+            if (!p.bi_tma && bias_smem) sbias[((kb >> 3) * BN + ct) * 8 + (kb & 7)] = (uint16_t)b_cur;
+            // Scale slot h % kScStages was last read by the epilogue for main block
+            // h - kScStages.  Passing a_empty for this block means the MMA of the block
+            // kABufs earlier finished, which waited for the epilogue to release the
+            // accumulator use two main blocks before that; kScStages >= kABufs + 3 keeps
+            // the slot free.
+            sSc[(h % kScStages) * BN + ct] = bf16_to_f32(s_cur);
+          } else {
+            // bias block: column t of block jb is k' = 64*jb + t of the [part][group]
+            // layout; its A value is bias[n][k' mod G] (zero past 3G)
+            if (kb == G && p.bi_tma && !mbar_wait_bounded(bias_full, (uint32_t)(tj & 1), budget, abort_flag)) {
+              give_up();
+              alive = false;
+              break;
+            }
+            const int base = (kb - G) * BK;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint32_t o[4] = {0u, 0u, 0u, 0u};
+              int j = base + 8 * c;
+              if (bias_smem && (G % 8) == 0) {
+                // a run of 8 columns never crosses a multiple of G: one 16-byte row of a
+                // staged bias box
+                if (nvalid && j < 3 * G) {
+                  if (j >= G) j -= G;
+                  if (j >= G) j -= G;
+                  const uint4 v = lds128(sbias + ((j >> 3) * BN + ct) * 8);
+                  o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  int jj = j + e;
+                  uint32_t v = 0u;
+                  if (nvalid && jj < 3 * G) {
+                    if (jj >= G) jj -= G;
+                    if (jj >= G) jj -= G;
+                    v = bias_smem ? (uint32_t)sbias[((jj >> 3) * BN + ct) * 8 + (jj & 7)] : ldg_u16(brow + jj);
+                  }
+                  o[e >> 1] |= v << (16 * (e & 1));
+                }
+              }
+              sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+            }
           }
+          fence_proxy_async_smem();  // the A tile is read by the tensor core (async proxy)
+          mbar_arrive(&a_full[ab]);
+          if (kb < G) {
+            mbar_arrive(&sc_full[h % kScStages]);
+            ++h;
+          }
+          mbar_arrive(&tma_empty[s]);
+          if (kb == KB - 1) mbar_arrive(bias_empty);  // the tile's bias boxes are read
+          ++g;
         }
-        fence_proxy_async_smem();  // the A tile is read by the tensor core (async proxy)
-        mbar_arrive(&a_full[ab]);
-        if (kb < G) mbar_arrive(&sc_full[kb % kScStages]);
-        mbar_arrive(&tma_empty[s]);
       }
     }
   } else {
@@ -530,53 +585,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int slice = (warp - kEpiWarp0) >> 2;
     const int ch_row = 32 * q + lane;  // output channel of this thread within the tile
     const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(slice * CW);
-    float y[CW];
-#pragma unroll
-    for (int i = 0; i < CW; ++i) y[i] = 0.0f;
+    int uses[2] = {0, 0};  // completed uses of each accumulator
+    int h = 0;             // main blocks so far
+    int g0 = 0;            // running index of the tile's first k block (as the issuers count)
     bool ok = true;
-    for (int kb = 0; kb < G; ++kb) {
-      const int buf = kb & 1, sc = kb % kScStages;
-      bool w_ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)(kb >> 1) & 1u, budget, abort_flag) &&
-                  mbar_wait_bounded(&sc_full[sc], (uint32_t)(kb / kScStages) & 1u, budget, abort_flag);
-      if (!__all_sync(0xffffffffu, w_ok)) {
-        give_up();
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const float sv = sSc[sc * BN + ch_row];
+    for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, g0 += KB) {
+      const int n0 = (t % p.tiles_n) * BN, m0 = (t / p.tiles_n) * BM;
+      float y[CW];
 #pragma unroll
-      for (int ch = 0; ch < CW / 8; ++ch) {
-        uint32_t r[8];
-        tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * ch), r);
-        tmem_wait_ld();
+      for (int i = 0; i < CW; ++i) y[i] = 0.0f;
+      for (int kb = 0; kb < G; ++kb, ++h) {
+        const int buf = (g0 + kb) & 1, sc = h % kScStages;
+        bool w_ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)uses[buf] & 1u, budget, abort_flag) &&
+                    mbar_wait_bounded(&sc_full[sc], (uint32_t)(h / kScStages) & 1u, budget, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float sv = sSc[sc * BN + ch_row];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          ffma2(y[8 * ch + 2 * i], y[8 * ch + 2 * i + 1], sv, sv, __uint_as_float(r[2 * i]),
-                __uint_as_float(r[2 * i + 1]));
-      }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
-    }
-    if (ok) {
-      bool w_ok = mbar_wait_bounded(&acc_full[G & 1], (uint32_t)(G >> 1) & 1u, budget, abort_flag);
-      if (!__all_sync(0xffffffffu, w_ok)) {
-        give_up();
-        ok = false;
-      }
-    }
-    if (ok) {
-      tc_fence_after();
-      const int buf = G & 1;
+        for (int ch = 0; ch < CW / 8; ++ch) {
+          uint32_t r[8];
+          tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * ch), r);
+          tmem_wait_ld();
 #pragma unroll
-      for (int ch = 0; ch < CW / 8; ++ch) {
-        uint32_t r[8];
-        tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * ch), r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y[8 * ch + i] = __fadd_rn(y[8 * ch + i], __uint_as_float(r[i]));
+          for (int i = 0; i < 4; ++i)
+            ffma2(y[8 * ch + 2 * i], y[8 * ch + 2 * i + 1], sv, sv, __uint_as_float(r[2 * i]),
+                  __uint_as_float(r[2 * i + 1]));
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        ++uses[buf];
       }
-      tc_fence_before();
+      if (!ok) break;
+      // the bias contraction of the tile: its blocks alternate between the two
+      // accumulators; the part of the tile's first bias block is added first.  Each
+      // accumulator is released before the stores, so the next tile's MMAs can start
+      // while this tile is written out.
+      const int nparts = p.NBB >= 2 ? 2 : 1;
+      for (int part = 0; part < nparts && ok; ++part) {
+        const int buf = (g0 + G + part) & 1;
+        bool w_ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)uses[buf] & 1u, budget, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < CW / 8; ++ch) {
+          uint32_t r[8];
+          tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * ch), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[8 * ch + i] = __fadd_rn(y[8 * ch + i], __uint_as_float(r[i]));
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        ++uses[buf];
+      }
+      if (!ok) break;
       // one channel per thread: lanes of a warp write 32 consecutive channels of a row
       const int n = n0 + ch_row;
       if (n < p.N) {
@@ -689,6 +759,19 @@ static void *scratch_get(size_t bytes) {
   return g_scratch[dev];
 }
 
+// SMs of the current device (cached per device)
+static int sm_count() {
+  static int cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
+  if (cached[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
 template <int BITS>
 static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
                         const uint16_t *S, int64_t lds, cudaStream_t st, int *status) {
@@ -736,7 +819,9 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   p.NBB = (int)(lds / pg::BK);
   p.status = status;
   p.budget_ns = wait_budget_ns();
-  dim3 grid((unsigned)((w->n + pg::BN - 1) / pg::BN), (unsigned)((m + pg::BM - 1) / pg::BM));
+  p.tiles_n = (w->n + pg::BN - 1) / pg::BN;
+  p.tiles = p.tiles_n * ((m + pg::BM - 1) / pg::BM);
+  const int grid = p.tiles < sm_count() ? p.tiles : sm_count();  // persistent: one CTA per SM
   pg::pgemm_kernel<BITS><<<grid, pg::kThreads, C::kAlloc, st>>>(tmX, tmW, tmS, tmSc, tmBi, p);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   return QL_OK;
