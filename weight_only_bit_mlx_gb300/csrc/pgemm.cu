@@ -70,11 +70,11 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiRows = BM / (kEpiWarps / 4);  // rows of X per epilogue thread
 constexpr int kXBytes = BM * BK * 2;            // X tile: BM rows x 64 bf16, 128-byte swizzle
 constexpr int kABytes = BN * BK * 2;            // converted W tile: 128 rows x 64 bf16, 128-byte swizzle
-constexpr int kABufs = 5;  // converted weight blocks the converters may run ahead of the MMA
+constexpr int kABufs = 4;  // converted weight blocks the converters may run ahead of the MMA
 constexpr int kTmemCols = 512;  // two accumulators of BM fp32 columns
 static_assert(2 * BM <= kTmemCols, "tensor memory budget");
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
-constexpr int kBiasG = 64;   // groups of bias staged in shared memory (k <= 4096); larger k reads global
+constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
 constexpr int kPf = 2;       // k blocks of scale/bias prefetch (no-TMA path)
 static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
 
