@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--bits", type=int, default=4, choices=[4, 6, 8])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default=None, choices=["pgemm", "ffn", "mv"],
+    ap.add_argument("--case", default=None, choices=["pgemm", "ffn", "mv", "window"],
                     help="run only one kernel (for profiler captures): warm-up launches, then --steps launches")
     ap.add_argument("--m", type=int, default=PROMPT, help="--case pgemm: rows of X")
     ap.add_argument("--n", type=int, default=D_FF, help="--case: output channels")
@@ -443,11 +443,16 @@ def run_ours(args):
                    "l2": "no flush: every decode pass streams 502 MB of distinct weights (> 129 MB L2)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "decode_r1": {"GB/s": value / world, "frac_of_hbm": value / world / pk["hbm"],
-                      "ms_per_pass": d1_ms / args.steps, "bytes_per_pass": d1_bytes},
+                      "ms_per_pass": d1_ms / args.steps, "bytes_per_pass": d1_bytes,
+                      "tok_s_modelled": 1.0 / (d1_ms / args.steps * 1e-3)},
         "decode_r16": {"GB/s": d16_gbs / world, "frac_of_hbm": d16_gbs / world / pk["hbm"],
-                       "ms_per_pass": d16_ms / args.steps, "bytes_per_pass": d16_bytes},
+                       "ms_per_pass": d16_ms / args.steps, "bytes_per_pass": d16_bytes,
+                       "tok_s_modelled": 16.0 / (d16_ms / args.steps * 1e-3)},
         "prefill": {"TFLOP/s": pf_tflops / world, "ms_per_pass": pf_ms / args.steps,
-                    "flops_per_pass": prefill_flops(), "includes": "pgemm (row-sum pre-pass + GEMM) and SwiGLU"},
+                    "flops_per_pass": prefill_flops(), "includes": "pgemm (row-sum pre-pass + GEMM) and SwiGLU",
+                    "tok_s_modelled": PROMPT / (gemm_ms / args.steps * 1e-3)},
+        "tok_s_note": "modelled from the linear layers only: decode R / (decode pass time), prefill "
+                      "prompt rows / (sum of the pass's pgemm times); attention, norms and sampling excluded",
         "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm (row-sum pre-pass + tcgen05 GEMM)",
                      "achieved": gemm_tflops, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                      "frac": gemm_tflops / pk["bf16_sus"], "traffic": traffic,
@@ -487,6 +492,8 @@ def run_case(args):
         b = (torch.rand(n, k // 64, generator=gen, device=dev) * 0.2 - 0.1).to(torch.bfloat16)
         return q.QWeight(wq, s, b, k, bits)
 
+    if args.case == "window":
+        return window_table(args, q, w, gen, dev)
     if args.case == "pgemm":
         wt = w()
         X = torch.randn(args.m, k, generator=gen, device=dev).to(torch.bfloat16)
@@ -531,6 +538,53 @@ def run_case(args):
                       "copies": args.copies,
                       "us_per_launch": ms * 1e3, unit: work / (ms * 1e-3) / scale,
                       "status": q.qlinear_last_error()}), flush=True)
+
+
+def window_table(args, q, make_w, gen, dev):
+    """Cost of one window of R rows through qlinear_mv_rows (R <= 16) and through
+    qlinear_pgemm (any R), with enough distinct weight copies cycled to exceed L2, so
+    every call streams its weights from HBM.  Prints the table and, per R, which call
+    is cheaper (a window of more than 16 rows can only take the GEMM)."""
+    import torch
+    n, k = args.n, args.k
+    props = torch.cuda.get_device_properties(dev)
+    wbytes = weight_bytes(n, k, args.bits)
+    copies = max(2, int(2 * props.L2_cache_size // wbytes) + 1)
+    ws = [make_w() for _ in range(copies)]
+    it = [0]
+
+    def timed(fn, reps=60):
+        for _ in range(copies):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3  # us per call
+
+    rows_list = [1, 2, 4, 8, 16, 32, 64, 128, 256]
+    table = []
+    for R in rows_list:
+        X = torch.randn(R, k, generator=gen, device=dev).to(torch.bfloat16)
+        Y = torch.empty(R, n, device=dev)
+
+        def nxt():
+            wt = ws[it[0] % copies]
+            it[0] += 1
+            return wt
+        mv = timed(lambda: q.qlinear_mv_rows(nxt(), X, Y)) if R <= 16 else None
+        pg = timed(lambda: q.qlinear_pgemm(nxt(), X, Y))
+        best = "qlinear_mv_rows" if mv is not None and mv <= pg else "qlinear_pgemm"
+        table.append({"rows": R, "mv_rows_us": mv, "pgemm_us": pg, "cheaper": best,
+                      "us_per_row": min(x for x in (mv, pg) if x is not None) / R})
+    # linear interpolation of the per-call cost between measured window sizes
+    print(json.dumps({"case": "window", "bits": args.bits, "n": n, "k": k, "weight_copies": copies,
+                      "weight_bytes": wbytes, "table": table,
+                      "interpolation": "cost(R) for R between two measured sizes is the linear interpolation "
+                                       "of their per-call costs", "status": q.qlinear_last_error()}), flush=True)
 
 
 def main():

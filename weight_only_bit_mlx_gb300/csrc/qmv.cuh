@@ -40,6 +40,9 @@ struct MvParams {
   int cs;                // CTAs per cluster along k
 };
 
+// groups per k-span of one CTA for the given code width
+int mv_span_g(int bits);
+
 // k-decomposition used by every decode launch (a function of k and bits only)
 void mv_geometry(int k, int bits, int &groups, int &span_g, int &nwarps, int &cs);
 
