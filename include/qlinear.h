@@ -172,6 +172,55 @@ int qswiglu(const float *a, const float *c, int32_t rows, int32_t n, int64_t lda
             uint16_t *h, int64_t ldh, void *stream);
 
 /*
+ * qattn_qknorm_rope_kv - the step after the attention projections for 1..16 decode
+ * streams: QK norm, partial RoPE and the KV store.  [P1696] "What it adds" ("QK norm
+ * with partial RoPE"; decode fuses RoPE with the KV store; per-stream KV rings).  The
+ * pages print no formula; the definitions (the plain ones, every constant an argument):
+ *   norm:  xhat_j = x_j / sqrt(mean_j x_j^2 + eps) * w_j over each head_dim-long head,
+ *          w = q_norm_w for q heads, k_norm_w for k heads (bf16 [head_dim] each);
+ *   RoPE:  rotate-half on the first rot_dim dims of each normed q and k head, at
+ *          position pos[r]: theta_i = pos[r] * rope_base^(-2i/rot_dim), i < rot_dim/2,
+ *          (a, b) = (x_i, x_{i+rot_dim/2}) -> (a cos - b sin, a sin + b cos);
+ *          dims rot_dim..head_dim-1 pass through;
+ *   store: q_out[r] = bf16(rotated q); k and v (v unchanged) of stream r, rounded to
+ *          bf16, into slot s = pos[r] mod ring_len (the non-negative remainder) of
+ *          stream r's rings.
+ * Arithmetic: fp32 for the norm and the rotation (fixed-order sums, so results are
+ * deterministic), the angle and its cos/sin in float64, one nearest-even rounding to
+ * bf16 per output.
+ *   q: float [rows, ldq] (n_q_heads*head_dim used); k, v: float [rows, ldk/ldv]
+ *   (n_kv_heads*head_dim used) - the outputs of qattn_proj_mv;
+ *   pos: int32 [rows] (device); q_out: bf16 bits [rows, ldqo];
+ *   k_ring, v_ring: bf16 bits [rows][ring_len][n_kv_heads*head_dim], slot s of stream r
+ *   at element offset (r*ring_len + s)*n_kv_heads*head_dim; other slots are untouched.
+ *   Requires 1 <= rows <= 16, head_dim a multiple of 32 in 32..256, rot_dim even in
+ *   0..head_dim, ring_len >= 1, rope_base > 0, eps >= 0 (else QL_ERR_ROWS/QL_ERR_SHAPE);
+ *   float pointers 4-byte and bf16 pointers 2-byte aligned and leading dimensions at
+ *   least the used widths (else QL_ERR_ALIGN).
+ */
+int qattn_qknorm_rope_kv(const float *q, int64_t ldq, const float *k, int64_t ldk, const float *v,
+                         int64_t ldv, int32_t rows, int32_t n_q_heads, int32_t n_kv_heads,
+                         int32_t head_dim, int32_t rot_dim, float rope_base, float eps,
+                         const uint16_t *q_norm_w, const uint16_t *k_norm_w, const int32_t *pos,
+                         uint16_t *q_out, int64_t ldqo, uint16_t *k_ring, uint16_t *v_ring,
+                         int32_t ring_len, void *stream);
+
+/*
+ * qresid_rmsnorm - post-add / next-norm after the w2 or o projection.  [P1514] "What
+ * changes" (post-add/next-norm fusion keeping the retained rounding boundaries).  The
+ * residual stream is stored in bf16: resid[r][j] <- bf16(resid[r][j] + y[r][j]), and
+ * out[r][j] = bf16(r'_j / sqrt(mean_j r'_j^2 + eps) * gamma_j), computed from the
+ * stored (rounded) r'.  fp32 arithmetic, fixed-order sums, nearest-even rounding.
+ *   y: float [rows, ldy]; resid: bf16 bits [rows, ldr], read and overwritten;
+ *   gamma: bf16 bits [n]; out: bf16 bits [rows, ldo] (must not overlap resid).
+ *   Requires rows >= 1 (QL_ERR_ROWS), n >= 1 and eps >= 0 (QL_ERR_SHAPE), aligned
+ *   pointers and leading dimensions >= n (QL_ERR_ALIGN).
+ */
+int qresid_rmsnorm(const float *y, int64_t ldy, uint16_t *resid, int64_t ldr, int32_t rows,
+                   int32_t n, const uint16_t *gamma, float eps, uint16_t *out, int64_t ldo,
+                   void *stream);
+
+/*
  * qlinear_last_error - synchronizes `stream`, then returns and clears the device
  * status word: QL_OK, or QL_ERR_TIMEOUT if a bounded device-side wait gave up in a
  * kernel enqueued since the last call.  Returns QL_ERR_CUDA if synchronization fails.

@@ -102,3 +102,38 @@ def test_bad_rows_and_layout_rejected_on_host(q):
 def test_wait_budget_setter(q):
     old = q.qlinear_set_wait_budget_ns(12345)
     assert q.qlinear_set_wait_budget_ns(old) == 12345
+
+
+def test_post_ops_reject_bad_arguments_on_host(q):
+    L = q.LIB
+    P = 0x40000
+    args = dict(q=P, ldq=2048, k=P, ldk=512, v=P, ldv=512, rows=1, nq=32, nkv=8, hd=64, rot=64, base=1e4, eps=1e-5,
+                qw=P, kw=P, pos=P, qo=P, ldqo=2048, kr=P, vr=P, L=16)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.qattn_qknorm_rope_kv(a["q"], a["ldq"], a["k"], a["ldk"], a["v"], a["ldv"], a["rows"], a["nq"],
+                                      a["nkv"], a["hd"], a["rot"], a["base"], a["eps"], a["qw"], a["kw"], a["pos"],
+                                      a["qo"], a["ldqo"], a["kr"], a["vr"], a["L"], None)
+
+    assert call(q=0) == q.QL_ERR_NULL
+    assert call(pos=0) == q.QL_ERR_NULL
+    assert call(rows=0) == q.QL_ERR_ROWS
+    assert call(rows=17) == q.QL_ERR_ROWS
+    assert call(hd=48) == q.QL_ERR_SHAPE
+    assert call(hd=288) == q.QL_ERR_SHAPE
+    assert call(rot=66) == q.QL_ERR_SHAPE
+    assert call(rot=63) == q.QL_ERR_SHAPE
+    assert call(L=0) == q.QL_ERR_SHAPE
+    assert call(base=0.0) == q.QL_ERR_SHAPE
+    assert call(eps=-1.0) == q.QL_ERR_SHAPE
+    assert call(ldq=2047) == q.QL_ERR_ALIGN
+    assert call(ldqo=100) == q.QL_ERR_ALIGN
+    assert call(k=P + 2) == q.QL_ERR_ALIGN
+    assert L.qresid_rmsnorm(0, 8, P, 8, 1, 8, P, 1e-5, P, 8, None) == q.QL_ERR_NULL
+    assert L.qresid_rmsnorm(P, 8, P, 8, 0, 8, P, 1e-5, P, 8, None) == q.QL_ERR_ROWS
+    assert L.qresid_rmsnorm(P, 8, P, 8, 1, 0, P, 1e-5, P, 8, None) == q.QL_ERR_SHAPE
+    assert L.qresid_rmsnorm(P, 8, P, 8, 1, 8, P, -1.0, P, 8, None) == q.QL_ERR_SHAPE
+    assert L.qresid_rmsnorm(P, 7, P, 8, 1, 8, P, 1e-5, P, 8, None) == q.QL_ERR_ALIGN
+    assert L.qresid_rmsnorm(P + 1, 8, P, 8, 1, 8, P, 1e-5, P, 8, None) == q.QL_ERR_ALIGN

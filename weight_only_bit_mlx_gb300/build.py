@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqlinear.so")
-SOURCES = ["abi.cu", "qmv.cu", "pgemm.cu"]
+SOURCES = ["abi.cu", "qmv.cu", "pgemm.cu", "qpost.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -58,6 +58,9 @@ def _load() -> ctypes.CDLL:
         "qlinear_pgemm": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
         "qlinear_pgemm_noalloc": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
         "qswiglu": (ctypes.c_int, [P, P, I32, I32, I64, P, I64, P]),
+        "qattn_qknorm_rope_kv": (ctypes.c_int, [P, I64, P, I64, P, I64, I32, I32, I32, I32, I32, ctypes.c_float,
+                                                ctypes.c_float, P, P, P, P, I64, P, P, I32, P]),
+        "qresid_rmsnorm": (ctypes.c_int, [P, I64, P, I64, I32, I32, P, ctypes.c_float, P, I64, P]),
         "qlinear_last_error": (ctypes.c_int, [P]),
         "qlinear_set_wait_budget_ns": (U64, [U64]),
         "qlinear_wait_probe": (ctypes.c_int, [U64, P]),
@@ -214,6 +217,64 @@ def qswiglu(a: torch.Tensor, c: torch.Tensor, h: torch.Tensor | None = None, str
     _check(LIB.qswiglu(a2.data_ptr(), c2.data_ptr(), rows, n, a2.stride(0), h.data_ptr(), h.stride(0),
                        _stream(stream)), "qswiglu")
     return h
+
+
+def _rows2d(t: torch.Tensor, dtype, what: str) -> torch.Tensor:
+    if t.dtype != dtype or not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA {dtype} tensor")
+    t = t.view(1, -1) if t.dim() == 1 else t
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{what} must be [rows, n] with unit column stride")
+    return t
+
+
+def qattn_qknorm_rope_kv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_q_heads: int, n_kv_heads: int,
+                         head_dim: int, rot_dim: int, rope_base: float, eps: float, q_norm_w: torch.Tensor,
+                         k_norm_w: torch.Tensor, pos: torch.Tensor, k_ring: torch.Tensor, v_ring: torch.Tensor,
+                         q_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """QK norm + partial RoPE of q and k, k/v into slot pos % ring_len of each stream's
+    rings.  q, k, v: float32 [rows, *]; q_norm_w, k_norm_w: bfloat16 [head_dim];
+    pos: int32 [rows]; k_ring, v_ring: bfloat16 [rows, ring_len, n_kv_heads*head_dim]
+    (contiguous).  Returns q_out (bfloat16 [rows, n_q_heads*head_dim])."""
+    q, k, v = (_rows2d(t, torch.float32, nm) for t, nm in ((q, "q"), (k, "k"), (v, "v")))
+    rows = int(q.shape[0])
+    if k.shape[0] != rows or v.shape[0] != rows or pos.numel() != rows or pos.dtype != torch.int32:
+        raise ValueError("q, k, v and pos must have one row / entry per stream (pos int32)")
+    for t, nm in ((q_norm_w, "q_norm_w"), (k_norm_w, "k_norm_w")):
+        if t.dtype != torch.bfloat16 or t.numel() != head_dim or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous bfloat16 [head_dim] tensor")
+    width = n_kv_heads * head_dim
+    for t, nm in ((k_ring, "k_ring"), (v_ring, "v_ring")):
+        if t.dtype != torch.bfloat16 or t.dim() != 3 or t.shape[0] != rows or t.shape[2] != width or \
+                not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous bfloat16 [rows, ring_len, {width}] tensor")
+    if k_ring.shape != v_ring.shape:
+        raise ValueError("k_ring and v_ring must have one shape")
+    if q_out is None:
+        q_out = torch.empty(rows, n_q_heads * head_dim, dtype=torch.bfloat16, device=q.device)
+    _check(LIB.qattn_qknorm_rope_kv(q.data_ptr(), q.stride(0), k.data_ptr(), k.stride(0), v.data_ptr(), v.stride(0),
+                                    rows, n_q_heads, n_kv_heads, head_dim, rot_dim, float(rope_base), float(eps),
+                                    q_norm_w.data_ptr(), k_norm_w.data_ptr(), pos.data_ptr(), q_out.data_ptr(),
+                                    q_out.stride(0), k_ring.data_ptr(), v_ring.data_ptr(), int(k_ring.shape[1]),
+                                    _stream(stream)), "qattn_qknorm_rope_kv")
+    return q_out
+
+
+def qresid_rmsnorm(y: torch.Tensor, resid: torch.Tensor, gamma: torch.Tensor, eps: float,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """resid <- bf16(resid + y) in place; returns out = bf16(rmsnorm(resid) * gamma).
+    y: float32 [rows, n]; resid: bfloat16 [rows, n]; gamma: bfloat16 [n]."""
+    y = _rows2d(y, torch.float32, "y")
+    r = _rows2d(resid, torch.bfloat16, "resid")
+    rows, n = int(y.shape[0]), int(y.shape[1])
+    if tuple(r.shape) != (rows, n) or gamma.dtype != torch.bfloat16 or gamma.numel() != n or \
+            not gamma.is_contiguous():
+        raise ValueError("resid must be [rows, n] like y and gamma a contiguous bfloat16 [n]")
+    if out is None:
+        out = torch.empty(rows, n, dtype=torch.bfloat16, device=y.device)
+    _check(LIB.qresid_rmsnorm(y.data_ptr(), y.stride(0), r.data_ptr(), r.stride(0), rows, n, gamma.data_ptr(),
+                              float(eps), out.data_ptr(), out.stride(0), _stream(stream)), "qresid_rmsnorm")
+    return out
 
 
 def qlinear_last_error(stream=None) -> int:

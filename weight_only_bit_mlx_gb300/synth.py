@@ -57,3 +57,26 @@ def make_x(rows: int, k: int, seed: int = 0, config_id: int = 0, tensor_id: int 
     """Random activations as bf16 bits [rows, k], x ~ N(0, 1)."""
     g = rng_for(seed, config_id, tensor_id)
     return f32_to_bf16_bits(g.standard_normal(size=(rows, k)))
+
+
+# Inputs of the steps after the projections (QK norm + partial RoPE + KV store, and
+# post-add / next-norm).  Recipe: projection outputs (q, k, v, y) ~ N(0, sigma^2) in
+# float32; norm weights ~ U(0.5, 1.5) rounded to bf16; the residual stream ~ N(0, 1)
+# rounded to bf16; positions uniform on {lo .. hi-1} as int32.
+def make_f32(rows: int, n: int, sigma: float = 1.0, seed: int = 0, config_id: int = 0,
+             tensor_id: int = 2000) -> np.ndarray:
+    g = rng_for(seed, config_id, tensor_id)
+    return (sigma * g.standard_normal(size=(rows, n))).astype(np.float32)
+
+
+def make_bf16(shape, lo: float | None = None, hi: float | None = None, seed: int = 0, config_id: int = 0,
+              tensor_id: int = 3000) -> np.ndarray:
+    """bf16 bits: U(lo, hi) when both are given, else N(0, 1)."""
+    g = rng_for(seed, config_id, tensor_id)
+    a = g.uniform(lo, hi, size=shape) if lo is not None else g.standard_normal(size=shape)
+    return f32_to_bf16_bits(a)
+
+
+def make_pos(rows: int, lo: int, hi: int, seed: int = 0, config_id: int = 0, tensor_id: int = 4000) -> np.ndarray:
+    g = rng_for(seed, config_id, tensor_id)
+    return g.integers(lo, hi, size=rows).astype(np.int32)
