@@ -301,6 +301,54 @@ def run_ours(args):
             n += 2
         return n
 
+    # ---- the steps after the projections (QK norm + partial RoPE + KV store, post-add /
+    #      next-norm): head_dim 64 (32 q heads, 8 kv heads), rotary on the first 32 dims,
+    #      base 1e6, eps 1e-5, KV rings of 1024 slots per stream
+    HD, ROT, RING = 64, 32, 1024
+    post = {}
+    for R in (1, 16):
+        post[R] = {
+            "q_out": torch.empty(R, D_MODEL, dtype=torch.bfloat16, device=dev),
+            "k_ring": torch.zeros(R, RING, D_KV, dtype=torch.bfloat16, device=dev),
+            "v_ring": torch.zeros(R, RING, D_KV, dtype=torch.bfloat16, device=dev),
+            "pos": torch.randint(0, 1 << 20, (R,), generator=gen, device=dev, dtype=torch.int32),
+            "resid": rnd_bf16(R, D_MODEL),
+        }
+    qn_w = (torch.rand(HD, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+    kn_w = (torch.rand(HD, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+    gammas = [(torch.rand(D_MODEL, generator=gen, device=dev) + 0.5).to(torch.bfloat16) for _ in range(2)]
+
+    def qknorm(R):
+        b, pp = bufs[R], post[R]
+        q.qattn_qknorm_rope_kv(b["q"], b["k"], b["v"], D_MODEL // HD, D_KV // HD, HD, ROT, 1e6, 1e-5, qn_w, kn_w,
+                               pp["pos"], pp["k_ring"], pp["v_ring"], q_out=pp["q_out"])
+
+    def resid_norm(R, y, gi):
+        # the normed output becomes the next linear's activation x
+        q.qresid_rmsnorm(y, post[R]["resid"], gammas[gi], 1e-5, out=bufs[R]["x"])
+
+    def decode_layer_pass(R):
+        """The decode pass with the steps between the linears: per attention layer
+        q/k/v/gate -> QK norm + RoPE + KV store -> o -> post-add / next-norm; per layer
+        w1 + w3 + SwiGLU -> w2 -> post-add / next-norm (attention itself excluded: o
+        reads a fixed attention output)."""
+        b = bufs[R]
+        n = 0
+        for layer in range(N_LAYERS):
+            p = f"L{layer}."
+            if layer in ATTN_LAYERS:
+                q.qattn_proj_mv(W[p + "q"], W[p + "k"], W[p + "v"], W[p + "g"], b["x"],
+                                outs=(b["q"], b["k"], b["v"], b["g"]))
+                qknorm(R)
+                q.qlinear_mv_rows(W[p + "o"], b["attn"], b["o"])
+                resid_norm(R, b["o"], 0)
+                n += 4
+            q.qffn_swiglu_mv(W[p + "w1"], W[p + "w3"], b["x"], b["h"])
+            q.qlinear_mv_rows(W[p + "w2"], b["h"], b["y"])
+            resid_norm(R, b["y"], 1)
+            n += 3
+        return n
+
     # prefill buffers
     X = rnd_bf16(PROMPT, D_MODEL)
     Pa = torch.empty(PROMPT, D_FF, device=dev)
@@ -358,9 +406,17 @@ def run_ours(args):
         with torch.cuda.graph(g):
             launches[f"decode{R}"] = decode_pass(R)
         graphs[R] = g
+    for R in (1, 16):
+        decode_layer_pass(R)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            launches[f"layer{R}"] = decode_layer_pass(R)
+        graphs[f"layer{R}"] = g
     for _ in range(args.warmup):
         graphs[1].replay()
         graphs[16].replay()
+        graphs["layer1"].replay()
+        graphs["layer16"].replay()
     torch.cuda.synchronize()
     assert q.qlinear_last_error() == q.QL_OK
 
@@ -408,6 +464,44 @@ def run_ours(args):
 
     total_ms, d1_ms, d16_ms, pf_ms, gemm_ms = (max_over_ranks(v) for v in (total_ms, d1_ms, d16_ms, pf_ms, gemm_ms))
 
+    # ---------------- the decode pass with the steps between the linears, and those steps alone
+    layer_ms = {}
+    for R in (1, 16):
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(args.steps):
+            graphs[f"layer{R}"].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        layer_ms[R] = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+
+    def time_kernel(fn, reps=200):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(20):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(reps // 20):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3  # us per launch (back to back, in a graph)
+
+    post_lines = {}
+    for R in (1, 16):
+        qk_us = time_kernel(lambda: qknorm(R))
+        rn_us = time_kernel(lambda: resid_norm(R, bufs[R]["y"], 1))
+        qk_bytes = R * ((D_MODEL + 2 * D_KV) * 4 + (D_MODEL + 2 * D_KV) * 2 + 4) + 2 * HD * 2
+        rn_bytes = R * D_MODEL * (4 + 2 + 2 + 2) + D_MODEL * 2
+        post_lines[f"r{R}"] = {"qattn_qknorm_rope_kv_us": qk_us, "qattn_qknorm_rope_kv_GB/s": qk_bytes / qk_us / 1e3,
+                               "qresid_rmsnorm_us": rn_us, "qresid_rmsnorm_GB/s": rn_bytes / rn_us / 1e3,
+                               "layer_pass_ms": layer_ms[R], "layer_pass_launches": launches[f"layer{R}"],
+                               "layer_pass_tok_s_modelled": R / (layer_ms[R] * 1e-3)}
+    assert q.qlinear_last_error() == q.QL_OK
+
     # ---------------- end to end: host buffers in pinned memory, copies inside the timed region
     xh = torch.empty(1, D_MODEL, dtype=torch.bfloat16).pin_memory()
     xh.copy_(bufs[1]["x"].cpu())
@@ -445,6 +539,11 @@ def run_ours(args):
         "decode_r1": {"GB/s": value / world, "frac_of_hbm": value / world / pk["hbm"],
                       "ms_per_pass": d1_ms / args.steps, "bytes_per_pass": d1_bytes,
                       "tok_s_modelled": 1.0 / (d1_ms / args.steps * 1e-3)},
+        "decode_post_ops": dict(post_lines, what="QK norm + partial RoPE + KV store after q/k/v/gate and "
+                                "post-add / next-norm after o and w2 (head_dim 64, rotary 32, 1024-slot rings); "
+                                "layer_pass = the decode pass with them between the linears (graph, timed "
+                                "after the main region); per-kernel times are back-to-back launches, "
+                                "bytes = algorithmic reads + writes (latency-bound at these sizes)"),
         "decode_r16": {"GB/s": d16_gbs / world, "frac_of_hbm": d16_gbs / world / pk["hbm"],
                        "ms_per_pass": d16_ms / args.steps, "bytes_per_pass": d16_bytes,
                        "tok_s_modelled": 16.0 / (d16_ms / args.steps * 1e-3)},

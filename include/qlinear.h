@@ -186,8 +186,8 @@ int qswiglu(const float *a, const float *c, int32_t rows, int32_t n, int64_t lda
  *          bf16, into slot s = pos[r] mod ring_len (the non-negative remainder) of
  *          stream r's rings.
  * Arithmetic: fp32 for the norm and the rotation (fixed-order sums, so results are
- * deterministic), the angle and its cos/sin in float64, one nearest-even rounding to
- * bf16 per output.
+ * deterministic); the angle is formed and reduced modulo 2*pi in float64, its cos/sin
+ * taken in fp32; one nearest-even rounding to bf16 per output.
  *   q: float [rows, ldq] (n_q_heads*head_dim used); k, v: float [rows, ldk/ldv]
  *   (n_kv_heads*head_dim used) - the outputs of qattn_proj_mv;
  *   pos: int32 [rows] (device); q_out: bf16 bits [rows, ldqo];

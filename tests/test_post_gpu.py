@@ -2,7 +2,8 @@
 (oracle/decoder_post_oracle.py): QK norm + partial RoPE + KV store (TensorFold PR
 #1696, "What it adds") and post-add / next-norm (PR #1514, "What changes").
 
-Outputs are bf16.  The kernels compute in fp32 (angles in float64) and round once,
+Outputs are bf16.  The kernels compute in fp32 (rotation angles formed and reduced in
+float64) and round once,
 so each output is within half a bf16 ulp of the float64 value plus the fp32 error:
     |out - o64| <= 2^-8 * |o64| + 1e-5        (values are O(1) after the norm)
 and nearly all outputs equal the nearest-even bf16 of o64.  The stored residual is an
@@ -119,7 +120,7 @@ def test_qknorm_rope_kv_deterministic(q):
     assert np.array_equal(bits_host(one)[0], outs[0][1][5])
 
 
-RESID_SHAPES = [(1, 2048), (3, 1000), (16, 2560), (40, 64), (2, 1), (1, 8192), (7, 4099)]
+RESID_SHAPES = [(1, 2048), (3, 1000), (16, 2560), (40, 64), (2, 1), (1, 8192), (7, 4099), (2, 20000), (3, 8200)]
 
 
 @pytest.mark.parametrize("rows,n", RESID_SHAPES)

@@ -15,7 +15,8 @@
 //   post-add:  r' = bf16(r + y) (the stored residual), out = bf16(r' * rstd * gamma)
 // One warp per head (QK norm): the sum of squares is a fixed xor-butterfly, so every
 // head's result depends on that head's data only.  The angles are formed and turned
-// into (cos, sin) in double precision; everything else is fp32, rounded to bf16 once.
+// reduced modulo 2*pi in double precision, then turned into (cos, sin) in fp32;
+// everything else is fp32, rounded to bf16 once.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -49,15 +50,37 @@ struct QkParams {
   int ring_len;
 };
 
+// The rotation angles of one position: theta_i = pos * base^(-2i/rot) formed in
+// float64 (positions up to 2^31 keep ~1e-7 rad absolute accuracy), reduced to
+// [-pi, pi] in float64 (2*pi as a two-part constant), then cos / sin of the remainder
+// in fp32.
+__device__ __forceinline__ float2 rope_cos_sin(double pos, int i, int rot, double base) {
+  const double theta = pos * pow(base, -2.0 * (double)i / (double)rot);
+  const double kTwoPiHi = 6.283185307179586;       // 2*pi rounded to double
+  const double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
+  const double n = rint(theta * 0.15915494309189535);  // theta / (2*pi)
+  const double r = fma(-n, kTwoPiLo, fma(-n, kTwoPiHi, theta));
+  float sn, cs;
+  sincosf((float)r, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
 // grid: (ceil((nq + nkv) / kHeadWarps), rows); warp = one head of q (head < nq) or k
-// (head >= nq, which also stores that kv head's v)
+// (head >= nq, which also stores that kv head's v).  The CTA's angle table (one row,
+// one position) is built first, once per CTA.
 __global__ void __launch_bounds__(kHeadWarps * 32) qk_norm_rope_kv_kernel(const __grid_constant__ QkParams p) {
   __shared__ float hbuf[kHeadWarps][kMaxHeadDim];
+  __shared__ float2 cs_tab[kMaxHeadDim / 2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x * kHeadWarps + warp;
   const int r = blockIdx.y;
+  const int half = p.rot >> 1;
+  // positions and norm weights are not written by a preceding kernel
+  const double pos = (double)p.pos[r];
+  for (int i = threadIdx.x; i < half; i += kHeadWarps * 32) cs_tab[i] = rope_cos_sin(pos, i, p.rot, p.base);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
   if (head >= p.nq + p.nkv) return;
   const bool is_q = head < p.nq;
   const int kvh = head - p.nq;
@@ -79,8 +102,6 @@ __global__ void __launch_bounds__(kHeadWarps * 32) qk_norm_rope_kv_kernel(const 
   for (int i = 0; i < kMaxHeadDim / 32; ++i)
     if (i < per) hbuf[warp][lane + 32 * i] = __fmul_rn(__fmul_rn(x[i], rstd), bf16_to_f32(ldg_u16(w + lane + 32 * i)));
   __syncwarp();
-  const int half = p.rot >> 1;
-  const double pos = (double)p.pos[r];
   uint16_t *dst;
   if (is_q) {
     dst = p.q_out + (size_t)r * p.ldqo + (size_t)head * p.hd;
@@ -97,10 +118,7 @@ __global__ void __launch_bounds__(kHeadWarps * 32) qk_norm_rope_kv_kernel(const 
     float out;
     if (j < p.rot) {
       const int i = j < half ? j : j - half;
-      const double theta = pos * pow(p.base, -2.0 * (double)i / (double)p.rot);
-      double sd, cd;
-      sincos(theta, &sd, &cd);
-      const float s = (float)sd, c = (float)cd;
+      const float c = cs_tab[i].x, s = cs_tab[i].y;
       const float a = hbuf[warp][i], b = hbuf[warp][i + half];
       out = j < half ? __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)) : __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
     } else {
@@ -111,7 +129,87 @@ __global__ void __launch_bounds__(kHeadWarps * 32) qk_norm_rope_kv_kernel(const 
 }
 
 // post-add / next-norm: one CTA per row; the sum of squares is reduced in a fixed order
-// (per-thread strided sums, then a tree over the warps' xor-butterfly results)
+// (per-thread sums over its elements in order, then a tree over the warps'
+// xor-butterfly results in warp order).  Vector form (16-byte rows and n % 8 == 0):
+// each thread owns chunks of 8 consecutive elements, c = tid + 256 k; the first
+// kVecKeep chunks of the stored residual stay in registers for the second pass.
+constexpr int kVecKeep = 4;
+
+__device__ __forceinline__ float block_sum_fixed(float ss, float *wsum) {
+  ss = warp_sum_xor(ss);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = wsum[0];
+  for (int i = 1; i < kNormThreads / 32; ++i) tot = __fadd_rn(tot, wsum[i]);
+  return tot;
+}
+
+__global__ void __launch_bounds__(kNormThreads) resid_rmsnorm_vec_kernel(const float *y, int64_t ldy, uint16_t *resid,
+                                                                       int64_t ldr, int n, const uint16_t *gamma,
+                                                                       float eps, uint16_t *out, int64_t ldo) {
+  __shared__ float wsum[kNormThreads / 32];
+  const int r = blockIdx.x;
+  const int nch = n >> 3;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const float *yr = y + (size_t)r * ldy;
+  uint16_t *rr = resid + (size_t)r * ldr;
+  // chunk c of this row: r' = bf16(r + y), stored; returns the packed r' and adds its
+  // squares to ss in element order
+  auto add_chunk = [&](int c, float &ss) -> uint4 {
+    const uint4 rv = *reinterpret_cast<const uint4 *>(rr + 8 * c);
+    const float4 y0 = *reinterpret_cast<const float4 *>(yr + 8 * c);
+    const float4 y1 = *reinterpret_cast<const float4 *>(yr + 8 * c + 4);
+    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+    const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    uint32_t nw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint16_t lo = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(rw[e] & 0xFFFFu), yv[2 * e]));
+      const uint16_t hi = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(rw[e] >> 16), yv[2 * e + 1]));
+      const float vl = bf16_to_f32(lo), vh = bf16_to_f32(hi);
+      ss = __fmaf_rn(vl, vl, ss);
+      ss = __fmaf_rn(vh, vh, ss);
+      nw[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    const uint4 nv = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+    *reinterpret_cast<uint4 *>(rr + 8 * c) = nv;
+    return nv;
+  };
+  uint4 keep[kVecKeep];
+  float ss = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kVecKeep; ++k) {
+    const int c = threadIdx.x + k * kNormThreads;
+    if (c < nch) keep[k] = add_chunk(c, ss);
+  }
+  for (int c = threadIdx.x + kVecKeep * kNormThreads; c < nch; c += kNormThreads) (void)add_chunk(c, ss);
+  const float tot = block_sum_fixed(ss, wsum);
+  const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)n), eps)));
+  uint16_t *orow = out + (size_t)r * ldo;
+  auto norm_chunk = [&](int c, const uint4 &nv) {
+    const uint4 gv = *reinterpret_cast<const uint4 *>(gamma + 8 * c);
+    const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t ow[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint16_t lo = f32_to_bf16_rn(__fmul_rn(__fmul_rn(bf16_to_f32(nw[e] & 0xFFFFu), rstd),
+                                                   bf16_to_f32(gw[e] & 0xFFFFu)));
+      const uint16_t hi = f32_to_bf16_rn(__fmul_rn(__fmul_rn(bf16_to_f32(nw[e] >> 16), rstd), bf16_to_f32(gw[e] >> 16)));
+      ow[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    *reinterpret_cast<uint4 *>(orow + 8 * c) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+  };
+#pragma unroll
+  for (int k = 0; k < kVecKeep; ++k) {
+    const int c = threadIdx.x + k * kNormThreads;
+    if (c < nch) norm_chunk(c, keep[k]);
+  }
+  for (int c = threadIdx.x + kVecKeep * kNormThreads; c < nch; c += kNormThreads)
+    norm_chunk(c, *reinterpret_cast<const uint4 *>(rr + 8 * c));
+}
+
+// Scalar form (any n, strides and alignment): the same arithmetic one element at a time.
 __global__ void __launch_bounds__(kNormThreads) resid_rmsnorm_kernel(const float *y, int64_t ldy, uint16_t *resid,
                                                                    int64_t ldr, int n, const uint16_t *gamma, float eps,
                                                                    uint16_t *out, int64_t ldo) {
@@ -128,11 +226,7 @@ __global__ void __launch_bounds__(kNormThreads) resid_rmsnorm_kernel(const float
     const float v = bf16_to_f32(nb);
     ss = __fmaf_rn(v, v, ss);
   }
-  ss = warp_sum_xor(ss);
-  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = wsum[0];
-  for (int i = 1; i < kNormThreads / 32; ++i) tot = __fadd_rn(tot, wsum[i]);
+  const float tot = block_sum_fixed(ss, wsum);
   const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)n), eps)));
   uint16_t *orow = out + (size_t)r * ldo;
   for (int j = threadIdx.x; j < n; j += kNormThreads)
@@ -162,8 +256,12 @@ cudaError_t launch_qk_norm_rope_kv(const QkParams &p, cudaStream_t st) {
 cudaError_t launch_resid_rmsnorm(const float *y, int64_t ldy, uint16_t *resid, int64_t ldr, int rows, int n,
                                  const uint16_t *gamma, float eps, uint16_t *out, int64_t ldo, cudaStream_t st) {
   void *args[] = {&y, &ldy, &resid, &ldr, &n, &gamma, &eps, &out, &ldo};
-  return launch_pdl(reinterpret_cast<const void *>(&resid_rmsnorm_kernel), dim3((unsigned)rows), dim3(kNormThreads),
-                    args, st);
+  auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0; };
+  const bool vec = (n % 8) == 0 && (ldy % 4) == 0 && (ldr % 8) == 0 && (ldo % 8) == 0 && a16(y) && a16(resid) &&
+                   a16(out) && a16(gamma);
+  const void *fn = vec ? reinterpret_cast<const void *>(&resid_rmsnorm_vec_kernel)
+                       : reinterpret_cast<const void *>(&resid_rmsnorm_kernel);
+  return launch_pdl(fn, dim3((unsigned)rows), dim3(kNormThreads), args, st);
 }
 
 }  // namespace qlk
