@@ -42,7 +42,7 @@ PROMPT = 8192
 
 # DRAM traffic per launch of the dominant kernels from one ncu capture, keyed to the
 # hash of the kernel source it was taken on; reported as null once the source changes.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"b67f87572d90cce1": 45395712 + 211595776}  # pgemm M=8192 N=8192 K=2048, 4-bit
 
 
 def parse():
@@ -371,7 +371,7 @@ def run_ours(args):
             e0.record(stream)
             q.qlinear_pgemm(w, Xin, Y)
             e1.record(stream)
-            gemm_events.append((e0, e1, 2 * Xin.shape[0] * w.n * w.k))
+            gemm_events.append((e0, e1, 2 * Xin.shape[0] * w.n * w.k, (int(Xin.shape[0]), w.n, w.k)))
         else:
             q.qlinear_pgemm(w, Xin, Y)
 
@@ -452,8 +452,12 @@ def run_ours(args):
     d1_ms = sum(m[0].elapsed_time(m[1]) for m in marks)
     d16_ms = sum(m[1].elapsed_time(m[2]) for m in marks)
     pf_ms = sum(m[2].elapsed_time(m[3]) for m in marks)
-    gemm_ms = sum(a.elapsed_time(b) for a, b, _ in gemm_events)
-    gemm_flops = sum(f for _, _, f in gemm_events)
+    gemm_ms = sum(a.elapsed_time(b) for a, b, _, _ in gemm_events)
+    gemm_flops = sum(f for _, _, f, _ in gemm_events)
+    # the roofline kernel: the M = 8192, N = 8192, K = 2048 launches (w1, w3 of every layer)
+    ffn_ev = [(a, b, f) for a, b, f, shape in gemm_events if shape == (PROMPT, D_FF, D_MODEL)]
+    ffn_ms = sum(a.elapsed_time(b) for a, b, _ in ffn_ev)
+    ffn_flops = sum(f for _, _, f in ffn_ev)
 
     def max_over_ranks(v):
         if world == 1:
@@ -462,7 +466,8 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
-    total_ms, d1_ms, d16_ms, pf_ms, gemm_ms = (max_over_ranks(v) for v in (total_ms, d1_ms, d16_ms, pf_ms, gemm_ms))
+    total_ms, d1_ms, d16_ms, pf_ms, gemm_ms, ffn_ms = (max_over_ranks(v) for v in (total_ms, d1_ms, d16_ms, pf_ms,
+                                                                                 gemm_ms, ffn_ms))
 
     # ---------------- the decode pass with the steps between the linears, and those steps alone
     layer_ms = {}
@@ -523,7 +528,8 @@ def run_ours(args):
     value = world * d1_bytes * args.steps / (d1_ms * 1e-3) / 1e9
     d16_gbs = world * d16_bytes * args.steps / (d16_ms * 1e-3) / 1e9
     pf_tflops = world * prefill_flops() * args.steps / (pf_ms * 1e-3) / 1e12
-    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12  # per GPU
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12  # per GPU, all GEMM launches of the pass
+    ffn_tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12      # per GPU, the roofline kernel's launches
     src = source_hash(["pgemm.cu", "common.cuh", "sync.cuh"])
     traffic = NCU_TRAFFIC.get(src)
     line = {
@@ -552,9 +558,14 @@ def run_ours(args):
                     "tok_s_modelled": PROMPT / (gemm_ms / args.steps * 1e-3)},
         "tok_s_note": "modelled from the linear layers only: decode R / (decode pass time), prefill "
                       "prompt rows / (sum of the pass's pgemm times); attention, norms and sampling excluded",
-        "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm (row-sum pre-pass + tcgen05 GEMM)",
-                     "achieved": gemm_tflops, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                     "frac": gemm_tflops / pk["bf16_sus"], "traffic": traffic,
+        "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm (row-sum pre-pass + tcgen05 GEMM), "
+                                                  f"M={PROMPT} N={D_FF} K={D_MODEL} launches (w1, w3)",
+                     "achieved": ffn_tflops, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                     "frac": ffn_tflops / pk["bf16_sus"], "traffic": traffic,
+                     "traffic_unit": "bytes per launch (DRAM read + write, one ncu capture of this shape)",
+                     "algorithmic_bytes_per_launch": PROMPT * D_MODEL * 2 + weight_bytes(D_FF, D_MODEL, bits)
+                     + PROMPT * D_FF * 4,
+                     "all_gemm_launches_TFLOP/s": gemm_tflops,
                      "peak_source": f"{pk['src']} bf16 sustained"},
         "roofline_decode": {"bound": "hbm", "kernel": "decode pass R=1 (qattn_proj_mv, qlinear_mv_rows, "
                                                       "qffn_swiglu_mv)",
