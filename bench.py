@@ -117,6 +117,23 @@ def prefill_flops():
     return sum(2 * PROMPT * n * k for _, n, k in layer_shapes())
 
 
+def max_over_ranks_of(v, world, device):
+    """The largest of v over all ranks: a replicated job ends when its slowest rank does."""
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, steps, max_ms, world):
+    """Whole-job throughput of `world` replicas (weak scaling): every rank processes
+    units_per_rank per step, and the job takes the slowest rank's time max_ms."""
+    return world * units_per_rank * steps / (max_ms * 1e-3)
+
+
 # ------------------------------------------------------------------------------------
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while it runs."""
@@ -460,11 +477,7 @@ def run_ours(args):
     ffn_flops = sum(f for _, _, f in ffn_ev)
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_of(v, world, dev)
 
     total_ms, d1_ms, d16_ms, pf_ms, gemm_ms, ffn_ms = (max_over_ranks(v) for v in (total_ms, d1_ms, d16_ms, pf_ms,
                                                                                  gemm_ms, ffn_ms))
@@ -525,9 +538,9 @@ def run_ours(args):
     pk = peaks()
     d1_bytes = decode_bytes(bits, 1)
     d16_bytes = decode_bytes(bits, 16)
-    value = world * d1_bytes * args.steps / (d1_ms * 1e-3) / 1e9
-    d16_gbs = world * d16_bytes * args.steps / (d16_ms * 1e-3) / 1e9
-    pf_tflops = world * prefill_flops() * args.steps / (pf_ms * 1e-3) / 1e12
+    value = job_throughput(d1_bytes, args.steps, d1_ms, world) / 1e9
+    d16_gbs = job_throughput(d16_bytes, args.steps, d16_ms, world) / 1e9
+    pf_tflops = job_throughput(prefill_flops(), args.steps, pf_ms, world) / 1e12
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12  # per GPU, all GEMM launches of the pass
     ffn_tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12      # per GPU, the roofline kernel's launches
     src = source_hash(["pgemm.cu", "common.cuh", "sync.cuh"])
@@ -572,7 +585,7 @@ def run_ours(args):
                             "achieved": value / world, "peak": pk["hbm"], "unit": "GB/s",
                             "frac": value / world / pk["hbm"], "traffic": None,
                             "peak_source": f"{pk['src']} copy bandwidth"},
-        "e2e": {"value": world * d1_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_throughput(d1_bytes, args.steps, e2e_ms, world) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": D_MODEL * 2, "d2h_bytes_per_step": D_MODEL * 4,
                 "what": "decode pass R=1 with x copied from pinned host memory and the last output copied back"},
         "gpu_launches": n_launch,
