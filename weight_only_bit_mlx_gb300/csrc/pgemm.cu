@@ -76,6 +76,7 @@ static_assert(2 * BM <= kTmemCols, "tensor memory budget");
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
 constexpr int kPf = 2;       // k blocks of scale/bias prefetch (no-TMA path)
+constexpr int kLdChunks = 2;  // epilogue tensor-memory loads (8 columns each) per wait
 static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
 
 template <int BITS> struct Cfg {
@@ -605,15 +606,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const float sv = sSc[sc * BN + ch_row];
+        // kLdChunks loads of 8 columns in flight per wait: the tensor-memory load
+        // latency is paid CW / (8 * kLdChunks) times per block instead of CW / 8
 #pragma unroll
-        for (int ch = 0; ch < CW / 8; ++ch) {
-          uint32_t r[8];
-          tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * ch), r);
+        for (int ch = 0; ch < CW / 8; ch += kLdChunks) {
+          uint32_t r[kLdChunks][8];
+#pragma unroll
+          for (int u = 0; u < kLdChunks; ++u) tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * (ch + u)), r[u]);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            ffma2(y[8 * ch + 2 * i], y[8 * ch + 2 * i + 1], sv, sv, __uint_as_float(r[2 * i]),
-                  __uint_as_float(r[2 * i + 1]));
+          for (int u = 0; u < kLdChunks; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              ffma2(y[8 * (ch + u) + 2 * i], y[8 * (ch + u) + 2 * i + 1], sv, sv, __uint_as_float(r[u][2 * i]),
+                    __uint_as_float(r[u][2 * i + 1]));
         }
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
