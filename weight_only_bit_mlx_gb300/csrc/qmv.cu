@@ -10,11 +10,12 @@
 // of n or of the fused/unfused choice):
 //   * a CTA owns a 16-row tile of W (both w1 and w3 in the fused FFN) and a k-span;
 //     CTAs of a cluster split k into spans;
-//   * the span is cut into kNch chunks of kGpc groups; a copy warp starts, chunk by
+//   * the span is cut into kNch chunks of kGpc groups; warp 0 first starts, chunk by
 //     chunk, one bulk copy (cp.async.bulk) per weight row of the chunk, straight
 //     from HBM into shared memory, each chunk completing its own mbarrier, so the
-//     compute warps start on chunk 0 while later chunks are still streaming in and
-//     the weight stream leaves the SM as large requests issued at kernel start;
+//     warps start on chunk 0 while later chunks are still streaming in and the
+//     weight stream leaves the SM as large requests issued at kernel start (no warp
+//     is kept only for copies, so the compute warps get 64 registers instead of 56);
 //   * scales and biases go in by bulk copy with chunk 0 (one copy for the whole tile
 //     when a CTA spans the full k), activations (the only input a preceding kernel
 //     may write) are loaded by the compute warps after griddepcontrol.wait, so with
@@ -76,8 +77,9 @@ template <int BITS, int NB, int MODE> struct MvLayout {
   static int max_bytes() { return bytes(kMvMaxCluster); }
 };
 
-// Four CTAs per SM: caps every variant at 56 registers, so the two-row-block (R > 8)
-// variants stay as resident as the one-row-block ones (measured: R = 16 pass +4 %).
+// Four CTAs of 256 threads per SM: 64 registers a thread, and every variant (one or
+// two row blocks) equally resident.  Measured on the decode pass: 3 per SM (80
+// registers) and 5 per SM (48 registers, spills) are both slower.
 constexpr int kMvCtasPerSm = 4;
 
 template <int BITS, int NB, int MODE>
@@ -127,13 +129,15 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
   for (int i = 0; i < NV; ++i) y[i] = 0.0f;
   uint32_t phase = 0;
   bool ok = true;
-  int armed = 0;  // chunks of the last span whose copies were started (copy warp)
+  int armed = 0;  // chunks of the last span whose copies were started (warp 0)
 
   for (int ch0 = gs0; ch0 < gs1; ch0 += SPAN) {
     const int ch1 = min(gs1, ch0 + SPAN);
     const int ng = ch1 - ch0;
-    if (warp == kMvWarps) {
-      // ---- copy warp: chunk by chunk, one bulk copy per weight row of the chunk
+    if (warp == 0) {
+      // ---- warp 0 first starts the span's copies, chunk by chunk, one bulk copy per
+      //      weight row of the chunk (every warp has finished the previous span: the
+      //      barrier at the end of each span)
       const int t = lane >> 4, r = lane & 15;
       const int row = tile * 16 + r;
       const bool mine = lane < NMAT * 16 && row < n;
@@ -161,8 +165,9 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
         }
         armed = cc + 1;
       }
-    } else {
-      // ---- compute warps
+    }
+    {
+      // ---- every warp computes
       const int tid = threadIdx.x;  // 0 .. kMvComputeThreads-1
       // Scales and biases of the span (not written by a preceding kernel, so read
       // before the dependency wait) -> fp32 factor pairs.  16-byte vectors of 8
@@ -256,13 +261,18 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
     if (ch1 < gs1) __syncthreads();  // the span's buffers are fully read before the next span refills them
   }
   if (!ok && lane == 0) record_status(p.status, kErrTimeout);
+  if (warp == 0 && lane == 0) {
+    // every copy this CTA started has landed before the partials reuse the weight area
+    // and before the CTA exits (immediate unless a wait gave up)
+    for (int cc = 0; cc < armed; ++cc) (void)mbar_wait_bounded(&bars[cc], phase ^ 1u, kMvDrainNs, nullptr);
+  }
 
   // ---- partials: warps in order, then cluster ranks in order.  The partials reuse
   //      the weight area, so every compute warp is past its last group first.  In a
   //      cluster each rank writes its CTA partial into slot `rank` of rank 0's cpart
   //      (distributed shared memory); after one cluster barrier rank 0 adds the slots
   //      in rank order and the other ranks may exit (nobody reads their shared memory).
-  if (warp < kMvWarps) {
+  {
     named_bar_sync(kBarCompute, kMvComputeThreads);
 #pragma unroll
     for (int i = 0; i < NV; ++i) red[(warp * NV + i) * 32 + lane] = y[i];
@@ -275,9 +285,6 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
       for (int w = 1; w < kMvWarps; ++w) acc = __fadd_rn(acc, red[(w * NV + i) * 32 + ln]);
       dst[i * 32 + ln] = acc;
     }
-  } else if (lane == 0 && armed > 0) {
-    // every copy this CTA started must land before its shared memory goes away
-    for (int cc = 0; cc < armed; ++cc) (void)mbar_wait_bounded(&bars[cc], phase ^ 1u, kMvDrainNs, nullptr);
   }
   if (p.cs > 1) cluster.sync();
   else __syncthreads();

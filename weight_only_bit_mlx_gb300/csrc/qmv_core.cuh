@@ -74,7 +74,7 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                : "memory");
 }
 
-constexpr int kMvThreads = (kMvWarps + 1) * 32;  // compute warps + one copy warp
+constexpr int kMvThreads = kMvWarps * 32;  // compute warps (warp 0 also starts the bulk copies)
 constexpr int kMvComputeThreads = kMvWarps * 32;
 constexpr int kBarCompute = 1;                   // named barrier of the compute warps
 constexpr uint64_t kMvDrainNs = 2000000000ull;
