@@ -145,3 +145,21 @@ def test_deterministic_repeat(q):
     a = q.qlinear_mv_rows(w, xd)
     b = q.qlinear_mv_rows(w, xd)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("bits,k", [(4, 24576), (4, 65536), (6, 12288), (8, 16384)])
+def test_several_spans_per_cta(q, bits, k):
+    # k large enough that each CTA of the k-split cluster walks more than one span of
+    # groups, reusing its shared-memory buffers between spans
+    n = 48
+    w = U.weight(n, k, bits, config_id=61, tensor_id=bits)
+    wd = U.dev_weight(w)
+    x = synth.make_x(9, k, config_id=61)
+    xd = U.dev_x(x)
+    y = q.qlinear_mv_rows(wd, xd)
+    y1 = q.qlinear_mv(wd, xd[4])
+    torch.cuda.synchronize()
+    y64, A = orc.qlinear_w(x, w)
+    U.assert_close(y, y64, A, f"bits={bits} k={k}")
+    assert torch.equal(y1, y[4])
+    assert q.qlinear_last_error() == q.QL_OK
