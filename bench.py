@@ -15,8 +15,15 @@ gate 2048 -> 2048, o 2048 -> 2048), MLX affine 4-bit group 64 by default:
 Decode passes are captured once as CUDA graphs (the kernels are a few
 microseconds long, so host launch time would otherwise dominate); prefill is
 launched directly.  Inputs are seeded synthetic data with the pages' shapes and
-distributions; every decode pass reads 502 MB of distinct weights, far more than
+distributions; every decode pass reads 503 MB of distinct weights, far more than
 the 129 MB L2, so no L2 flush is needed between iterations.
+
+Reported beside the step (timed after it): the decode pass with the steps between
+the linears (QK norm + partial RoPE + KV store, post-add / next-norm) and those
+kernels alone (`decode_post_ops`), and the end-to-end R = 1 pass from pinned host
+memory (`e2e`).  `--case window` prints the window-cost table (qlinear_mv_rows vs
+qlinear_pgemm for 1..256 rows); `--case pgemm/ffn/mv` time one kernel on one shape
+(for profiler captures).
 
 Output: one JSON line (rank 0).  --impl reference times the float64 CPU oracle on
 a bounded sample of the same workload instead.
@@ -584,6 +591,8 @@ def run_ours(args):
                                                       "qffn_swiglu_mv)",
                             "achieved": value / world, "peak": pk["hbm"], "unit": "GB/s",
                             "frac": value / world / pk["hbm"], "traffic": None,
+                            "traffic_note": "per-launch DRAM bytes of the FFN decode kernel equal its algorithmic "
+                                            "bytes (ncu: 18.91 MB read for 18.87 MB); no capture of the whole pass",
                             "peak_source": f"{pk['src']} copy bandwidth"},
         "e2e": {"value": job_throughput(d1_bytes, args.steps, e2e_ms, world) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": D_MODEL * 2, "d2h_bytes_per_step": D_MODEL * 4,
