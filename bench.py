@@ -124,6 +124,16 @@ def prefill_flops():
     return sum(2 * PROMPT * n * k for _, n, k in layer_shapes())
 
 
+def workload_config(bits, world):
+    """The `config` object both arms report: the workload the metric is quoted on."""
+    return {"workload": f"full-depth sweep: 16 layers (FFN 2048->8192->2048) + 6 attention sets "
+                        f"(q,g,o 2048->2048; k,v 2048->512), MLX affine {bits}-bit g64; decode R=1 "
+                        f"(value) and R=16, prefill M={PROMPT} pgemm",
+            "rows": 1, "prompt_rows": PROMPT, "bits": bits,
+            "l2": "no flush: every decode pass streams 503 MB of distinct weights (> 129 MB L2)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def max_over_ranks_of(v, world, device):
     """The largest of v over all ranks: a replicated job ends when its slowest rank does."""
     if world == 1:
@@ -255,7 +265,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": f"full-depth sweep sample, {bits}-bit", "sample": sample},
+            "data": "synthetic", "config": dict(workload_config(bits, 1), sample=sample),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -556,12 +566,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16xq%d->f32" % bits, "data": "synthetic",
-        "config": {"workload": f"full-depth sweep: 16 layers (FFN 2048->8192->2048) + 6 attention sets "
-                               f"(q,g,o 2048->2048; k,v 2048->512), MLX affine {bits}-bit g64; decode R=1 "
-                               f"(value) and R=16, prefill M={PROMPT} pgemm",
-                   "rows": 1, "prompt_rows": PROMPT, "bits": bits,
-                   "l2": "no flush: every decode pass streams 502 MB of distinct weights (> 129 MB L2)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(bits, world),
         "decode_r1": {"GB/s": value / world, "frac_of_hbm": value / world / pk["hbm"],
                       "ms_per_pass": d1_ms / args.steps, "bytes_per_pass": d1_bytes,
                       "tok_s_modelled": 1.0 / (d1_ms / args.steps * 1e-3)},
