@@ -13,10 +13,9 @@
 namespace qlk {
 
 template <int BITS> struct Geo;
-#ifndef QL_MV_NCH
-#define QL_MV_NCH 1
-#endif
-constexpr int kNch = QL_MV_NCH;  // chunks per span (one mbarrier each)
+// chunks per span, one mbarrier each (2, computing the first half while the second
+// lands, measured slower on the decode pass)
+constexpr int kNch = 1;
 // spans of 32 groups (4-bit) or 16 groups (6/8-bit), split over the compute warps and chunks
 template <> struct Geo<4> {
   static constexpr int kLw = 2;                          // words per lane per row per group
