@@ -361,7 +361,7 @@ def run_ours(args):
         # the normed output becomes the next linear's activation x
         q.qresid_rmsnorm(y, post[R]["resid"], gammas[gi], 1e-5, out=bufs[R]["x"])
 
-    def decode_layer_pass(R):
+    def decode_layer_pass(R, fused=False):
         """The decode pass with the steps between the linears: per attention layer
         q/k/v/gate -> QK norm + RoPE + KV store -> o -> post-add / next-norm; per layer
         w1 + w3 + SwiGLU -> w2 -> post-add / next-norm (attention itself excluded: o
@@ -374,13 +374,21 @@ def run_ours(args):
                 q.qattn_proj_mv(W[p + "q"], W[p + "k"], W[p + "v"], W[p + "g"], b["x"],
                                 outs=(b["q"], b["k"], b["v"], b["g"]))
                 qknorm(R)
-                q.qlinear_mv_rows(W[p + "o"], b["attn"], b["o"])
-                resid_norm(R, b["o"], 0)
-                n += 4
+                if fused:  # the post-add / next-norm as the matvec's epilogue
+                    q.qlinear_mv_resid_norm(W[p + "o"], b["attn"], post[R]["resid"], gammas[0], 1e-5, out=b["x"])
+                    n += 3
+                else:
+                    q.qlinear_mv_rows(W[p + "o"], b["attn"], b["o"])
+                    resid_norm(R, b["o"], 0)
+                    n += 4
             q.qffn_swiglu_mv(W[p + "w1"], W[p + "w3"], b["x"], b["h"])
-            q.qlinear_mv_rows(W[p + "w2"], b["h"], b["y"])
-            resid_norm(R, b["y"], 1)
-            n += 3
+            if fused:
+                q.qlinear_mv_resid_norm(W[p + "w2"], b["h"], post[R]["resid"], gammas[1], 1e-5, out=b["x"])
+                n += 2
+            else:
+                q.qlinear_mv_rows(W[p + "w2"], b["h"], b["y"])
+                resid_norm(R, b["y"], 1)
+                n += 3
         return n
 
     # prefill buffers
@@ -441,16 +449,18 @@ def run_ours(args):
             launches[f"decode{R}"] = decode_pass(R)
         graphs[R] = g
     for R in (1, 16):
-        decode_layer_pass(R)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            launches[f"layer{R}"] = decode_layer_pass(R)
-        graphs[f"layer{R}"] = g
+        for fused in (False, True):
+            key = f"layer{R}" + ("f" if fused else "")
+            decode_layer_pass(R, fused)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                launches[key] = decode_layer_pass(R, fused)
+            graphs[key] = g
     for _ in range(args.warmup):
         graphs[1].replay()
         graphs[16].replay()
-        graphs["layer1"].replay()
-        graphs["layer16"].replay()
+        for key in ("layer1", "layer16", "layer1f", "layer16f"):
+            graphs[key].replay()
     torch.cuda.synchronize()
     assert q.qlinear_last_error() == q.QL_OK
 
@@ -501,14 +511,14 @@ def run_ours(args):
 
     # ---------------- the decode pass with the steps between the linears, and those steps alone
     layer_ms = {}
-    for R in (1, 16):
+    for key in ("layer1", "layer16", "layer1f", "layer16f"):
         e0, e1 = ev(), ev()
         e0.record(stream)
         for _ in range(args.steps):
-            graphs[f"layer{R}"].replay()
+            graphs[key].replay()
         e1.record(stream)
         torch.cuda.synchronize()
-        layer_ms[R] = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+        layer_ms[key] = max_over_ranks(e0.elapsed_time(e1)) / args.steps
 
     def time_kernel(fn, reps=200):
         g = torch.cuda.CUDAGraph()
@@ -533,8 +543,11 @@ def run_ours(args):
         rn_bytes = R * D_MODEL * (4 + 2 + 2 + 2) + D_MODEL * 2
         post_lines[f"r{R}"] = {"qattn_qknorm_rope_kv_us": qk_us, "qattn_qknorm_rope_kv_GB/s": qk_bytes / qk_us / 1e3,
                                "qresid_rmsnorm_us": rn_us, "qresid_rmsnorm_GB/s": rn_bytes / rn_us / 1e3,
-                               "layer_pass_ms": layer_ms[R], "layer_pass_launches": launches[f"layer{R}"],
-                               "layer_pass_tok_s_modelled": R / (layer_ms[R] * 1e-3)}
+                               "layer_pass_ms": layer_ms[f"layer{R}"], "layer_pass_launches": launches[f"layer{R}"],
+                               "layer_pass_tok_s_modelled": R / (layer_ms[f"layer{R}"] * 1e-3),
+                               "layer_pass_fused_ms": layer_ms[f"layer{R}f"],
+                               "layer_pass_fused_launches": launches[f"layer{R}f"],
+                               "layer_pass_fused_tok_s_modelled": R / (layer_ms[f"layer{R}f"] * 1e-3)}
     assert q.qlinear_last_error() == q.QL_OK
 
     # ---------------- end to end: host buffers in pinned memory, copies inside the timed region
@@ -573,7 +586,8 @@ def run_ours(args):
         "decode_post_ops": dict(post_lines, what="QK norm + partial RoPE + KV store after q/k/v/gate and "
                                 "post-add / next-norm after o and w2 (head_dim 64, rotary 32, 1024-slot rings); "
                                 "layer_pass = the decode pass with them between the linears (graph, timed "
-                                "after the main region); per-kernel times are back-to-back launches, "
+                                "after the main region); layer_pass_fused = the same with the post-add / next-norm "
+                                "as the o / w2 matvec's epilogue (qlinear_mv_resid_norm); per-kernel times are back-to-back launches, "
                                 "bytes = algorithmic reads + writes (latency-bound at these sizes)"),
         "decode_r16": {"GB/s": d16_gbs / world, "frac_of_hbm": d16_gbs / world / pk["hbm"],
                        "ms_per_pass": d16_ms / args.steps, "bytes_per_pass": d16_bytes,

@@ -221,6 +221,26 @@ int qresid_rmsnorm(const float *y, int64_t ldy, uint16_t *resid, int64_t ldr, in
                    void *stream);
 
 /*
+ * qlinear_mv_resid_norm - the w2 / o decode matvec with the post-add / next-norm step as
+ * its epilogue, in one launch.  [P1514] "What changes" (post-add/next-norm fusion with the
+ * retained rounding boundaries); [P1696] "What it adds" (decode matvecs).
+ *   y = W x[r] as qlinear_mv_rows computes it (bit-equal), then
+ *   resid[r][i] <- bf16(resid[r][i] + y[r][i])      (bit-equal to qresid_rmsnorm's), and
+ *   out[r][i] = bf16(r'_i / sqrt(mean_i r'_i^2 + eps) * gamma_i) from the stored r'.
+ * The sum of squares runs in a fixed order of its own (per 16-channel tile, then tiles in
+ * order), so out is deterministic and row-local but not bit-equal to qresid_rmsnorm's;
+ * both are within half a bf16 ulp plus fp32 error of the float64 value.
+ *   x: bf16 [rows, ldx]; resid: bf16 bits [rows, ldr], read and overwritten; gamma: bf16
+ *   [n]; out: bf16 bits [rows, ldo] (must not overlap resid).  rows 1..16, n <= 65536.
+ *   Uses a library-owned per-device scratch (per-tile sums and a counter that every launch
+ *   leaves at zero): calls on one device must be ordered on one stream.  Errors as
+ *   qlinear_mv_rows, plus QL_ERR_NULL for resid/gamma/out and QL_ERR_SHAPE for eps < 0.
+ */
+int qlinear_mv_resid_norm(const ql_weight *w, const uint16_t *x, int32_t rows, int64_t ldx,
+                          uint16_t *resid, int64_t ldr, const uint16_t *gamma, float eps,
+                          uint16_t *out, int64_t ldo, void *stream);
+
+/*
  * qlinear_last_error - synchronizes `stream`, then returns and clears the device
  * status word: QL_OK, or QL_ERR_TIMEOUT if a bounded device-side wait gave up in a
  * kernel enqueued since the last call.  Returns QL_ERR_CUDA if synchronization fails.

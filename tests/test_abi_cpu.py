@@ -137,3 +137,14 @@ def test_post_ops_reject_bad_arguments_on_host(q):
     assert L.qresid_rmsnorm(P, 8, P, 8, 1, 8, P, -1.0, P, 8, None) == q.QL_ERR_SHAPE
     assert L.qresid_rmsnorm(P, 7, P, 8, 1, 8, P, 1e-5, P, 8, None) == q.QL_ERR_ALIGN
     assert L.qresid_rmsnorm(P + 1, 8, P, 8, 1, 8, P, 1e-5, P, 8, None) == q.QL_ERR_ALIGN
+
+
+def test_fused_resid_norm_rejects_bad_arguments_on_host(q):
+    w = _w(q)
+    L = q.LIB
+    P = 0x40000
+    assert L.qlinear_mv_resid_norm(ctypes.byref(w), P, 1, 128, 0, 64, P, 1e-5, P, 64, None) == q.QL_ERR_NULL
+    assert L.qlinear_mv_resid_norm(ctypes.byref(w), P, 1, 128, P, 64, P, -1.0, P, 64, None) == q.QL_ERR_SHAPE
+    assert L.qlinear_mv_resid_norm(ctypes.byref(w), P, 17, 128, P, 64, P, 1e-5, P, 64, None) == q.QL_ERR_ROWS
+    assert L.qlinear_mv_resid_norm(ctypes.byref(w), P, 2, 128, P, 32, P, 1e-5, P, 64, None) == q.QL_ERR_ALIGN
+    assert L.qlinear_mv_resid_norm(ctypes.byref(w), P + 8, 1, 128, P, 64, P, 1e-5, P, 64, None) == q.QL_ERR_ALIGN

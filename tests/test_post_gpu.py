@@ -160,3 +160,53 @@ def test_resid_rmsnorm_rows_independent(q):
     outb = q.qresid_rmsnorm(y[4:5], rb, g, 1e-5)
     assert np.array_equal(bits_host(outa)[4], bits_host(outb)[0])
     assert np.array_equal(bits_host(ra)[4], bits_host(rb)[0])
+
+
+# ---- the post-add / next-norm step as the epilogue of the w2 / o matvec
+@pytest.mark.parametrize("bits,rows,n,k", [(4, 1, 2048, 8192), (4, 16, 2048, 2048), (6, 5, 100, 192),
+                                           (8, 9, 513, 2048), (4, 3, 4096, 576)])
+def test_mv_resid_norm_fused(q, bits, rows, n, k):
+    cid = bits * 1000 + rows * 10 + n % 7
+    w = q.QWeight.from_numpy(synth.make_weight(n, k, bits, config_id=cid, tensor_id=1))
+    x = q.bf16_from_bits(synth.make_x(rows, k, config_id=cid, tensor_id=2))
+    r0 = synth.make_bf16((rows, n), config_id=cid, tensor_id=3)
+    gamma = bf16_dev(synth.make_bf16((n,), 0.5, 1.5, config_id=cid, tensor_id=4))
+    eps = 1e-5
+    # fused
+    rf = bf16_dev(r0)
+    out_f = q.qlinear_mv_resid_norm(w, x, rf, gamma, eps)
+    # unfused: the matvec, then the post-add / next-norm kernel
+    rs = bf16_dev(r0)
+    y = q.qlinear_mv_rows(w, x)
+    out_s = q.qresid_rmsnorm(y, rs, gamma, eps)
+    torch.cuda.synchronize()
+    assert q.qlinear_last_error() == q.QL_OK
+    # the stored residual is the same decision in the same precision: bit-equal
+    assert np.array_equal(bits_host(rf), bits_host(rs))
+    # the normed output against the float64 definition on the stored residual
+    rb = bits_host(rf)
+    rn = po.bf16_bits_to_f64(rb)
+    o64 = rn / np.sqrt((rn * rn).mean(axis=1, keepdims=True) + float(np.float32(eps))) * \
+        po.bf16_bits_to_f64(bits_host(gamma)).reshape(1, -1)
+    check_bf16(bits_host(out_f), o64, "fused normed output")
+    check_bf16(bits_host(out_s), o64, "unfused normed output")
+    # repeated launches (the tile counter returns to zero) give the same bits
+    rf2 = bf16_dev(r0)
+    out_f2 = q.qlinear_mv_resid_norm(w, x, rf2, gamma, eps)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_host(out_f2), bits_host(out_f)) and np.array_equal(bits_host(rf2), rb)
+
+
+def test_mv_resid_norm_rows_independent(q):
+    n, k, bits = 2048, 2048, 4
+    w = q.QWeight.from_numpy(synth.make_weight(n, k, bits, config_id=77, tensor_id=1))
+    x = q.bf16_from_bits(synth.make_x(12, k, config_id=77, tensor_id=2))
+    r0 = synth.make_bf16((12, n), config_id=77, tensor_id=3)
+    gamma = bf16_dev(synth.make_bf16((n,), 0.5, 1.5, config_id=77, tensor_id=4))
+    ra = bf16_dev(r0)
+    oa = q.qlinear_mv_resid_norm(w, x, ra, gamma, 1e-5)
+    rb = bf16_dev(r0[7:8])
+    ob = q.qlinear_mv_resid_norm(w, x[7:8].clone(), rb, gamma, 1e-5)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_host(oa)[7], bits_host(ob)[0])
+    assert np.array_equal(bits_host(ra)[7], bits_host(rb)[0])

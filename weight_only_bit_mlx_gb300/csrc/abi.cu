@@ -153,6 +153,39 @@ int qlinear_mv_rows(const ql_weight *w, const uint16_t *x, int32_t rows, int64_t
   return launch_status(launch_mv(p, kMvPlain, w->bits, tiles, static_cast<cudaStream_t>(stream)));
 }
 
+int qlinear_mv_resid_norm(const ql_weight *w, const uint16_t *x, int32_t rows, int64_t ldx, uint16_t *resid,
+                          int64_t ldr, const uint16_t *gamma, float eps, uint16_t *out, int64_t ldo, void *stream) {
+  int e = check_weight(w);
+  if (e) return e;
+  if ((e = check_x(x, rows, ldx, w->k))) return e;
+  if (resid == nullptr || gamma == nullptr || out == nullptr) return QL_ERR_NULL;
+  if (!(eps >= 0.0f)) return QL_ERR_SHAPE;
+  if ((w->n + 15) / 16 > kMvResidMaxTiles) return QL_ERR_SHAPE;
+  if ((rows > 1 && (ldr < w->n || ldo < w->n)) || !aligned(resid, 2) || !aligned(out, 2) || !aligned(gamma, 2))
+    return QL_ERR_ALIGN;
+  int *status = nullptr;
+  if ((e = device_setup(&status))) return e;
+  MvParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (mv_resid_scratch(&p.part, &p.counter)) return QL_ERR_CUDA;
+  p.status = status;
+  p.budget_ns = wait_budget_ns();
+  p.m[0] = make_mat(w, nullptr, 0);
+  p.x = x;
+  p.ldx = ldx;
+  p.rows = rows;
+  p.k = w->k;
+  p.resid = resid;
+  p.ldr = ldr;
+  p.gamma = gamma;
+  p.eps = eps;
+  p.nout = out;
+  p.ldn = ldo;
+  const int tiles = (w->n + 15) / 16;
+  p.ntiles = tiles;
+  return launch_status(launch_mv(p, kMvResid, w->bits, tiles, static_cast<cudaStream_t>(stream)));
+}
+
 int qlinear_mv(const ql_weight *w, const uint16_t *x, float *y, void *stream) {
   return qlinear_mv_rows(w, x, 1, w ? w->k : 0, y, w ? w->n : 0, stream);
 }
@@ -277,6 +310,8 @@ int qlinear_last_error(void *stream) {
   if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QL_ERR_CUDA;
   const int zero = 0;
   if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return QL_ERR_CUDA;
+  // a post-add / next-norm launch that gave up may have left its tile counter part-way
+  if (v != QL_OK && mv_resid_counter_reset() != 0) return QL_ERR_CUDA;
   return v;
 }
 

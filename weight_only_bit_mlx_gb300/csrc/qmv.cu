@@ -46,6 +46,25 @@ namespace cg = cooperative_groups;
 
 namespace qlk {
 
+// per-tile sums of squares and the finished-tile counter of kMvResid launches (one per
+// device that loads the library; the counter is back at zero after every launch)
+__device__ float g_resid_part[kMvResidMaxTiles * 16];
+__device__ unsigned g_resid_counter = 0;
+
+int mv_resid_scratch(float **part, unsigned **counter) {
+  void *a = nullptr, *b = nullptr;
+  if (cudaGetSymbolAddress(&a, g_resid_part) != cudaSuccess || cudaGetSymbolAddress(&b, g_resid_counter) != cudaSuccess)
+    return -1;
+  *part = static_cast<float *>(a);
+  *counter = static_cast<unsigned *>(b);
+  return 0;
+}
+
+int mv_resid_counter_reset() {
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_resid_counter, &zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
+}
+
 int mv_span_g(int bits) { return bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6>() : span_g<8>()); }
 
 // Shared-memory layout of one CTA (dynamic, 128-byte aligned):
@@ -81,6 +100,89 @@ template <int BITS, int NB, int MODE> struct MvLayout {
 // two row blocks) equally resident.  Measured on the decode pass: 3 per SM (80
 // registers) and 5 per SM (48 registers, spills) are both slower.
 constexpr int kMvCtasPerSm = 4;
+
+// The post-add / next-norm epilogue after the tile's residual rows are stored
+// (TensorFold PR #1514, "What changes": post-add/next-norm fusion): the tile's sum of
+// squares per activation row (its 16 channels in order) goes to its slot; the CTA that
+// finishes last (a device counter) adds the slots in tile order, and normalises every
+// channel of every row from the stored residual: out = bf16(r' / sqrt(mean r'^2 + eps)
+// * gamma).  No CTA waits for another; every order is fixed, so the result is
+// deterministic and each activation row's depends on that row alone.
+template <int NB>
+__device__ __forceinline__ void resid_norm_tail(const MvParams &p, int tile, float (*s_sq)[17]) {
+  __shared__ float s_wsum[kMvWarps][8 * NB];
+  __shared__ float s_rstd[8 * NB];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = p.m[0].n;
+  __syncthreads();  // s_sq complete
+  if (tid < p.rows) {
+    float sacc = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) sacc = __fadd_rn(sacc, s_sq[tid][c]);
+    p.part[(size_t)tile * 16 + tid] = sacc;
+  }
+  __threadfence();  // this tile's residual rows and slot are visible device-wide
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(p.counter, 1u) == (unsigned)(p.ntiles - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // sums of squares per activation row: tiles strided over the threads, then each
+  // warp's butterfly, then the warps in order
+  float a[8 * NB];
+#pragma unroll
+  for (int r = 0; r < 8 * NB; ++r) a[r] = 0.0f;
+  for (int tl = tid; tl < p.ntiles; tl += kMvThreads) {
+#pragma unroll
+    for (int r = 0; r < 8 * NB; ++r)
+      if (r < p.rows) a[r] = __fadd_rn(a[r], __ldcg(p.part + (size_t)tl * 16 + r));
+  }
+#pragma unroll
+  for (int r = 0; r < 8 * NB; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a[r] = __fadd_rn(a[r], __shfl_xor_sync(0xffffffffu, a[r], o));
+    if (lane == 0) s_wsum[warp][r] = a[r];
+  }
+  __syncthreads();
+  if (tid < p.rows) {
+    float tot = s_wsum[0][tid];
+    for (int w = 1; w < kMvWarps; ++w) tot = __fadd_rn(tot, s_wsum[w][tid]);
+    s_rstd[tid] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)n), p.eps)));
+  }
+  __syncthreads();
+  const bool vec = (n % 8) == 0 && (p.ldr % 8) == 0 && (p.ldn % 8) == 0 &&
+                   ((reinterpret_cast<uintptr_t>(p.resid) | reinterpret_cast<uintptr_t>(p.nout) |
+                     reinterpret_cast<uintptr_t>(p.gamma)) & 15) == 0;
+  if (vec) {
+    // 8 channels per 16-byte access, several accesses of each thread in flight
+    const int nch = n >> 3, total = p.rows * nch;
+#pragma unroll 4
+    for (int c = tid; c < total; c += kMvThreads) {
+      const int xr = c / nch, i = (c - xr * nch) * 8;
+      const uint4 rv = __ldcg(reinterpret_cast<const uint4 *>(p.resid + (size_t)xr * p.ldr + i));
+      const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(p.gamma + i));
+      const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      const float rs = s_rstd[xr];
+      uint32_t ow[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint16_t lo = f32_to_bf16_rn(__fmul_rn(__fmul_rn(bf16_to_f32(rw[q] & 0xFFFFu), rs), bf16_to_f32(gw[q] & 0xFFFFu)));
+        const uint16_t hi = f32_to_bf16_rn(__fmul_rn(__fmul_rn(bf16_to_f32(rw[q] >> 16), rs), bf16_to_f32(gw[q] >> 16)));
+        ow[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      *reinterpret_cast<uint4 *>(p.nout + (size_t)xr * p.ldn + i) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    }
+  } else {
+#pragma unroll 4
+    for (int e = tid; e < p.rows * n; e += kMvThreads) {
+      const int xr = e / n, i = e - xr * n;
+      const float v = bf16_to_f32(__ldcg(p.resid + (size_t)xr * p.ldr + i));
+      p.nout[(size_t)xr * p.ldn + i] = f32_to_bf16_rn(__fmul_rn(__fmul_rn(v, s_rstd[xr]), bf16_to_f32(p.gamma[i])));
+    }
+  }
+  if (tid == 0) atomicExch(p.counter, 0u);  // ready for the next launch (stream order)
+}
 
 template <int BITS, int NB, int MODE>
 __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __grid_constant__ MvParams p) {
@@ -290,6 +392,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
   else __syncthreads();
   if (rank == 0) {
     constexpr int NO = NB * 4;  // outputs per lane per matrix
+    __shared__ float s_sq[MODE == kMvResid ? 8 * NB : 1][17];  // [activation row][channel of the tile]
     for (int v = threadIdx.x; v < NO * 32; v += kMvThreads) {
       const int i = v >> 5, ln = v & 31;
       float acc[NMAT];
@@ -303,7 +406,18 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
       const int h = i >> 2, e = i & 3;
       const int row = tile * 16 + (ln >> 2) + ((e & 2) ? 8 : 0);
       const int xr = 8 * h + 2 * (ln & 3) + (e & 1);
-      if (row < n && xr < p.rows) {
+      if constexpr (MODE == kMvResid) {
+        // post-add: the stored residual r' = bf16(r + y) and its square
+        float sq = 0.0f;
+        if (row < n && xr < p.rows) {
+          uint16_t *rp = p.resid + (size_t)xr * p.ldr + row;
+          const uint16_t nb = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(*rp), acc[0]));
+          *rp = nb;
+          const float v = bf16_to_f32(nb);
+          sq = __fmul_rn(v, v);
+        }
+        s_sq[xr][(ln >> 2) + ((e & 2) ? 8 : 0)] = sq;
+      } else if (row < n && xr < p.rows) {
         const MvMat &M = p.m[mi];
         if constexpr (MODE == kMvFfn) {
           static_cast<uint16_t *>(M.out)[(size_t)xr * M.ldo + row] = swiglu_bf16(acc[0], acc[1]);
@@ -312,6 +426,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
         }
       }
     }
+    if constexpr (MODE == kMvResid) resid_norm_tail<NB>(p, tile, s_sq);
   }
 }
 
@@ -387,6 +502,7 @@ cudaError_t launch_mv(MvParams &p, int mode, int bits, int tiles, cudaStream_t s
   switch (mode) {
     case kMvFfn: return launch_mode<kMvFfn>(p, bits, tiles, st);
     case kMvAttn: return launch_mode<kMvAttn>(p, bits, tiles, st);
+    case kMvResid: return launch_mode<kMvResid>(p, bits, tiles, st);
     default: return launch_mode<kMvPlain>(p, bits, tiles, st);
   }
 }

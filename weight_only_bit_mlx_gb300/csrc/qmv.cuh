@@ -10,7 +10,7 @@ namespace qlk {
 constexpr int kMvWarps = 8;
 constexpr int kMvMaxCluster = 8;  // CTAs per cluster along k
 
-enum { kMvPlain = 0, kMvFfn = 1, kMvAttn = 2 };
+enum { kMvPlain = 0, kMvFfn = 1, kMvAttn = 2, kMvResid = 3 };
 
 struct MvMat {
   const uint32_t *wq;
@@ -31,6 +31,16 @@ struct MvParams {
   int *status;           // device status word (bounded waits record QL_ERR_TIMEOUT)
   int sb_bulk;           // scales/biases rows are 16-byte aligned: copied in bulk
   uint64_t budget_ns;    // bound of every device-side wait
+  // kMvResid: the post-add / next-norm epilogue (one weight, like kMvPlain)
+  uint16_t *resid;       // bf16 [rows, ldr], read and overwritten with bf16(resid + y)
+  int64_t ldr;
+  const uint16_t *gamma; // bf16 [n]
+  float eps;
+  uint16_t *nout;        // bf16 [rows, ldn]: the normalised stored residual times gamma
+  int64_t ldn;
+  float *part;           // [tiles][16] per-tile sums of squares (library scratch)
+  unsigned *counter;     // tiles finished (library scratch, zero between calls)
+  int ntiles;            // 16-row tiles of the launch
   // filled by launch_mv from k and bits
   int groups;
   int wpr;
@@ -43,6 +53,12 @@ int mv_span_g(int bits);
 
 // k-decomposition used by every decode launch (a function of k and bits only)
 void mv_geometry(int k, int bits, int &groups, int &span_g, int &nwarps, int &cs);
+
+// Maximum 16-row tiles of a kMvResid launch (n <= 65536) and the device addresses of its
+// per-tile partial sums and finished-tile counter (current device); reset the counter.
+constexpr int kMvResidMaxTiles = 4096;
+int mv_resid_scratch(float **part, unsigned **counter);
+int mv_resid_counter_reset();
 
 // Enqueue one decode launch over `tiles` 16-row tiles.
 cudaError_t launch_mv(MvParams &p, int mode, int bits, int tiles, cudaStream_t st);

@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
         "qattn_qknorm_rope_kv": (ctypes.c_int, [P, I64, P, I64, P, I64, I32, I32, I32, I32, I32, ctypes.c_float,
                                                 ctypes.c_float, P, P, P, P, I64, P, P, I32, P]),
         "qresid_rmsnorm": (ctypes.c_int, [P, I64, P, I64, I32, I32, P, ctypes.c_float, P, I64, P]),
+        "qlinear_mv_resid_norm": (ctypes.c_int, [W, P, I32, I64, P, I64, P, ctypes.c_float, P, I64, P]),
         "qlinear_last_error": (ctypes.c_int, [P]),
         "qlinear_set_wait_budget_ns": (U64, [U64]),
         "qlinear_wait_probe": (ctypes.c_int, [U64, P]),
@@ -274,6 +275,23 @@ def qresid_rmsnorm(y: torch.Tensor, resid: torch.Tensor, gamma: torch.Tensor, ep
         out = torch.empty(rows, n, dtype=torch.bfloat16, device=y.device)
     _check(LIB.qresid_rmsnorm(y.data_ptr(), y.stride(0), r.data_ptr(), r.stride(0), rows, n, gamma.data_ptr(),
                               float(eps), out.data_ptr(), out.stride(0), _stream(stream)), "qresid_rmsnorm")
+    return out
+
+
+def qlinear_mv_resid_norm(w: QWeight, x: torch.Tensor, resid: torch.Tensor, gamma: torch.Tensor, eps: float,
+                          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = W x; resid <- bf16(resid + y) in place; returns out = bf16(rmsnorm(resid) * gamma),
+    in one launch.  x: bfloat16 [rows, k]; resid: bfloat16 [rows, n]; gamma: bfloat16 [n]."""
+    x, rows, ldx = _act(x, w.k)
+    r = _rows2d(resid, torch.bfloat16, "resid")
+    if tuple(r.shape) != (rows, w.n) or gamma.dtype != torch.bfloat16 or gamma.numel() != w.n or \
+            not gamma.is_contiguous():
+        raise ValueError("resid must be [rows, n] and gamma a contiguous bfloat16 [n]")
+    if out is None:
+        out = torch.empty(rows, w.n, dtype=torch.bfloat16, device=x.device)
+    _check(LIB.qlinear_mv_resid_norm(ctypes.byref(w.c), x.data_ptr(), rows, ldx, r.data_ptr(), r.stride(0),
+                                     gamma.data_ptr(), float(eps), out.data_ptr(), out.stride(0), _stream(stream)),
+           "qlinear_mv_resid_norm")
     return out
 
 
