@@ -379,28 +379,40 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
 #pragma unroll
     for (int i = 0; i < NV; ++i) red[(warp * NV + i) * 32 + lane] = y[i];
     named_bar_sync(kBarCompute, kMvComputeThreads);
-    float *dst = (p.cs > 1 ? cluster.map_shared_rank(csum, 0) : csum) + rank * NV * 32;
-    for (int v = threadIdx.x; v < NV * 32; v += kMvComputeThreads) {
-      const int i = v >> 5, ln = v & 31;
-      float acc = red[i * 32 + ln];
+    if (p.cs > 1) {
+      float *dst = cluster.map_shared_rank(csum, 0) + rank * NV * 32;
+      for (int v = threadIdx.x; v < NV * 32; v += kMvComputeThreads) {
+        const int i = v >> 5, ln = v & 31;
+        float acc = red[i * 32 + ln];
 #pragma unroll
-      for (int w = 1; w < kMvWarps; ++w) acc = __fadd_rn(acc, red[(w * NV + i) * 32 + ln]);
-      dst[i * 32 + ln] = acc;
+        for (int w = 1; w < kMvWarps; ++w) acc = __fadd_rn(acc, red[(w * NV + i) * 32 + ln]);
+        dst[i * 32 + ln] = acc;
+      }
     }
   }
+  // without a cluster the warp partials are added in warp order right below, where
+  // they are stored (the same order; the barrier above made them visible)
   if (p.cs > 1) cluster.sync();
-  else __syncthreads();
   if (rank == 0) {
     constexpr int NO = NB * 4;  // outputs per lane per matrix
     __shared__ float s_sq[MODE == kMvResid ? 8 * NB : 1][17];  // [activation row][channel of the tile]
     for (int v = threadIdx.x; v < NO * 32; v += kMvThreads) {
       const int i = v >> 5, ln = v & 31;
       float acc[NMAT];
+      if (p.cs > 1) {
 #pragma unroll
-      for (int t = 0; t < NMAT; ++t) acc[t] = csum[(t * NO + i) * 32 + ln];
-      for (int r = 1; r < p.cs; ++r) {
+        for (int t = 0; t < NMAT; ++t) acc[t] = csum[(t * NO + i) * 32 + ln];
+        for (int r = 1; r < p.cs; ++r) {
 #pragma unroll
-        for (int t = 0; t < NMAT; ++t) acc[t] = __fadd_rn(acc[t], csum[r * NV * 32 + (t * NO + i) * 32 + ln]);
+          for (int t = 0; t < NMAT; ++t) acc[t] = __fadd_rn(acc[t], csum[r * NV * 32 + (t * NO + i) * 32 + ln]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < NMAT; ++t) {
+          acc[t] = red[(t * NO + i) * 32 + ln];
+#pragma unroll
+          for (int w = 1; w < kMvWarps; ++w) acc[t] = __fadd_rn(acc[t], red[(w * NV + t * NO + i) * 32 + ln]);
+        }
       }
       // value i of lane ln: half h = i / 4, element e = i % 4
       const int h = i >> 2, e = i & 3;
