@@ -70,8 +70,8 @@ int mv_span_g(int bits) { return bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6
 // Shared-memory layout of one CTA (dynamic, 128-byte aligned):
 //   wsm [NMAT][16][wpitch]             weight rows of the span (one bulk copy per row and chunk);
 //                                      after the last group it holds the warp partials
-//                                      red[kMvWarps][NV][32] and, without a cluster, the
-//                                      CTA partial csum[NV][32]
+//                                      red[kMvWarps][NV][32] (without a cluster they are
+//                                      added in warp order where the outputs are stored)
 //   sbf [NMAT][span][16] float2        per (group, row): (16s, b - 16s) for 4-bit, (s, b) else
 //   bars[kNch]                         one per chunk
 //   cpart[cs][NV][32] fp32             with a cluster of cs > 1 CTAs: every rank's CTA
