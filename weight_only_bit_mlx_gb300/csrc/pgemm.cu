@@ -45,6 +45,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -767,15 +768,15 @@ static void *scratch_get(size_t bytes) {
 
 // SMs of the current device (cached per device)
 static int sm_count() {
-  static int cached[kMaxDev] = {};
+  static std::atomic<int> cached[kMaxDev];  // per device, 0 until first queried
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
-  if (cached[dev] == 0) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
-    cached[dev] = v;
+  int c = cached[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 1;
+    cached[dev].store(c, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return c;
 }
 
 template <int BITS>
@@ -803,14 +804,14 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
                                (uint64_t)G * 2, 8, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!sc_tma) tmSc = tmX;  // never read
   if (!bi_tma) tmBi = tmX;  // never read
-  static bool attr_set[kMaxDev] = {};
+  static std::atomic<bool> attr_set[kMaxDev];  // per device; setting the attribute twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < kMaxDev && !attr_set[dev]) {
+  if (dev >= 0 && dev < kMaxDev && !attr_set[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(pg::pgemm_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc) !=
         cudaSuccess)
       return QL_ERR_LAUNCH;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_relaxed);
   }
   pg::Params p;
   p.scales = w->scales;

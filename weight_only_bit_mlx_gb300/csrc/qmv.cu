@@ -37,6 +37,8 @@
 // data alone, so a row's result does not depend on how many rows share the call.
 #include <cooperative_groups.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "qmv.cuh"
 #include "qmv_core.cuh"
@@ -445,10 +447,10 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
 template <int BITS, int NB, int MODE>
 static cudaError_t launch_t(const MvParams &p, int tiles, cudaStream_t st) {
   using Lay = MvLayout<BITS, NB, MODE>;
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];  // per device; setting the attributes twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_done[dev].load(std::memory_order_relaxed)) {
     cudaError_t e = cudaFuncSetAttribute(qmv_kernel<BITS, NB, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::max_bytes());
     if (e != cudaSuccess) return e;
@@ -457,7 +459,7 @@ static cudaError_t launch_t(const MvParams &p, int tiles, cudaStream_t st) {
     e = cudaFuncSetAttribute(qmv_kernel<BITS, NB, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_relaxed);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * p.cs));
