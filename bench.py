@@ -15,7 +15,7 @@ gate 2048 -> 2048, o 2048 -> 2048), MLX affine 4-bit group 64 by default:
 Decode passes are captured once as CUDA graphs (the kernels are a few
 microseconds long, so host launch time would otherwise dominate); prefill is
 launched directly.  Inputs are seeded synthetic data with the pages' shapes and
-distributions; every decode pass reads 503 MB of distinct weights, far more than
+distributions; every decode pass reads 502.5 MB of distinct weights, far more than
 the 129 MB L2, so no L2 flush is needed between iterations.
 
 Reported beside the step (timed after it): the decode pass with the steps between
@@ -130,7 +130,7 @@ def workload_config(bits, world):
                         f"(q,g,o 2048->2048; k,v 2048->512), MLX affine {bits}-bit g64; decode R=1 "
                         f"(value) and R=16, prefill M={PROMPT} pgemm",
             "rows": 1, "prompt_rows": PROMPT, "bits": bits,
-            "l2": "no flush: every decode pass streams 503 MB of distinct weights (> 129 MB L2)",
+            "l2": "no flush: every decode pass streams 502.5 MB of distinct weights (> 129 MB L2)",
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 

@@ -1,0 +1,47 @@
+"""The bench's algorithmic byte and flop counts (the numerators of every roofline
+figure it reports), pinned to hand-computed values for the workload's shapes."""
+from __future__ import annotations
+
+import pytest
+
+import bench
+
+
+def test_weight_bytes_by_hand():
+    # 2048 x 2048 at 4 bits: codes 2048*2048/2, scales + biases 2 * 2048 * 32 bf16
+    assert bench.weight_bytes(2048, 2048, 4) == 2_097_152 + 262_144
+    # 8192 x 2048 at 6 bits: codes 8192*2048*6/8, scales + biases 2 * 8192 * 32 * 2
+    assert bench.weight_bytes(8192, 2048, 6) == 12_582_912 + 1_048_576
+    # 2048 x 8192 at 8 bits
+    assert bench.weight_bytes(2048, 8192, 8) == 16_777_216 + 1_048_576
+
+
+def test_layer_shapes_match_the_workload():
+    shapes = bench.layer_shapes()
+    assert len(shapes) == 16 * 3 + 6 * 5
+    ffn = [(n, k) for name, n, k in shapes if name.endswith((".w1", ".w3"))]
+    assert ffn == [(8192, 2048)] * 32
+    assert all((n, k) == (2048, 8192) for name, n, k in shapes if name.endswith(".w2"))
+    kv = [(n, k) for name, n, k in shapes if name.endswith((".k", ".v"))]
+    assert kv == [(512, 2048)] * 12
+
+
+def test_decode_bytes_by_hand():
+    # weights of one pass: 16 x (w1 + w3 + w2) + 6 x (q + k + v + gate + o), 4-bit
+    w = lambda n, k: n * k // 2 + 2 * n * (k // 64) * 2  # noqa: E731
+    weights = 16 * (2 * w(8192, 2048) + w(2048, 8192)) + 6 * (3 * w(2048, 2048) + 2 * w(512, 2048))
+    # activations read and outputs written per launch at R = 1
+    attn = 6 * ((2048 * 2 + (2 * 2048 + 2 * 512) * 4) + (2048 * 2 + 2048 * 4))
+    ffn = 16 * ((2048 * 2 + 8192 * 2) + (8192 * 2 + 2048 * 4))
+    assert bench.decode_bytes(4, 1) == weights + attn + ffn
+    assert weights == 502_530_048  # 502.5 MB of distinct weights per pass
+
+
+def test_prefill_flops_by_hand():
+    per_layer_ffn = 3 * 2 * 8192 * 8192 * 2048
+    per_attn = 2 * 8192 * 2048 * (3 * 2048 + 2 * 512)
+    assert bench.prefill_flops() == 16 * per_layer_ffn + 6 * per_attn
+
+
+def test_job_throughput_is_units_over_time():
+    assert bench.job_throughput(503_472_128, 10, 2.62, 1) == pytest.approx(503_472_128 * 10 / 2.62e-3, rel=1e-12)
