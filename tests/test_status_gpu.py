@@ -24,3 +24,29 @@ def test_wait_probe_times_out_and_context_survives():
     torch.cuda.synchronize()
     assert torch.isfinite(y).all()
     assert q.qlinear_last_error() == q.QL_OK
+
+
+def test_fused_resid_norm_after_timeout_status():
+    """Reading a non-zero status also re-arms the fused post-add / next-norm epilogue
+    (its tile counter is zeroed); the fused call must then still match the unfused
+    pair bit for bit, twice in a row."""
+    import numpy as np
+    from weight_only_bit_mlx_gb300 import qlinear as q
+    from weight_only_bit_mlx_gb300 import synth
+
+    q.qlinear_wait_probe(1_000_000)  # 1 ms
+    assert q.qlinear_last_error() == q.QL_ERR_TIMEOUT
+    n, k = 1024, 2048
+    w = q.QWeight.from_numpy(synth.make_weight(n, k, 4, config_id=71, tensor_id=1))
+    x = q.bf16_from_bits(synth.make_x(3, k, config_id=71, tensor_id=2))
+    r0 = q.bf16_from_bits(synth.make_bf16((3, n), config_id=71, tensor_id=3))
+    gamma = q.bf16_from_bits(synth.make_bf16((n,), 0.5, 1.5, config_id=71, tensor_id=4))
+    rs = r0.clone()
+    out_s = q.qresid_rmsnorm(q.qlinear_mv_rows(w, x), rs, gamma, 1e-5)
+    for _ in range(2):
+        rf = r0.clone()
+        out_f = q.qlinear_mv_resid_norm(w, x, rf, gamma, 1e-5)
+        torch.cuda.synchronize()
+        assert q.qlinear_last_error() == q.QL_OK
+        assert torch.equal(rf.view(torch.int16), rs.view(torch.int16))
+        assert np.array_equal(out_f.view(torch.int16).cpu().numpy(), out_s.view(torch.int16).cpu().numpy())
