@@ -691,6 +691,44 @@ def run_case(args):
                       "status": q.qlinear_last_error()}), flush=True)
 
 
+def interp_cost(points, rows):
+    """Per-call cost of a window of `rows` rows from costs measured at a few window
+    sizes (TensorFold PR #1696, later revision, "What it adds": windows are timed at a
+    handful of sizes at load and the rest interpolated).  points: [(rows_i, us_i)] with
+    distinct rows_i.  Between two measured sizes the cost is the straight line through
+    them; below the smallest size it is the smallest size's cost; above the largest it
+    follows the last segment (a single measured size is a constant).  Returns None when
+    no size was measured."""
+    pts = sorted((int(r), float(c)) for r, c in points if c is not None)
+    if not pts:
+        return None
+    if rows <= pts[0][0] or len(pts) == 1:
+        return pts[0][1]
+    for (r0, c0), (r1, c1) in zip(pts, pts[1:]):
+        if rows <= r1:
+            return c0 + (c1 - c0) * (rows - r0) / (r1 - r0)
+    (r0, c0), (r1, c1) = pts[-2], pts[-1]
+    return c0 + (c1 - c0) * (rows - r0) / (r1 - r0)
+
+
+def window_choice(table, max_rows, mv_max_rows=16):
+    """For every window size 1..max_rows, the cheaper call by interpolated cost
+    (qlinear_mv_rows only up to mv_max_rows rows), merged into runs:
+    [{"rows": [lo, hi], "call": name}, ...]."""
+    mv = [(t["rows"], t["mv_rows_us"]) for t in table if t["mv_rows_us"] is not None]
+    pg = [(t["rows"], t["pgemm_us"]) for t in table]
+    runs = []
+    for R in range(1, max_rows + 1):
+        c_mv = interp_cost(mv, R) if R <= mv_max_rows else None
+        c_pg = interp_cost(pg, R)
+        call = "qlinear_mv_rows" if c_mv is not None and (c_pg is None or c_mv <= c_pg) else "qlinear_pgemm"
+        if runs and runs[-1]["call"] == call:
+            runs[-1]["rows"][1] = R
+        else:
+            runs.append({"rows": [R, R], "call": call})
+    return runs
+
+
 def window_table(args, q, make_w, gen, dev):
     """Cost of one window of R rows through qlinear_mv_rows (R <= 16) and through
     qlinear_pgemm (any R), with enough distinct weight copies cycled to exceed L2, so
@@ -731,11 +769,12 @@ def window_table(args, q, make_w, gen, dev):
         best = "qlinear_mv_rows" if mv is not None and mv <= pg else "qlinear_pgemm"
         table.append({"rows": R, "mv_rows_us": mv, "pgemm_us": pg, "cheaper": best,
                       "us_per_row": min(x for x in (mv, pg) if x is not None) / R})
-    # linear interpolation of the per-call cost between measured window sizes
     print(json.dumps({"case": "window", "bits": args.bits, "n": n, "k": k, "weight_copies": copies,
                       "weight_bytes": wbytes, "table": table,
                       "interpolation": "cost(R) for R between two measured sizes is the linear interpolation "
-                                       "of their per-call costs", "status": q.qlinear_last_error()}), flush=True)
+                                       "of their per-call costs",
+                      "choice": window_choice(table, rows_list[-1]),
+                      "status": q.qlinear_last_error()}), flush=True)
 
 
 def main():

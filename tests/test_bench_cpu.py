@@ -45,3 +45,33 @@ def test_prefill_flops_by_hand():
 
 def test_job_throughput_is_units_over_time():
     assert bench.job_throughput(503_472_128, 10, 2.62, 1) == pytest.approx(503_472_128 * 10 / 2.62e-3, rel=1e-12)
+
+
+def test_interp_cost_is_piecewise_linear():
+    pts = [(1, 9.0), (2, 9.2), (4, 9.4), (8, 9.6), (16, 9.8)]
+    # measured sizes come back exactly; in-between sizes sit on the segment
+    for r, c in pts:
+        assert bench.interp_cost(pts, r) == pytest.approx(c)
+    assert bench.interp_cost(pts, 3) == pytest.approx(9.3)
+    assert bench.interp_cost(pts, 12) == pytest.approx(9.7)
+    # order of the points does not matter; missing costs are ignored
+    assert bench.interp_cost(list(reversed(pts)) + [(32, None)], 6) == pytest.approx(9.5)
+    # below the smallest size: its cost; above the largest: the last segment extended
+    assert bench.interp_cost([(4, 5.0), (8, 7.0)], 1) == pytest.approx(5.0)
+    assert bench.interp_cost([(4, 5.0), (8, 7.0)], 12) == pytest.approx(9.0)
+    assert bench.interp_cost([(4, 5.0)], 100) == pytest.approx(5.0)
+    assert bench.interp_cost([], 3) is None
+
+
+def test_window_choice_runs():
+    table = [{"rows": r, "mv_rows_us": mv, "pgemm_us": pg} for r, mv, pg in
+             [(1, 9.0, 37.0), (2, 9.1, 37.0), (4, 9.2, 37.1), (8, 9.5, 37.1), (16, 9.8, 37.2),
+              (32, None, 37.2), (64, None, 37.3)]]
+    assert bench.window_choice(table, 64) == [{"rows": [1, 16], "call": "qlinear_mv_rows"},
+                                              {"rows": [17, 64], "call": "qlinear_pgemm"}]
+    # a matvec that grows past the GEMM's cost inside 1..16 hands over where the lines cross
+    table2 = [{"rows": 1, "mv_rows_us": 10.0, "pgemm_us": 30.0},
+              {"rows": 16, "mv_rows_us": 40.0, "pgemm_us": 30.0}]
+    # crossing at 10 + 2 (R - 1) = 30  ->  R = 11 (ties go to the matvec)
+    assert bench.window_choice(table2, 20) == [{"rows": [1, 11], "call": "qlinear_mv_rows"},
+                                               {"rows": [12, 20], "call": "qlinear_pgemm"}]
