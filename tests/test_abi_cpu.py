@@ -148,3 +148,21 @@ def test_fused_resid_norm_rejects_bad_arguments_on_host(q):
     assert L.qlinear_mv_resid_norm(ctypes.byref(w), P, 17, 128, P, 64, P, 1e-5, P, 64, None) == q.QL_ERR_ROWS
     assert L.qlinear_mv_resid_norm(ctypes.byref(w), P, 2, 128, P, 32, P, 1e-5, P, 64, None) == q.QL_ERR_ALIGN
     assert L.qlinear_mv_resid_norm(ctypes.byref(w), P + 8, 1, 128, P, 64, P, 1e-5, P, 64, None) == q.QL_ERR_ALIGN
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """A copy of the Python package with no libqlinear.so beside it must refuse to
+    import: there is no CPU or eager fallback behind the binding."""
+    import shutil
+    import sys
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "weight_only_bit_mlx_gb300")
+    dst = tmp_path / "weight_only_bit_mlx_gb300"
+    dst.mkdir()
+    for name in os.listdir(src):
+        if name.endswith(".py"):
+            shutil.copy(os.path.join(src, name), dst / name)
+    assert not (dst / "libqlinear.so").exists()
+    r = subprocess.run([sys.executable, "-c", "import weight_only_bit_mlx_gb300.qlinear"], cwd=tmp_path,
+                       env={**os.environ, "PYTHONPATH": str(tmp_path)}, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "is not built" in r.stderr
