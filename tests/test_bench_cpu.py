@@ -75,3 +75,36 @@ def test_window_choice_runs():
     # crossing at 10 + 2 (R - 1) = 30  ->  R = 11 (ties go to the matvec)
     assert bench.window_choice(table2, 20) == [{"rows": [1, 11], "call": "qlinear_mv_rows"},
                                                {"rows": [12, 20], "call": "qlinear_pgemm"}]
+
+
+def _run_bench(args, env_extra=None):
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {**os.environ, **(env_extra or {})}
+    r = subprocess.run([sys.executable, "bench.py", *args], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_prints_one_contract_line():
+    (line,) = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0"])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["metric"] == bench.METRIC and line["steps"] == 1 and line["value"] > 0
+    assert line["dtype"] == "f64" and line["data"] == "synthetic" and line["vs_baseline"] is None
+    # the same workload description as the CUDA arm's line, plus what one step samples
+    cfg = dict(line["config"])
+    assert cfg.pop("sample")
+    assert cfg == bench.workload_config(4, 1)
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_do_no_work():
+    assert _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0"],
+                      {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
