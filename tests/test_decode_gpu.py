@@ -111,8 +111,34 @@ def test_fused_ffn_decode(q, rows):
         assert torch.equal(q.qffn_swiglu_mv(d1, d3, xd[r]), h[r:r + 1])
 
 
+@pytest.mark.parametrize("bits,n,k", [(6, 8192, 2048), (8, 8192, 2048), (4, 1000, 192), (6, 37, 64),
+                                      (8, 520, 1024)])
+@pytest.mark.parametrize("rows", [1, 5, 16])
+def test_fused_ffn_bits_and_ragged(q, bits, n, k, rows):
+    # the fused w1 + w3 + SwiGLU decode at 6 and 8 bits and on channel counts that leave
+    # a ragged last 16-row tile: h against the propagated float64 bound, fused ==
+    # unfused and R rows == R one-row calls, bit for bit
+    cid = 60 + bits
+    w1 = U.weight(n, k, bits, config_id=cid, tensor_id=1)
+    w3 = U.weight(n, k, bits, config_id=cid, tensor_id=3)
+    x = synth.make_x(rows, k, config_id=cid)
+    d1, d3, xd = U.dev_weight(w1), U.dev_weight(w3), U.dev_x(x)
+    h = q.qffn_swiglu_mv(d1, d3, xd)
+    a = q.qlinear_mv_rows(d1, xd)
+    c = q.qlinear_mv_rows(d3, xd)
+    assert torch.equal(h, q.qswiglu(a, c))
+    torch.cuda.synchronize()
+    a64, aa, c64, ac, h64 = orc.ffn_swiglu(x, w1, w3)
+    U.assert_close(a, a64, aa, "w1 x")
+    U.assert_close(c, c64, ac, "w3 x")
+    hg = h.float().cpu().numpy().astype(np.float64)
+    assert (np.abs(hg - h64) <= U.h_bound(a64, aa, c64, ac, h64)).all(), "h out of propagated bound"
+    for r in (0, rows - 1):
+        assert torch.equal(q.qffn_swiglu_mv(d1, d3, xd[r]), h[r:r + 1])
+
+
 @pytest.mark.parametrize("rows", [1, 4, 16])
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [4, 6, 8])
 def test_fused_attention_projections(q, rows, bits):
     # q 2048->2048 (32 heads x 64), k, v 2048->512 (8 KV heads x 64), gate 2048->2048
     ns = {"q": 2048, "k": 512, "v": 512, "g": 2048}
