@@ -233,7 +233,9 @@ int qresid_rmsnorm(const float *y, int64_t ldy, uint16_t *resid, int64_t ldr, in
  *   x: bf16 [rows, ldx]; resid: bf16 bits [rows, ldr], read and overwritten; gamma: bf16
  *   [n]; out: bf16 bits [rows, ldo] (must not overlap resid).  rows 1..16, n <= 65536.
  *   Uses a library-owned per-device scratch (per-tile sums and a counter that every launch
- *   leaves at zero): calls on one device must be ordered on one stream.  Errors as
+ *   leaves at zero): calls on one device must be ordered on one stream.  The first call on
+ *   a device looks up the scratch's device address and caches it; make that first call
+ *   before any stream capture.  Errors as
  *   qlinear_mv_rows, plus QL_ERR_NULL for resid/gamma/out and QL_ERR_SHAPE for eps < 0.
  */
 int qlinear_mv_resid_norm(const ql_weight *w, const uint16_t *x, int32_t rows, int64_t ldx,

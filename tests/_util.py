@@ -44,3 +44,22 @@ def h_bound(a64, aa, c64, ac, h64):
     ta, tc = tol(aa), tol(ac)
     return (1.1 * (np.abs(c64) + tc) * ta + (np.abs(orc.silu(a64)) + 1.1 * ta) * tc
             + 2.0 ** -8 * np.abs(h64) + 1e-6)
+
+
+def pack_codes(q, bits):
+    """Pack integer codes q[n, k] into uint32 rows, value j at bit offset bits*j of its
+    row's little-endian stream (a field may straddle two words).  Test-side packer,
+    vectorised over rows; independent of the oracle's unpacker."""
+    q = np.asarray(q, dtype=np.uint64)
+    n, k = q.shape
+    nw = k * bits // 32
+    per = 32 // int(np.gcd(32, bits))        # codes per period of whole words
+    wper = per * bits // 32                  # words per period
+    words = np.zeros((n, nw + 1), dtype=np.uint64)
+    for j in range(per):
+        pos = bits * j
+        w, off = pos // 32, pos % 32
+        v = q[:, j::per] << np.uint64(off)
+        words[:, w:nw:wper] |= v & np.uint64(0xFFFFFFFF)
+        words[:, w + 1:nw + 1:wper] |= v >> np.uint64(32)
+    return words[:, :nw].astype(np.uint32)

@@ -48,9 +48,11 @@ def test_noalloc_matches_pgemm_on_two_calls_in_a_row():
     torch.cuda.synchronize()
     assert q.qlinear_last_error() == q.QL_OK
     for (w, X, wd, Xd, Y_ref), Y in zip(data, outs):
-        _, A = orc.pgemm(X, w)
-        diff = np.abs(Y.cpu().numpy().astype(np.float64) - Y_ref.cpu().numpy().astype(np.float64))
-        assert (diff <= U.tol(A)).all()
+        # the same kernels on the same inputs: the same bits as qlinear_pgemm
+        assert torch.equal(Y, Y_ref)
+        # and within the library's tolerance of the float64 oracle
+        y64, A = orc.pgemm(X, w)
+        U.assert_close(Y, y64, A, "qlinear_pgemm_noalloc")
 
 
 def test_noalloc_rejects_problems_beyond_its_fixed_scratch():
@@ -62,6 +64,12 @@ def test_noalloc_rejects_problems_beyond_its_fixed_scratch():
     Y = torch.zeros(3000, 64, device="cuda")
     assert _noalloc(q, w, X, Y) == q.QL_ERR_TOO_LARGE
     assert "fixed scratch" in q.qlinear_strerror(q.QL_ERR_TOO_LARGE)
-    assert _noalloc(q, w, X[:2730], Y[:2730]) == q.QL_OK  # 2730 * 384 fits
+    # the largest m that fits (2730 * 384 values), on seeded non-zero rows: the same bits
+    # as qlinear_pgemm, so the scratch pitch holds at the size limit
+    Xs = U.dev_x(synth.make_x(2730, 8192, config_id=81, tensor_id=100))
+    Ys = torch.full((2730, 64), float("nan"), device="cuda")
+    assert _noalloc(q, w, Xs, Ys) == q.QL_OK
+    Y_ref = q.qlinear_pgemm(w, Xs)
     torch.cuda.synchronize()
-    assert torch.isfinite(Y[:2730]).all()
+    assert q.qlinear_last_error() == q.QL_OK
+    assert torch.equal(Ys, Y_ref)

@@ -13,26 +13,6 @@ namespace qlk {
 constexpr int kGroup = 64;
 constexpr int kErrTimeout = -9;
 
-__device__ __forceinline__ uint32_t ldg_nc_u32(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint2 ldg_nc_v2(const uint32_t *p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-               : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint4 ldg_nc_v4(const uint32_t *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
 // activations: keep them in L1, they are re-read by every CTA on the SM
 __device__ __forceinline__ uint4 ldg_v4(const void *p) {
   uint4 v;
@@ -90,16 +70,15 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t w, uint32_t w4, int t) {
   return fma_bf16x2(v, kBf16One2, kBf16Neg128x2);
 }
 
-// 4-bit, offset form: codes t and t+4 of word w (t = 0..3) as the bf16 pair
-// (1 + q_t/16, 1 + q_{t+4}/16).  A bf16 in [1, 2) has a unit in the last place of
-// 2^-7, so a 4-bit code placed in mantissa bits 3..6 of 1.0 gives 1 + q/16 exactly;
-// one shift and one mask-or per pair, no arithmetic.  A dot product with these
-// values is S + P/16 (S = sum of the activations, P = sum q*x), so
-// sum (s*q + b) x = 16s * dot + (b - 16s) * S.
-constexpr uint32_t kBf16One2Mask4 = 0x00780078u;  // mantissa bits 3..6 of both halves
-__device__ __forceinline__ uint32_t q4_off_pair(uint32_t w, int t) {
-  const uint32_t v = t == 0 ? (w << 3) : (w >> (4 * t - 3));
-  return (v & kBf16One2Mask4) | kBf16One2;
+// 4-bit: codes t and t+4 of word w (t = 0..3) as the exact bf16 pair (q_t, q_{t+4}).
+// Nibble t sits at bits 4t..4t+3 and nibble t+4 at bits 16+4t..16+4t+3, so one shift
+// puts both at the bottom of their 16-bit halves; the mask-or places them in the
+// mantissas of (128, 128) and one bf16x2 fma takes the 128 off.  Pairing t with t+4
+// (instead of 2t with 2t+1) saves the byte permute; the activations are loaded in the
+// same order.
+__device__ __forceinline__ uint32_t q4_split_pair(uint32_t w, int t) {
+  const uint32_t v = ((t == 0 ? w : (w >> (4 * t))) & 0x000F000Fu) | kBf16Magic2;
+  return fma_bf16x2(v, kBf16One2, kBf16Neg128x2);
 }
 
 // 6-bit: a 12-bit field f (two 6-bit codes, lower code in bits 0..5)

@@ -25,12 +25,9 @@
 //     codes are converted exactly to bf16 and multiplied on the tensor cores with
 //     mma.sync m16n8k16 (rows of W as A, activation rows as B), a fresh fp32
 //     accumulator per group, and the affine step follows in group order:
-//       6/8-bit:  P_g = sum_{j in g} q_j x_j;          y = fma(s, P_g, y); y = fma(b, S_g, y)
-//       4-bit:    D_g = sum_{j in g} (1 + q_j/16) x_j; y = fma(16s, D_g, y); y = fma(b - 16s, S_g, y)
-//     (the 4-bit codes go into the mantissa of 1.0, two instructions per bf16 pair;
-//     D_g = S_g + P_g/16, so both forms are s*P_g + b*S_g).  S_g = sum_{j in g} x_j
-//     is computed once per activation row and group while the activations are
-//     staged, in a fixed order;
+//       P_g = sum_{j in g} q_j x_j;   y = fma(s, P_g, y); y = fma(b, S_g, y)
+//     with S_g = sum_{j in g} x_j from the same tensor-core path (A = 1), once per
+//     activation row and group;
 //   * warp partials are added in warp order through shared memory, CTA partials in
 //     rank order through distributed shared memory.  No atomics, no scratch memory.
 // The tensor core computes every output column (activation row) from that column's
@@ -38,6 +35,7 @@
 #include <cooperative_groups.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 #include "qmv.cuh"
@@ -53,12 +51,30 @@ namespace qlk {
 __device__ float g_resid_part[kMvResidMaxTiles * 16];
 __device__ unsigned g_resid_counter = 0;
 
+// Device addresses of the two arrays, looked up once per device (with that device
+// current) and cached: in host code the arrays' names are only host-side stand-ins.
+// The first post-add / next-norm call on a device does the lookup, so it should come
+// before any stream capture.
+static std::mutex g_resid_mu;
+static float *g_resid_part_addr[64];
+static unsigned *g_resid_counter_addr[64];
+
 int mv_resid_scratch(float **part, unsigned **counter) {
-  void *a = nullptr, *b = nullptr;
-  if (cudaGetSymbolAddress(&a, g_resid_part) != cudaSuccess || cudaGetSymbolAddress(&b, g_resid_counter) != cudaSuccess)
-    return -1;
-  *part = static_cast<float *>(a);
-  *counter = static_cast<unsigned *>(b);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> lk(g_resid_mu);
+  if (g_resid_part_addr[dev] == nullptr) {
+    void *a = nullptr, *b = nullptr;
+    if (cudaGetSymbolAddress(&a, g_resid_part) != cudaSuccess ||
+        cudaGetSymbolAddress(&b, g_resid_counter) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return -1;
+    }
+    g_resid_counter_addr[dev] = static_cast<unsigned *>(b);
+    g_resid_part_addr[dev] = static_cast<float *>(a);
+  }
+  *part = g_resid_part_addr[dev];
+  *counter = g_resid_counter_addr[dev];
   return 0;
 }
 
@@ -74,7 +90,7 @@ int mv_span_g(int bits) { return bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6
 //                                      after the last group it holds the warp partials
 //                                      red[kMvWarps][NV][32] (without a cluster they are
 //                                      added in warp order where the outputs are stored)
-//   sbf [NMAT][span][16] float2        per (group, row): (16s, b - 16s) for 4-bit, (s, b) else
+//   sbf [NMAT][span][16] float2        per (group, row): (scale, bias) in fp32
 //   bars[kNch]                         one per chunk
 //   cpart[cs][NV][32] fp32             with a cluster of cs > 1 CTAs: every rank's CTA
 //                                      partial (only rank 0's copy is read); a region of
@@ -197,7 +213,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
   constexpr int SPAN = span_g<BITS>();
   constexpr int GB = gbytes<BITS>();
   constexpr int WP = wpitch<BITS>();
-  constexpr bool kOff = BITS == 4;  // offset-form conversion (1 + q/16)
+  constexpr bool kPair4 = BITS == 4;  // 4-bit codes paired (t, t+4): activations in that order
   extern __shared__ __align__(128) uint8_t smem[];
   float2 *sbf = reinterpret_cast<float2 *>(smem + Lay::kSbf);
   float *red = reinterpret_cast<float *>(smem + Lay::kRed);
@@ -274,7 +290,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
       // ---- every warp computes
       const int tid = threadIdx.x;  // 0 .. kMvComputeThreads-1
       // Scales and biases of the span (not written by a preceding kernel, so read
-      // before the dependency wait) -> fp32 factor pairs.  16-byte vectors of 8
+      // before the dependency wait) -> fp32 (scale, bias) pairs.  16-byte vectors of 8
       // groups when the rows allow it, else one value at a time.
       if (p.sb_bulk) {
         const int v8 = ng >> 3;  // vectors per row
@@ -292,7 +308,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
           for (int q2 = 0; q2 < 8; ++q2) {
             const float s1 = bf16_to_f32((ss[q2 >> 1] >> (16 * (q2 & 1))) & 0xFFFFu);
             const float b1 = bf16_to_f32((bb[q2 >> 1] >> (16 * (q2 & 1))) & 0xFFFFu);
-            sbf[(t * SPAN + 8 * v + q2) * 16 + rr] = factor_pair<BITS>(s1, b1);
+            sbf[(t * SPAN + 8 * v + q2) * 16 + rr] = make_float2(s1, b1);
           }
         }
       } else {
@@ -305,7 +321,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
             s1 = bf16_to_f32(ldg_u16(p.m[mi + t].s + off));
             b1 = bf16_to_f32(ldg_u16(p.m[mi + t].b + off));
           }
-          sbf[(t * SPAN + gg) * 16 + rr] = factor_pair<BITS>(s1, b1);
+          sbf[(t * SPAN + gg) * 16 + rr] = make_float2(s1, b1);
         }
       }
       // Activations: a preceding kernel may write them, so they are read only after
@@ -314,7 +330,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         asm volatile("griddepcontrol.wait;" ::: "memory");
       }
-      named_bar_sync(kBarCompute, kMvComputeThreads);  // factor pairs visible
+      named_bar_sync(kBarCompute, kMvComputeThreads);  // (scale, bias) pairs visible
       bool xv[NB];
 #pragma unroll
       for (int h = 0; h < NB; ++h) xv[h] = (8 * h + g4) < p.rows;
@@ -330,7 +346,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
           Xa[h] = make_uint4(0, 0, 0, 0);
           Xb[h] = make_uint4(0, 0, 0, 0);
           if (xv[h] && gcnt > 0)
-            load_x_frag<kOff>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)gw0 * 64 + 16 * c, Xa[h], Xb[h]);
+            load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)gw0 * 64 + 16 * c, Xa[h], Xb[h]);
         }
         if (ok) ok = mbar_wait_bounded(&bars[cc], phase, p.budget_ns, nullptr);
         if (!ok) continue;  // keep every barrier below matched; the status word records why
@@ -347,10 +363,10 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
                 X0[h] = Xa[h];
                 X1[h] = Xb[h];
                 if (NB == 1 && xv[h] && gi + 1 < gcnt)
-                  load_x_frag<kOff>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi + 1) * 64 + 16 * c, Xa[h],
+                  load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi + 1) * 64 + 16 * c, Xa[h],
                                     Xb[h]);
               } else if (xv[h]) {
-                load_x_frag<kOff>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi) * 64 + 16 * c, X0[h], X1[h]);
+                load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi) * 64 + 16 * c, X0[h], X1[h]);
               } else {
                 X0[h] = make_uint4(0, 0, 0, 0);
                 X1[h] = make_uint4(0, 0, 0, 0);

@@ -1,5 +1,5 @@
 // qmv_core.cuh - the arithmetic of the decode kernels (sm_103a): code extraction,
-// activation fragments, scale/bias factor pairs and the per-group tensor-core step
+// activation fragments, scale/bias pairs and the per-group tensor-core step
 // mv_group(), kept apart from the kernel's data movement so that any kernel splitting
 // the same work the same way computes bit-identical results.
 #pragma once
@@ -79,12 +79,13 @@ constexpr int kBarCompute = 1;                   // named barrier of the compute
 constexpr uint64_t kMvDrainNs = 2000000000ull;
 
 // activation fragment of lane (g4, c) for one group: x[row][64g + 16c .. +16) as two
-// 16-byte pieces; 4-bit takes each 8-value block in the order x0 x4 x1 x5 x2 x6 x3 x7
-template <bool kOff>
+// 16-byte pieces; 4-bit takes each 8-value block in the order x0 x4 x1 x5 x2 x6 x3 x7,
+// the order in which q4_split_pair pairs the codes of a word
+template <bool kPair4>
 __device__ __forceinline__ void load_x_frag(const uint16_t *px, uint4 &a, uint4 &b) {
   a = ldg_v4(px);
   b = ldg_v4(px + 8);
-  if constexpr (kOff) {
+  if constexpr (kPair4) {
     a = make_uint4(__byte_perm(a.x, a.z, 0x5410), __byte_perm(a.x, a.z, 0x7632), __byte_perm(a.y, a.w, 0x5410),
                    __byte_perm(a.y, a.w, 0x7632));
     b = make_uint4(__byte_perm(b.x, b.z, 0x5410), __byte_perm(b.x, b.z, 0x7632), __byte_perm(b.y, b.w, 0x5410),
@@ -93,18 +94,19 @@ __device__ __forceinline__ void load_x_frag(const uint16_t *px, uint4 &a, uint4 
 }
 
 // One group of one warp: S of the group for this lane's output columns (MMA with
-// A = 1), then for each of the NMAT matrices the exact codes of rows g4 and g4 + 8
+// A = 1), then for each of the NMAT matrices the exact integer codes of rows g4 and g4 + 8
 // (wrow: the lane's bytes of row 0 of matrix 0 of the group; rows WP bytes apart,
 // matrices 16 rows apart) on the tensor cores with a fresh accumulator, and the
-// group's affine step y = fma(f.x, P, y); y = fma(f.y, S, y) with the factor pairs
-// f of rows g4 and g4 + 8 (fg: matrix 0's pairs of the group, 16 rows; matrices
-// fstride pairs apart).
+// group's affine step y = fma(s, P, y); y = fma(b, S, y) with the (scale, bias) pairs
+// of rows g4 and g4 + 8 (fg: matrix 0's pairs of the group, 16 rows; matrices
+// fstride pairs apart).  With integer codes, P and S are exact up to the fp32
+// rounding of their sums, so a row whose dequantized weights vanish (q = 0, b = 0;
+// or q = c, b = -s*c) gets an error of the order of 2^-24 * s * |P|, not of s * |S|.
 template <int BITS, int NB, int NMAT>
 __device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const float2 *fg, int fstride,
                                          const uint4 (&X0)[NB], const uint4 (&X1)[NB], int g4,
                                          float (&y)[NMAT * NB * 4]) {
   constexpr int LW = Geo<BITS>::kLw;
-  constexpr bool kOff = BITS == 4;
   const uint32_t ones[4] = {kBf16One2, kBf16One2, kBf16One2, kBf16One2};
   float S[NB][4];
 #pragma unroll
@@ -124,11 +126,11 @@ __device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const floa
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t a[4];
-      if constexpr (kOff) {
-        a[0] = q4_off_pair(W0[0], j);
-        a[1] = q4_off_pair(W1[0], j);
-        a[2] = q4_off_pair(W0[1], j);
-        a[3] = q4_off_pair(W1[1], j);
+      if constexpr (BITS == 4) {
+        a[0] = q4_split_pair(W0[0], j);
+        a[1] = q4_split_pair(W1[0], j);
+        a[2] = q4_split_pair(W0[1], j);
+        a[3] = q4_split_pair(W1[1], j);
       } else {
         lane_pairs<BITS>(W0, j, a[0], a[2]);
         lane_pairs<BITS>(W1, j, a[1], a[3]);
@@ -136,7 +138,7 @@ __device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const floa
 #pragma unroll
       for (int h = 0; h < NB; ++h) mma_bf16_16816(P[h], a, u4get(X0[h], j), u4get(X1[h], j), P[h]);
     }
-    // (scale-like, bias-like) factors of rows g4 and g4 + 8
+    // (scale, bias) of rows g4 and g4 + 8
     const float2 f0 = fg[t * fstride + g4];
     const float2 f1 = fg[t * fstride + g4 + 8];
 #pragma unroll
@@ -148,14 +150,6 @@ __device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const floa
       yy[3] = __fmaf_rn(f1.x, P[h][3], yy[3]); yy[3] = __fmaf_rn(f1.y, S[h][1], yy[3]);
     }
   }
-}
-
-// scale/bias of one (row, group) as the fp32 factor pair the group step uses:
-// (16s, b - 16s) for 4-bit offset-form codes, (s, b) otherwise
-template <int BITS>
-__device__ __forceinline__ float2 factor_pair(float s1, float b1) {
-  if constexpr (BITS == 4) return make_float2(s1 * 16.0f, __fsub_rn(b1, s1 * 16.0f));
-  else return make_float2(s1, b1);
 }
 
 }  // namespace qlk
