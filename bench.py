@@ -210,60 +210,129 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------
-def cpu_baseline_sample(bits, target_s=10.0):
-    """The float64 oracle, as it stands, on the host cores: decode of the FFN of one
-    layer (w1, w3, SwiGLU, w2) at R = 1, repeated for about target_s seconds."""
+def sweep_weight_bytes(bits):
+    """Packed codes + scales + biases of every linear of the sweep (one decode pass reads
+    each once)."""
+    return sum(weight_bytes(n, k, bits) for _, n, k in layer_shapes())
+
+
+def _oracle_layer_inputs(bits):
+    from weight_only_bit_mlx_gb300 import synth
+    mk = synth.make_weight
+    ffn = {"w1": mk(D_FF, D_MODEL, bits, config_id=4, tensor_id=1), "w3": mk(D_FF, D_MODEL, bits, config_id=4, tensor_id=3),
+           "w2": mk(D_MODEL, D_FF, bits, config_id=4, tensor_id=2)}
+    attn = {t: mk(n, D_MODEL, bits, config_id=4, tensor_id=10 + i)
+            for i, (t, n) in enumerate((("q", D_MODEL), ("k", D_KV), ("v", D_KV), ("g", D_MODEL), ("o", D_MODEL)))}
+    x = synth.make_x(1, D_MODEL, config_id=4)
+    return ffn, attn, x
+
+
+def _oracle_ffn_layer(ffn, x):
     from oracle import qlinear_oracle as orc
     from weight_only_bit_mlx_gb300 import synth
-    w1 = synth.make_weight(D_FF, D_MODEL, bits, config_id=4, tensor_id=1)
-    w3 = synth.make_weight(D_FF, D_MODEL, bits, config_id=4, tensor_id=3)
-    w2 = synth.make_weight(D_MODEL, D_FF, bits, config_id=4, tensor_id=2)
-    x = synth.make_x(1, D_MODEL, config_id=4)
-    per = (2 * weight_bytes(D_FF, D_MODEL, bits) + D_MODEL * 2 + D_FF * 2
-           + weight_bytes(D_MODEL, D_FF, bits) + D_FF * 2 + D_MODEL * 4)
+    _, _, _, _, h = orc.ffn_swiglu(x, ffn["w1"], ffn["w3"])
+    orc.qlinear_w(synth.f32_to_bf16_bits(h.astype(np.float32)), ffn["w2"])
+
+
+def _oracle_attn_set(attn, x):
+    from oracle import qlinear_oracle as orc
+    for t in ("q", "k", "v", "g", "o"):
+        orc.qlinear_w(x, attn[t])
+
+
+def ffn_layer_bytes(bits, rows=1):
+    return (2 * weight_bytes(D_FF, D_MODEL, bits) + rows * (D_MODEL * 2 + D_FF * 2)
+            + weight_bytes(D_MODEL, D_FF, bits) + rows * (D_FF * 2 + D_MODEL * 4))
+
+
+def attn_set_bytes(bits, rows=1):
+    nq = 2 * D_MODEL + 2 * D_KV
+    return (sum(weight_bytes(n, D_MODEL, bits) for n in (D_MODEL, D_KV, D_KV, D_MODEL)) + rows * (D_MODEL * 2 + nq * 4)
+            + weight_bytes(D_MODEL, D_MODEL, bits) + rows * (D_MODEL * 2 + D_MODEL * 4))
+
+
+def _timed(fn, min_s):
     reps, t0 = 0, time.perf_counter()
     while True:
-        _, _, _, _, h = orc.ffn_swiglu(x, w1, w3)
-        hb = synth.f32_to_bf16_bits(h.astype(np.float32))
-        orc.qlinear_w(hb, w2)
+        fn()
         reps += 1
         el = time.perf_counter() - t0
-        if el >= target_s:
-            break
-    return {"value": per * reps / el / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{reps} x one layer's FFN decode (w1+w3+SwiGLU+w2, 2048->8192->2048, {bits}-bit, R=1) "
-                      f"in {el:.1f} s; numpy float64 (BLAS on all cores, unpack/dequant single-threaded)"}
+        if el >= min_s:
+            return el / reps, reps
+
+
+def cpu_baselines(bits, budget_s=16.0):
+    """The float64 oracle, as it stands, on the host cores, for each workload (configs
+    0-3 on their own shapes; the full-depth sweep scaled from one layer of each kind).
+    About budget_s seconds of CPU work in all."""
+    from oracle import qlinear_oracle as orc
+    from weight_only_bit_mlx_gb300 import synth
+    cores = os.cpu_count()
+    kind = "oracle"
+    note = "numpy float64 (BLAS on all cores, unpack/dequant single-threaded)"
+    out = {}
+    per = budget_s / 5
+    # config 0: one 2048 -> 2048 qmv, R = 1
+    w0 = synth.make_weight(D_MODEL, D_MODEL, bits, config_id=0, tensor_id=0)
+    x0 = synth.make_x(1, D_MODEL, config_id=0)
+    t, reps = _timed(lambda: orc.qlinear_w(x0, w0), per)
+    b0 = weight_bytes(D_MODEL, D_MODEL, bits) + D_MODEL * 2 + D_MODEL * 4
+    out["c0_qmv"] = {"value": b0 / t / 1e9, "unit": "GB/s", "cores": cores, "kind": kind,
+                     "sample": f"{reps} x qmv 2048->2048 {bits}-bit R=1; {note}"}
+    ffn, attn, x = _oracle_layer_inputs(bits)
+    t_f, reps = _timed(lambda: _oracle_ffn_layer(ffn, x), per)
+    out["c1_ffn_decode"] = {"value": ffn_layer_bytes(bits) / t_f / 1e9, "unit": "GB/s", "cores": cores, "kind": kind,
+                            "sample": f"{reps} x one layer's FFN decode (w1+w3+SwiGLU+w2, 2048->8192->2048, "
+                                      f"{bits}-bit, R=1); {note}"}
+    t_a, reps = _timed(lambda: _oracle_attn_set(attn, x), per)
+    out["c2_attn_decode"] = {"value": attn_set_bytes(bits) / t_a / 1e9, "unit": "GB/s", "cores": cores, "kind": kind,
+                             "sample": f"{reps} x one layer's attention projections (q, k, v, gate, o; {bits}-bit, "
+                                       f"R=1); {note}"}
+    pass_s = N_LAYERS * t_f + N_ATTN * t_a
+    out["sweep_decode_r1"] = {"value": decode_bytes(bits, 1) / pass_s / 1e9, "unit": "GB/s", "cores": cores,
+                              "kind": kind,
+                              "sample": f"full-depth decode pass R=1 scaled from one layer of each kind: 16 x "
+                                        f"{t_f * 1e3:.0f} ms (FFN) + 6 x {t_a * 1e3:.0f} ms (attention set); {note}"}
+    # config 3: the 1024-row prompt GEMM, 2048 -> 8192
+    w3 = synth.make_weight(D_FF, D_MODEL, bits, config_id=3, tensor_id=0)
+    X3 = synth.make_x(1024, D_MODEL, config_id=3)
+    t3, reps = _timed(lambda: orc.pgemm(X3, w3), per)
+    f3 = 2.0 * 1024 * D_FF * D_MODEL
+    out["c3_pgemm"] = {"value": f3 / t3 / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": kind,
+                       "sample": f"{reps} x pgemm X[1024, 2048] x W 2048->8192 {bits}-bit ({f3 / t3 / 1e9:.1f} "
+                                 f"GFLOP/s); the M=8192 prefill would take {prefill_flops() / (f3 / t3):.0f} s at "
+                                 f"this rate; {note}"}
+    return out
 
 
 def run_reference(args):
-    """--impl reference: the float64 oracle on the host cores, a bounded sample per step."""
+    """--impl reference: the float64 oracle on the host cores.  Each step is a bounded
+    sample of the workload: one layer's FFN decode and one layer's attention projections
+    at R = 1; the throughput is the full-depth decode pass's bytes over the pass time
+    those imply (16 FFN layers + 6 attention sets), the metric of the GPU arm's `value`."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from oracle import qlinear_oracle as orc
-    from weight_only_bit_mlx_gb300 import synth
     bits = args.bits
-    w1 = synth.make_weight(D_FF, D_MODEL, bits, config_id=4, tensor_id=1)
-    w3 = synth.make_weight(D_FF, D_MODEL, bits, config_id=4, tensor_id=3)
-    w2 = synth.make_weight(D_MODEL, D_FF, bits, config_id=4, tensor_id=2)
-    x = synth.make_x(1, D_MODEL, config_id=4)
-    per = (2 * weight_bytes(D_FF, D_MODEL, bits) + D_MODEL * 2 + D_FF * 2
-           + weight_bytes(D_MODEL, D_FF, bits) + D_FF * 2 + D_MODEL * 4)
-
-    def step():
-        _, _, _, _, h = orc.ffn_swiglu(x, w1, w3)
-        orc.qlinear_w(synth.f32_to_bf16_bits(h.astype(np.float32)), w2)
-
+    ffn, attn, x = _oracle_layer_inputs(bits)
     for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
+        _oracle_ffn_layer(ffn, x)
+        _oracle_attn_set(attn, x)
+    t_f = t_a = 0.0
     for _ in range(args.steps):
-        step()
-    el = time.perf_counter() - t0
-    value = per * args.steps / el / 1e9
-    sample = f"per step: one layer's FFN decode (w1+w3+SwiGLU+w2, {bits}-bit, R=1) by the float64 oracle"
+        t0 = time.perf_counter()
+        _oracle_ffn_layer(ffn, x)
+        t1 = time.perf_counter()
+        _oracle_attn_set(attn, x)
+        t2 = time.perf_counter()
+        t_f += t1 - t0
+        t_a += t2 - t1
+    pass_s = (N_LAYERS * t_f + N_ATTN * t_a) / args.steps
+    value = decode_bytes(bits, 1) / pass_s / 1e9
+    sample = (f"per step: one layer's FFN decode and one layer's attention projections ({bits}-bit, R=1) by the "
+              f"float64 oracle; the full-depth pass time scaled from them (16 x FFN + 6 x attention)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": (t_f + t_a) / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": dict(workload_config(bits, 1), sample=sample),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
@@ -272,7 +341,230 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# ------------------------------------------------------------------------------------
+class Sweep:
+    """The full-depth sweep's weights and buffers at one code width, on one device, with
+    the passes of the workload: decode at R rows, the 8192-row prefill as one M = 8192
+    pgemm per linear, and the same prefill in windows of `win` rows."""
+
+    HD, ROT, RING = 64, 32, 1024  # head_dim, rotary dims, KV ring slots per stream
+
+    def __init__(self, q, bits, gen, dev, with_post=True):
+        import torch
+        self.q, self.bits, self.gen, self.dev = q, bits, gen, dev
+        self.W = {name: self._weight(n, k) for name, n, k in layer_shapes()}
+
+        def rnd(*shape):
+            return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        self.rnd = rnd
+        self.bufs = {}
+        for R in (1, 16):
+            self.bufs[R] = {
+                "x": rnd(R, D_MODEL), "attn": rnd(R, D_MODEL),
+                "q": torch.empty(R, D_MODEL, device=dev), "k": torch.empty(R, D_KV, device=dev),
+                "v": torch.empty(R, D_KV, device=dev), "g": torch.empty(R, D_MODEL, device=dev),
+                "o": torch.empty(R, D_MODEL, device=dev), "h": torch.empty(R, D_FF, dtype=torch.bfloat16, device=dev),
+                "y": torch.empty(R, D_MODEL, device=dev),
+            }
+        # prefill buffers
+        self.X = rnd(PROMPT, D_MODEL)
+        self.Pa = torch.empty(PROMPT, D_FF, device=dev)
+        self.Pc = torch.empty(PROMPT, D_FF, device=dev)
+        self.Ph = torch.empty(PROMPT, D_FF, dtype=torch.bfloat16, device=dev)
+        self.Pout = torch.empty(PROMPT, D_MODEL, device=dev)
+        self.Pq = torch.empty(PROMPT, D_MODEL, device=dev)
+        self.Pkv = torch.empty(PROMPT, D_KV, device=dev)
+        self.Patt = rnd(PROMPT, D_MODEL)
+        self.gemm_events = []  # (start, stop, flops, (m, n, k)) of the timed pgemm calls
+        if with_post:
+            self._post_buffers()
+
+    def _weight(self, n, k):
+        # seeded synthetic weight drawn on the device (same recipe as synth.make_weight:
+        # uniform words, scale ~ U(0.005, 0.02), bias ~ U(-0.1, 0.1), rounded to bf16)
+        import torch
+        gen, dev, bits = self.gen, self.dev, self.bits
+        wq = torch.randint(-2**31, 2**31 - 1, (n, k * bits // 32), generator=gen, dtype=torch.int32, device=dev)
+        s = (torch.rand(n, k // 64, generator=gen, device=dev, dtype=torch.float32) * 0.015 + 0.005)
+        b = (torch.rand(n, k // 64, generator=gen, device=dev, dtype=torch.float32) * 0.2 - 0.1)
+        return self.q.QWeight(wq, s.to(torch.bfloat16), b.to(torch.bfloat16), k, bits)
+
+    def decode_pass(self, R):
+        q, W, b = self.q, self.W, self.bufs[R]
+        n = 0
+        for layer in range(N_LAYERS):
+            p = f"L{layer}."
+            if layer in ATTN_LAYERS:
+                q.qattn_proj_mv(W[p + "q"], W[p + "k"], W[p + "v"], W[p + "g"], b["x"],
+                                outs=(b["q"], b["k"], b["v"], b["g"]))
+                q.qlinear_mv_rows(W[p + "o"], b["attn"], b["o"])
+                n += 2
+            q.qffn_swiglu_mv(W[p + "w1"], W[p + "w3"], b["x"], b["h"])
+            q.qlinear_mv_rows(W[p + "w2"], b["h"], b["y"])
+            n += 2
+        return n
+
+    # ---- the steps after the projections (QK norm + partial RoPE + KV store, post-add /
+    #      next-norm): head_dim 64 (32 q heads, 8 kv heads), rotary on the first 32 dims,
+    #      base 1e6, eps 1e-5, KV rings of 1024 slots per stream
+    def _post_buffers(self):
+        import torch
+        gen, dev, rnd = self.gen, self.dev, self.rnd
+        self.post = {}
+        for R in (1, 16):
+            self.post[R] = {
+                "q_out": torch.empty(R, D_MODEL, dtype=torch.bfloat16, device=dev),
+                "k_ring": torch.zeros(R, self.RING, D_KV, dtype=torch.bfloat16, device=dev),
+                "v_ring": torch.zeros(R, self.RING, D_KV, dtype=torch.bfloat16, device=dev),
+                "pos": torch.randint(0, 1 << 20, (R,), generator=gen, device=dev, dtype=torch.int32),
+                "resid": rnd(R, D_MODEL),
+            }
+        self.qn_w = (torch.rand(self.HD, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+        self.kn_w = (torch.rand(self.HD, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+        self.gammas = [(torch.rand(D_MODEL, generator=gen, device=dev) + 0.5).to(torch.bfloat16) for _ in range(2)]
+
+    def qknorm(self, R):
+        b, pp = self.bufs[R], self.post[R]
+        self.q.qattn_qknorm_rope_kv(b["q"], b["k"], b["v"], D_MODEL // self.HD, D_KV // self.HD, self.HD, self.ROT,
+                                    1e6, 1e-5, self.qn_w, self.kn_w, pp["pos"], pp["k_ring"], pp["v_ring"],
+                                    q_out=pp["q_out"])
+
+    def resid_norm(self, R, y, gi):
+        # the normed output becomes the next linear's activation x
+        self.q.qresid_rmsnorm(y, self.post[R]["resid"], self.gammas[gi], 1e-5, out=self.bufs[R]["x"])
+
+    def decode_layer_pass(self, R, fused=False):
+        """The decode pass with the steps between the linears: per attention layer
+        q/k/v/gate -> QK norm + RoPE + KV store -> o -> post-add / next-norm; per layer
+        w1 + w3 + SwiGLU -> w2 -> post-add / next-norm (attention itself excluded: o
+        reads a fixed attention output)."""
+        q, W, b = self.q, self.W, self.bufs[R]
+        n = 0
+        for layer in range(N_LAYERS):
+            p = f"L{layer}."
+            if layer in ATTN_LAYERS:
+                q.qattn_proj_mv(W[p + "q"], W[p + "k"], W[p + "v"], W[p + "g"], b["x"],
+                                outs=(b["q"], b["k"], b["v"], b["g"]))
+                self.qknorm(R)
+                if fused:  # the post-add / next-norm as the matvec's epilogue
+                    q.qlinear_mv_resid_norm(W[p + "o"], b["attn"], self.post[R]["resid"], self.gammas[0], 1e-5,
+                                            out=b["x"])
+                    n += 3
+                else:
+                    q.qlinear_mv_rows(W[p + "o"], b["attn"], b["o"])
+                    self.resid_norm(R, b["o"], 0)
+                    n += 4
+            q.qffn_swiglu_mv(W[p + "w1"], W[p + "w3"], b["x"], b["h"])
+            if fused:
+                q.qlinear_mv_resid_norm(W[p + "w2"], b["h"], self.post[R]["resid"], self.gammas[1], 1e-5, out=b["x"])
+                n += 2
+            else:
+                q.qlinear_mv_rows(W[p + "w2"], b["h"], b["y"])
+                self.resid_norm(R, b["y"], 1)
+                n += 3
+        return n
+
+    def _pgemm(self, w, Xin, Y, timed):
+        import torch
+        if timed:
+            st = torch.cuda.current_stream()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            self.q.qlinear_pgemm(w, Xin, Y)
+            e1.record(st)
+            self.gemm_events.append((e0, e1, 2 * Xin.shape[0] * w.n * w.k, (int(Xin.shape[0]), w.n, w.k)))
+        else:
+            self.q.qlinear_pgemm(w, Xin, Y)
+
+    def prefill_pass(self, timed=False, lo=0, hi=PROMPT):
+        """Rows lo..hi-1 of the prompt through every linear (one pgemm per linear; SwiGLU
+        between w1/w3 and w2).  Returns the number of launches."""
+        W, n = self.W, 0
+        X, Patt = self.X[lo:hi], self.Patt[lo:hi]
+        Pa, Pc, Ph = self.Pa[lo:hi], self.Pc[lo:hi], self.Ph[lo:hi]
+        Pq, Pkv, Pout = self.Pq[lo:hi], self.Pkv[lo:hi], self.Pout[lo:hi]
+        for layer in range(N_LAYERS):
+            p = f"L{layer}."
+            if layer in ATTN_LAYERS:
+                self._pgemm(W[p + "q"], X, Pq, timed)
+                self._pgemm(W[p + "k"], X, Pkv, timed)
+                self._pgemm(W[p + "v"], X, Pkv, timed)
+                self._pgemm(W[p + "g"], X, Pq, timed)
+                self._pgemm(W[p + "o"], Patt, Pout, timed)
+                n += 10
+            self._pgemm(W[p + "w1"], X, Pa, timed)
+            self._pgemm(W[p + "w3"], X, Pc, timed)
+            self.q.qswiglu(Pa, Pc, Ph)
+            self._pgemm(W[p + "w2"], Ph, Pout, timed)
+            n += 7
+        return n
+
+    def prefill_windows_pass(self, win):
+        """The 8192-row prompt in windows of `win` rows, each window through all the
+        layers before the next (every window streams every weight again)."""
+        n = 0
+        for lo in range(0, PROMPT, win):
+            n += self.prefill_pass(lo=lo, hi=min(PROMPT, lo + win))
+        return n
+
+    def gemm_summary(self, shape=None):
+        """(ms, flops) summed over the timed pgemm calls (of one shape if given)."""
+        ev = [(a, b, f) for a, b, f, sh in self.gemm_events if shape is None or sh == shape]
+        return sum(a.elapsed_time(b) for a, b, _ in ev), sum(f for _, _, f in ev)
+
+
+def graph_of(fn):
+    """Capture fn() once into a CUDA graph; returns (graph, fn's return value)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ret = fn()
+    return g, ret
+
+
+def width_line(q, bits, gen, dev, steps, pk):
+    """Decode R = 1 / R = 16 and the M = 8192 prompt GEMM at another code width (the
+    same shapes), measured the way the main step measures them."""
+    import torch
+    sw = Sweep(q, bits, gen, dev, with_post=False)
+    sw.decode_pass(1)
+    sw.decode_pass(16)
+    sw.prefill_pass()
+    torch.cuda.synchronize()
+    g1, n1 = graph_of(lambda: sw.decode_pass(1))
+    g16, _ = graph_of(lambda: sw.decode_pass(16))
+    for _ in range(3):
+        g1.replay()
+        g16.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ms = {}
+    for key, g in (("r1", g1), ("r16", g16)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(steps):
+            g.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        ms[key] = e0.elapsed_time(e1) / steps
+    for _ in range(max(1, steps // 4)):
+        sw.prefill_pass(timed=True)
+    torch.cuda.synchronize()
+    gemm_ms, gemm_flops = sw.gemm_summary((PROMPT, D_FF, D_MODEL))
+    tf = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    status = q.qlinear_last_error()
+    out = {"bits": bits,
+           "decode_r1": {"GB/s": decode_bytes(bits, 1) / (ms["r1"] * 1e-3) / 1e9, "ms_per_pass": ms["r1"],
+                         "frac_of_hbm": decode_bytes(bits, 1) / (ms["r1"] * 1e-3) / 1e9 / pk["hbm"]},
+           "decode_r16": {"GB/s": decode_bytes(bits, 16) / (ms["r16"] * 1e-3) / 1e9, "ms_per_pass": ms["r16"],
+                          "frac_of_hbm": decode_bytes(bits, 16) / (ms["r16"] * 1e-3) / 1e9 / pk["hbm"]},
+           "pgemm_m8192_n8192_k2048": {"TFLOP/s": tf, "frac_of_sustained": tf / pk["bf16_sus"],
+                                       "frac_of_burst": tf / pk["bf16"]},
+           "status": status}
+    del sw, g1, g16
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -286,185 +578,47 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     from weight_only_bit_mlx_gb300 import qlinear as q
-    from weight_only_bit_mlx_gb300 import synth
 
     bits = args.bits
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
-
-    def dev_weight(n, k, tid):
-        # seeded synthetic weight drawn on the device (same recipe as synth.make_weight:
-        # uniform words, scale ~ U(0.005, 0.02), bias ~ U(-0.1, 0.1), rounded to bf16)
-        wq = torch.randint(-2**31, 2**31 - 1, (n, k * bits // 32), generator=gen, dtype=torch.int32, device=dev)
-        s = (torch.rand(n, k // 64, generator=gen, device=dev, dtype=torch.float32) * 0.015 + 0.005)
-        b = (torch.rand(n, k // 64, generator=gen, device=dev, dtype=torch.float32) * 0.2 - 0.1)
-        return q.QWeight(wq, s.to(torch.bfloat16), b.to(torch.bfloat16), k, bits)
-
-    W = {}
-    for name, n, k in layer_shapes():
-        W[name] = dev_weight(n, k, name)
+    sw = Sweep(q, bits, gen, dev)
     torch.cuda.synchronize()
-
-    def rnd_bf16(*shape):
-        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
-
-    # decode activations and outputs (per R)
-    bufs = {}
-    for R in (1, 16):
-        bufs[R] = {
-            "x": rnd_bf16(R, D_MODEL), "attn": rnd_bf16(R, D_MODEL),
-            "q": torch.empty(R, D_MODEL, device=dev), "k": torch.empty(R, D_KV, device=dev),
-            "v": torch.empty(R, D_KV, device=dev), "g": torch.empty(R, D_MODEL, device=dev),
-            "o": torch.empty(R, D_MODEL, device=dev), "h": torch.empty(R, D_FF, dtype=torch.bfloat16, device=dev),
-            "y": torch.empty(R, D_MODEL, device=dev),
-        }
-    launches = {"decode": 0, "prefill": 0}
-
-    def decode_pass(R, count=False):
-        b = bufs[R]
-        n = 0
-        for layer in range(N_LAYERS):
-            if layer in ATTN_LAYERS:
-                p = f"L{layer}."
-                q.qattn_proj_mv(W[p + "q"], W[p + "k"], W[p + "v"], W[p + "g"], b["x"],
-                                outs=(b["q"], b["k"], b["v"], b["g"]))
-                q.qlinear_mv_rows(W[p + "o"], b["attn"], b["o"])
-                n += 2
-            q.qffn_swiglu_mv(W[f"L{layer}.w1"], W[f"L{layer}.w3"], b["x"], b["h"])
-            q.qlinear_mv_rows(W[f"L{layer}.w2"], b["h"], b["y"])
-            n += 2
-        return n
-
-    # ---- the steps after the projections (QK norm + partial RoPE + KV store, post-add /
-    #      next-norm): head_dim 64 (32 q heads, 8 kv heads), rotary on the first 32 dims,
-    #      base 1e6, eps 1e-5, KV rings of 1024 slots per stream
-    HD, ROT, RING = 64, 32, 1024
-    post = {}
-    for R in (1, 16):
-        post[R] = {
-            "q_out": torch.empty(R, D_MODEL, dtype=torch.bfloat16, device=dev),
-            "k_ring": torch.zeros(R, RING, D_KV, dtype=torch.bfloat16, device=dev),
-            "v_ring": torch.zeros(R, RING, D_KV, dtype=torch.bfloat16, device=dev),
-            "pos": torch.randint(0, 1 << 20, (R,), generator=gen, device=dev, dtype=torch.int32),
-            "resid": rnd_bf16(R, D_MODEL),
-        }
-    qn_w = (torch.rand(HD, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
-    kn_w = (torch.rand(HD, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
-    gammas = [(torch.rand(D_MODEL, generator=gen, device=dev) + 0.5).to(torch.bfloat16) for _ in range(2)]
-
-    def qknorm(R):
-        b, pp = bufs[R], post[R]
-        q.qattn_qknorm_rope_kv(b["q"], b["k"], b["v"], D_MODEL // HD, D_KV // HD, HD, ROT, 1e6, 1e-5, qn_w, kn_w,
-                               pp["pos"], pp["k_ring"], pp["v_ring"], q_out=pp["q_out"])
-
-    def resid_norm(R, y, gi):
-        # the normed output becomes the next linear's activation x
-        q.qresid_rmsnorm(y, post[R]["resid"], gammas[gi], 1e-5, out=bufs[R]["x"])
-
-    def decode_layer_pass(R, fused=False):
-        """The decode pass with the steps between the linears: per attention layer
-        q/k/v/gate -> QK norm + RoPE + KV store -> o -> post-add / next-norm; per layer
-        w1 + w3 + SwiGLU -> w2 -> post-add / next-norm (attention itself excluded: o
-        reads a fixed attention output)."""
-        b = bufs[R]
-        n = 0
-        for layer in range(N_LAYERS):
-            p = f"L{layer}."
-            if layer in ATTN_LAYERS:
-                q.qattn_proj_mv(W[p + "q"], W[p + "k"], W[p + "v"], W[p + "g"], b["x"],
-                                outs=(b["q"], b["k"], b["v"], b["g"]))
-                qknorm(R)
-                if fused:  # the post-add / next-norm as the matvec's epilogue
-                    q.qlinear_mv_resid_norm(W[p + "o"], b["attn"], post[R]["resid"], gammas[0], 1e-5, out=b["x"])
-                    n += 3
-                else:
-                    q.qlinear_mv_rows(W[p + "o"], b["attn"], b["o"])
-                    resid_norm(R, b["o"], 0)
-                    n += 4
-            q.qffn_swiglu_mv(W[p + "w1"], W[p + "w3"], b["x"], b["h"])
-            if fused:
-                q.qlinear_mv_resid_norm(W[p + "w2"], b["h"], post[R]["resid"], gammas[1], 1e-5, out=b["x"])
-                n += 2
-            else:
-                q.qlinear_mv_rows(W[p + "w2"], b["h"], b["y"])
-                resid_norm(R, b["y"], 1)
-                n += 3
-        return n
-
-    # prefill buffers
-    X = rnd_bf16(PROMPT, D_MODEL)
-    Pa = torch.empty(PROMPT, D_FF, device=dev)
-    Pc = torch.empty(PROMPT, D_FF, device=dev)
-    Ph = torch.empty(PROMPT, D_FF, dtype=torch.bfloat16, device=dev)
-    Pout = torch.empty(PROMPT, D_MODEL, device=dev)
-    Pq = torch.empty(PROMPT, D_MODEL, device=dev)
-    Pkv = torch.empty(PROMPT, D_KV, device=dev)
-    Patt = rnd_bf16(PROMPT, D_MODEL)
-    stream = torch.cuda.current_stream()
-
-    def ev():
-        return torch.cuda.Event(enable_timing=True)
-
-    gemm_events = []  # (start, stop, flops) of every pgemm call of the timed steps
-
-    def pgemm(w, Xin, Y, timed):
-        if timed:
-            e0, e1 = ev(), ev()
-            e0.record(stream)
-            q.qlinear_pgemm(w, Xin, Y)
-            e1.record(stream)
-            gemm_events.append((e0, e1, 2 * Xin.shape[0] * w.n * w.k, (int(Xin.shape[0]), w.n, w.k)))
-        else:
-            q.qlinear_pgemm(w, Xin, Y)
-
-    def prefill_pass(timed=False):
-        n = 0
-        for layer in range(N_LAYERS):
-            p = f"L{layer}."
-            if layer in ATTN_LAYERS:
-                pgemm(W[p + "q"], X, Pq, timed)
-                pgemm(W[p + "k"], X, Pkv, timed)
-                pgemm(W[p + "v"], X, Pkv, timed)
-                pgemm(W[p + "g"], X, Pq, timed)
-                pgemm(W[p + "o"], Patt, Pout, timed)
-                n += 10
-            pgemm(W[p + "w1"], X, Pa, timed)
-            pgemm(W[p + "w3"], X, Pc, timed)
-            q.qswiglu(Pa, Pc, Ph)
-            pgemm(W[p + "w2"], Ph, Pout, timed)
-            n += 7
-        return n
+    launches = {}
 
     # warm-up (also sizes the library's scratch before any capture)
     for _ in range(max(1, args.warmup)):
-        decode_pass(1)
-        decode_pass(16)
-        prefill_pass()
+        sw.decode_pass(1)
+        sw.decode_pass(16)
+        sw.prefill_pass()
     torch.cuda.synchronize()
 
     graphs = {}
     for R in (1, 16):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            launches[f"decode{R}"] = decode_pass(R)
-        graphs[R] = g
+        graphs[R], launches[f"decode{R}"] = graph_of(lambda: sw.decode_pass(R))
     for R in (1, 16):
         for fused in (False, True):
             key = f"layer{R}" + ("f" if fused else "")
-            decode_layer_pass(R, fused)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                launches[key] = decode_layer_pass(R, fused)
-            graphs[key] = g
+            sw.decode_layer_pass(R, fused)
+            graphs[key], launches[key] = graph_of(lambda: sw.decode_layer_pass(R, fused))
+    # the prompt in windows of 128 rows (north of 10,000 launches: one graph)
+    WIN = 128
+    graphs["win"], launches["win"] = graph_of(lambda: sw.prefill_windows_pass(WIN))
     for _ in range(args.warmup):
         graphs[1].replay()
         graphs[16].replay()
         for key in ("layer1", "layer16", "layer1f", "layer16f"):
             graphs[key].replay()
+    graphs["win"].replay()
     torch.cuda.synchronize()
     assert q.qlinear_last_error() == q.QL_OK
 
-    # ---------------- timed region
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+
+    # ---------------- timed region: K steps of (decode R=1, decode R=16, prefill as one
+    #                  M=8192 pgemm per linear, prefill in windows of 128 rows)
     marks = []
     with ClockSampler(local) as clk:
         if world > 1:
@@ -474,15 +628,18 @@ def run_ours(args):
         t_start.record(stream)
         n_launch = 0
         for _ in range(args.steps):
-            e = [ev() for _ in range(4)]
+            e = [ev() for _ in range(5)]
             e[0].record(stream)
             graphs[1].replay()
             e[1].record(stream)
             graphs[16].replay()
             e[2].record(stream)
             n_launch += launches["decode1"] + launches["decode16"]
-            n_launch += prefill_pass(timed=True)
+            n_launch += sw.prefill_pass(timed=True)
             e[3].record(stream)
+            graphs["win"].replay()
+            n_launch += launches["win"]
+            e[4].record(stream)
             marks.append(e)
         t_stop = ev()
         t_stop.record(stream)
@@ -496,18 +653,16 @@ def run_ours(args):
     d1_ms = sum(m[0].elapsed_time(m[1]) for m in marks)
     d16_ms = sum(m[1].elapsed_time(m[2]) for m in marks)
     pf_ms = sum(m[2].elapsed_time(m[3]) for m in marks)
-    gemm_ms = sum(a.elapsed_time(b) for a, b, _, _ in gemm_events)
-    gemm_flops = sum(f for _, _, f, _ in gemm_events)
+    win_ms = sum(m[3].elapsed_time(m[4]) for m in marks)
+    gemm_ms, gemm_flops = sw.gemm_summary()
     # the roofline kernel: the M = 8192, N = 8192, K = 2048 launches (w1, w3 of every layer)
-    ffn_ev = [(a, b, f) for a, b, f, shape in gemm_events if shape == (PROMPT, D_FF, D_MODEL)]
-    ffn_ms = sum(a.elapsed_time(b) for a, b, _ in ffn_ev)
-    ffn_flops = sum(f for _, _, f in ffn_ev)
+    ffn_ms, ffn_flops = sw.gemm_summary((PROMPT, D_FF, D_MODEL))
 
     def max_over_ranks(v):
         return max_over_ranks_of(v, world, dev)
 
-    total_ms, d1_ms, d16_ms, pf_ms, gemm_ms, ffn_ms = (max_over_ranks(v) for v in (total_ms, d1_ms, d16_ms, pf_ms,
-                                                                                 gemm_ms, ffn_ms))
+    total_ms, d1_ms, d16_ms, pf_ms, win_ms, gemm_ms, ffn_ms = (
+        max_over_ranks(v) for v in (total_ms, d1_ms, d16_ms, pf_ms, win_ms, gemm_ms, ffn_ms))
 
     # ---------------- the decode pass with the steps between the linears, and those steps alone
     layer_ms = {}
@@ -521,10 +676,7 @@ def run_ours(args):
         layer_ms[key] = max_over_ranks(e0.elapsed_time(e1)) / args.steps
 
     def time_kernel(fn, reps=200):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(20):
-                fn()
+        g, _ = graph_of(lambda: [fn() for _ in range(20)])
         g.replay()
         torch.cuda.synchronize()
         e0, e1 = ev(), ev()
@@ -537,9 +689,9 @@ def run_ours(args):
 
     post_lines = {}
     for R in (1, 16):
-        qk_us = time_kernel(lambda: qknorm(R))
-        rn_us = time_kernel(lambda: resid_norm(R, bufs[R]["y"], 1))
-        qk_bytes = R * ((D_MODEL + 2 * D_KV) * 4 + (D_MODEL + 2 * D_KV) * 2 + 4) + 2 * HD * 2
+        qk_us = time_kernel(lambda: sw.qknorm(R))
+        rn_us = time_kernel(lambda: sw.resid_norm(R, sw.bufs[R]["y"], 1))
+        qk_bytes = R * ((D_MODEL + 2 * D_KV) * 4 + (D_MODEL + 2 * D_KV) * 2 + 4) + 2 * Sweep.HD * 2
         rn_bytes = R * D_MODEL * (4 + 2 + 2 + 2) + D_MODEL * 2
         post_lines[f"r{R}"] = {"qattn_qknorm_rope_kv_us": qk_us, "qattn_qknorm_rope_kv_GB/s": qk_bytes / qk_us / 1e3,
                                "qresid_rmsnorm_us": rn_us, "qresid_rmsnorm_GB/s": rn_bytes / rn_us / 1e3,
@@ -552,15 +704,15 @@ def run_ours(args):
 
     # ---------------- end to end: host buffers in pinned memory, copies inside the timed region
     xh = torch.empty(1, D_MODEL, dtype=torch.bfloat16).pin_memory()
-    xh.copy_(bufs[1]["x"].cpu())
+    xh.copy_(sw.bufs[1]["x"].cpu())
     yh = torch.empty(1, D_MODEL, dtype=torch.float32).pin_memory()
     torch.cuda.synchronize()
     e0, e1 = ev(), ev()
     e0.record(stream)
     for _ in range(args.steps):
-        bufs[1]["x"].copy_(xh, non_blocking=True)
+        sw.bufs[1]["x"].copy_(xh, non_blocking=True)
         graphs[1].replay()
-        yh.copy_(bufs[1]["y"], non_blocking=True)
+        yh.copy_(sw.bufs[1]["y"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1))
@@ -571,10 +723,19 @@ def run_ours(args):
     value = job_throughput(d1_bytes, args.steps, d1_ms, world) / 1e9
     d16_gbs = job_throughput(d16_bytes, args.steps, d16_ms, world) / 1e9
     pf_tflops = job_throughput(prefill_flops(), args.steps, pf_ms, world) / 1e12
+    win_tflops = job_throughput(prefill_flops(), args.steps, win_ms, world) / 1e12
+    win_wbytes = (PROMPT // WIN) * sweep_weight_bytes(bits)
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12  # per GPU, all GEMM launches of the pass
     ffn_tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12      # per GPU, the roofline kernel's launches
     src = source_hash(["pgemm.cu", "common.cuh", "sync.cuh"])
     traffic = NCU_TRAFFIC.get(src)
+    del graphs
+    # the same sweep at the other code widths (decode and the prompt GEMM)
+    widths = {}
+    if rank == 0 or world > 1:
+        for b2 in (4, 6, 8):
+            if b2 != bits:
+                widths[str(b2)] = width_line(q, b2, gen, dev, args.steps, pk)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -587,32 +748,47 @@ def run_ours(args):
                                 "post-add / next-norm after o and w2 (head_dim 64, rotary 32, 1024-slot rings); "
                                 "layer_pass = the decode pass with them between the linears (graph, timed "
                                 "after the main region); layer_pass_fused = the same with the post-add / next-norm "
-                                "as the o / w2 matvec's epilogue (qlinear_mv_resid_norm); per-kernel times are back-to-back launches, "
-                                "bytes = algorithmic reads + writes (latency-bound at these sizes)"),
+                                "as the o / w2 matvec's epilogue (qlinear_mv_resid_norm); per-kernel times are "
+                                "back-to-back launches, bytes = algorithmic reads + writes (latency-bound at these "
+                                "sizes)"),
         "decode_r16": {"GB/s": d16_gbs / world, "frac_of_hbm": d16_gbs / world / pk["hbm"],
                        "ms_per_pass": d16_ms / args.steps, "bytes_per_pass": d16_bytes,
                        "tok_s_modelled": 16.0 / (d16_ms / args.steps * 1e-3)},
         "prefill": {"TFLOP/s": pf_tflops / world, "ms_per_pass": pf_ms / args.steps,
                     "flops_per_pass": prefill_flops(), "includes": "pgemm (row-sum pre-pass + GEMM) and SwiGLU",
                     "tok_s_modelled": PROMPT / (gemm_ms / args.steps * 1e-3)},
+        "prefill_windows": {"window_rows": WIN, "windows": PROMPT // WIN,
+                            "TFLOP/s": win_tflops / world, "ms_per_pass": win_ms / args.steps,
+                            "launches_per_pass": launches["win"],
+                            "us_per_pgemm_call": win_ms / args.steps * 1e3 / ((PROMPT // WIN) * len(layer_shapes())),
+                            "weight_stream_GB/s": win_wbytes / (win_ms / args.steps * 1e-3) / 1e9 / world,
+                            "weight_stream_frac_of_hbm": win_wbytes / (win_ms / args.steps * 1e-3) / 1e9 / world
+                            / pk["hbm"],
+                            "vs_one_m8192_pass": (win_ms / args.steps) / (pf_ms / args.steps),
+                            "what": "the 8192-row prompt in 64 windows of 128 rows, each window through all 16 "
+                                    "layers (78 pgemm + 16 SwiGLU per window, one CUDA graph) before the next: "
+                                    "every window streams every weight again (64 x the sweep's weight bytes)"},
         "tok_s_note": "modelled from the linear layers only: decode R / (decode pass time), prefill "
                       "prompt rows / (sum of the pass's pgemm times); attention, norms and sampling excluded",
         "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm (row-sum pre-pass + tcgen05 GEMM), "
                                                   f"M={PROMPT} N={D_FF} K={D_MODEL} launches (w1, w3)",
                      "achieved": ffn_tflops, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                     "frac": ffn_tflops / pk["bf16_sus"], "traffic": traffic,
+                     "frac": ffn_tflops / pk["bf16_sus"], "frac_of_burst": ffn_tflops / pk["bf16"],
+                     "traffic": traffic,
                      "traffic_unit": "bytes per launch (DRAM read + write, one ncu capture of this shape)",
                      "algorithmic_bytes_per_launch": PROMPT * D_MODEL * 2 + weight_bytes(D_FF, D_MODEL, bits)
                      + PROMPT * D_FF * 4,
                      "all_gemm_launches_TFLOP/s": gemm_tflops,
-                     "peak_source": f"{pk['src']} bf16 sustained"},
+                     "peak_source": f"{pk['src']} bf16 sustained (the launches run back to back inside a "
+                                    "seconds-long step); frac_of_burst against the burst figure"},
         "roofline_decode": {"bound": "hbm", "kernel": "decode pass R=1 (qattn_proj_mv, qlinear_mv_rows, "
                                                       "qffn_swiglu_mv)",
                             "achieved": value / world, "peak": pk["hbm"], "unit": "GB/s",
                             "frac": value / world / pk["hbm"], "traffic": None,
                             "traffic_note": "per-launch DRAM bytes of the FFN decode kernel equal its algorithmic "
-                                            "bytes (ncu: 18.91 MB read for 18.87 MB); no capture of the whole pass",
+                                            "bytes (ncu); no capture of the whole pass",
                             "peak_source": f"{pk['src']} copy bandwidth"},
+        "widths": widths,
         "e2e": {"value": job_throughput(d1_bytes, args.steps, e2e_ms, world) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": D_MODEL * 2, "d2h_bytes_per_step": D_MODEL * 4,
                 "what": "decode pass R=1 with x copied from pinned host memory and the last output copied back"},
@@ -621,7 +797,10 @@ def run_ours(args):
         "status": status,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample(bits)
+        base = cpu_baselines(bits)
+        line["cpu_baseline"] = base["sweep_decode_r1"]
+        line["cpu_baselines"] = base
+        line["roofline"]["cpu_baseline"] = base["c3_pgemm"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -108,3 +108,14 @@ def test_reference_arm_prints_one_contract_line():
 def test_reference_arm_other_ranks_do_no_work():
     assert _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0"],
                       {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
+
+
+def test_layer_bytes_add_up_to_the_pass():
+    # the oracle baseline scales one FFN layer and one attention set to the pass: 16 + 6
+    for bits in (4, 6, 8):
+        for rows in (1, 16):
+            assert 16 * bench.ffn_layer_bytes(bits, rows) + 6 * bench.attn_set_bytes(bits, rows) == \
+                bench.decode_bytes(bits, rows)
+    assert bench.sweep_weight_bytes(4) == 502_530_048
+    # the windowed prefill streams every weight once per window
+    assert bench.sweep_weight_bytes(8) == sum(bench.weight_bytes(n, k, 8) for _, n, k in bench.layer_shapes())

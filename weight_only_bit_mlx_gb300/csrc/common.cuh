@@ -70,30 +70,33 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t w, uint32_t w4, int t) {
   return fma_bf16x2(v, kBf16One2, kBf16Neg128x2);
 }
 
-// 4-bit: codes t and t+4 of word w (t = 0..3) as the exact bf16 pair (q_t, q_{t+4}).
-// Nibble t sits at bits 4t..4t+3 and nibble t+4 at bits 16+4t..16+4t+3, so one shift
-// puts both at the bottom of their 16-bit halves; the mask-or places them in the
-// mantissas of (128, 128) and one bf16x2 fma takes the 128 off.  Pairing t with t+4
+// 4-bit: codes t and t+4 of word w (t = 0..3) as the exact bf16 pair
+// (q_t - z, q_{t+4} - z).  Nibble t sits at bits 4t..4t+3 and nibble t+4 at bits
+// 16+4t..16+4t+3, so one shift puts both at the bottom of their 16-bit halves; the
+// mask-or places them in the mantissas of (128, 128) and one bf16x2 fma adds
+// zc = -(128 + z) in both halves (z = 0: the codes themselves).  Pairing t with t+4
 // (instead of 2t with 2t+1) saves the byte permute; the activations are loaded in the
 // same order.
-__device__ __forceinline__ uint32_t q4_split_pair(uint32_t w, int t) {
+__device__ __forceinline__ uint32_t q4_split_pair(uint32_t w, int t, uint32_t zc = kBf16Neg128x2) {
   const uint32_t v = ((t == 0 ? w : (w >> (4 * t))) & 0x000F000Fu) | kBf16Magic2;
-  return fma_bf16x2(v, kBf16One2, kBf16Neg128x2);
+  return fma_bf16x2(v, kBf16One2, zc);
 }
 
-// 6-bit: a 12-bit field f (two 6-bit codes, lower code in bits 0..5)
-__device__ __forceinline__ uint32_t q6_pair(uint32_t f) {
+// 6-bit: a 12-bit field f (two 6-bit codes, lower code in bits 0..5) as the exact bf16
+// pair (q0 - z, q1 - z), zc = -(128 + z) in both halves
+__device__ __forceinline__ uint32_t q6_pair(uint32_t f, uint32_t zc = kBf16Neg128x2) {
   uint32_t v = (f & 0x3Fu) | ((f << 10) & 0x003F0000u) | kBf16Magic2;
-  return fma_bf16x2(v, kBf16One2, kBf16Neg128x2);
+  return fma_bf16x2(v, kBf16One2, zc);
 }
 
-// 8-bit: natural pair t (bytes 2t and 2t+1) of word w, through float32 2^23 + q
-__device__ __forceinline__ uint32_t q8_pair(uint32_t w, int t) {
+// 8-bit: natural pair t (bytes 2t and 2t+1) of word w as the exact bf16 pair
+// (q0 - z, q1 - z), through float32 2^23 + q; zf = 2^23 + z
+__device__ __forceinline__ uint32_t q8_pair(uint32_t w, int t, float zf = 8388608.0f) {
   const uint32_t m = 0x4B000000u;  // bytes (0, 0, 0, 0x4B)
   const uint32_t s0 = (uint32_t)(2 * t) | (4u << 4) | (4u << 8) | (7u << 12);
   const uint32_t s1 = (uint32_t)(2 * t + 1) | (4u << 4) | (4u << 8) | (7u << 12);
-  float lo = __uint_as_float(__byte_perm(w, m, s0)) - 8388608.0f;
-  float hi = __uint_as_float(__byte_perm(w, m, s1)) - 8388608.0f;
+  float lo = __fsub_rn(__uint_as_float(__byte_perm(w, m, s0)), zf);
+  float hi = __fsub_rn(__uint_as_float(__byte_perm(w, m, s1)), zf);
   return pack_bf16x2(lo, hi);
 }
 

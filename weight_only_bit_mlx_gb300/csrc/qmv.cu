@@ -25,8 +25,10 @@
 //     codes are converted exactly to bf16 and multiplied on the tensor cores with
 //     mma.sync m16n8k16 (rows of W as A, activation rows as B), a fresh fp32
 //     accumulator per group, and the affine step follows in group order:
-//       P_g = sum_{j in g} q_j x_j;   y = fma(s, P_g, y); y = fma(b, S_g, y)
-//     with S_g = sum_{j in g} x_j from the same tensor-core path (A = 1), once per
+//       P'_g = sum_{j in g} (q_j - z) x_j;   y = fma(s, P'_g, y); y = fma(b + s*z, S_g, y)
+//     with the group's zero point z = round(-b/s) in the code range (the codes are
+//     centred as they are converted, at no extra instruction; see group_factors)
+//     and S_g = sum_{j in g} x_j from the same tensor-core path (A = 1), once per
 //     activation row and group;
 //   * warp partials are added in warp order through shared memory, CTA partials in
 //     rank order through distributed shared memory.  No atomics, no scratch memory.
@@ -90,7 +92,8 @@ int mv_span_g(int bits) { return bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6
 //                                      after the last group it holds the warp partials
 //                                      red[kMvWarps][NV][32] (without a cluster they are
 //                                      added in warp order where the outputs are stored)
-//   sbf [NMAT][span][16] float2        per (group, row): (scale, bias) in fp32
+//   sbf [NMAT][span][16] float4        per (group, row): group_factors (scale, centred
+//                                      bias, offset constant)
 //   bars[kNch]                         one per chunk
 //   cpart[cs][NV][32] fp32             with a cluster of cs > 1 CTAs: every rank's CTA
 //                                      partial (only rank 0's copy is read); a region of
@@ -107,7 +110,7 @@ template <int BITS, int NB, int MODE> struct MvLayout {
   static constexpr int kPartBytes = kCsum + NV * 32 * 4;
   static constexpr int kWBytes = NMAT * 16 * wpitch<BITS>() > kPartBytes ? NMAT * 16 * wpitch<BITS>() : kPartBytes;
   static constexpr int kSbf = kWBytes;
-  static constexpr int kBar = kSbf + NMAT * span_g<BITS>() * 16 * 8;
+  static constexpr int kBar = kSbf + NMAT * span_g<BITS>() * 16 * 16;
   static constexpr int kCpart = (kBar + kNch * 8 + 15) / 16 * 16;
   static constexpr int kBytes = kCpart;  // without a cluster
   static int bytes(int cs) { return cs > 1 ? kCpart + cs * NV * 32 * 4 : kBytes; }
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
   constexpr int WP = wpitch<BITS>();
   constexpr bool kPair4 = BITS == 4;  // 4-bit codes paired (t, t+4): activations in that order
   extern __shared__ __align__(128) uint8_t smem[];
-  float2 *sbf = reinterpret_cast<float2 *>(smem + Lay::kSbf);
+  float4 *sbf = reinterpret_cast<float4 *>(smem + Lay::kSbf);
   float *red = reinterpret_cast<float *>(smem + Lay::kRed);
   float *csum = reinterpret_cast<float *>(smem + (p.cs > 1 ? Lay::kCpart : Lay::kCsum));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
       // ---- every warp computes
       const int tid = threadIdx.x;  // 0 .. kMvComputeThreads-1
       // Scales and biases of the span (not written by a preceding kernel, so read
-      // before the dependency wait) -> fp32 (scale, bias) pairs.  16-byte vectors of 8
+      // before the dependency wait) -> per-group factors (group_factors).  16-byte vectors of 8
       // groups when the rows allow it, else one value at a time.
       if (p.sb_bulk) {
         const int v8 = ng >> 3;  // vectors per row
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
           for (int q2 = 0; q2 < 8; ++q2) {
             const float s1 = bf16_to_f32((ss[q2 >> 1] >> (16 * (q2 & 1))) & 0xFFFFu);
             const float b1 = bf16_to_f32((bb[q2 >> 1] >> (16 * (q2 & 1))) & 0xFFFFu);
-            sbf[(t * SPAN + 8 * v + q2) * 16 + rr] = make_float2(s1, b1);
+            sbf[(t * SPAN + 8 * v + q2) * 16 + rr] = group_factors<BITS>(s1, b1);
           }
         }
       } else {
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
             s1 = bf16_to_f32(ldg_u16(p.m[mi + t].s + off));
             b1 = bf16_to_f32(ldg_u16(p.m[mi + t].b + off));
           }
-          sbf[(t * SPAN + gg) * 16 + rr] = make_float2(s1, b1);
+          sbf[(t * SPAN + gg) * 16 + rr] = group_factors<BITS>(s1, b1);
         }
       }
       // Activations: a preceding kernel may write them, so they are read only after
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         asm volatile("griddepcontrol.wait;" ::: "memory");
       }
-      named_bar_sync(kBarCompute, kMvComputeThreads);  // (scale, bias) pairs visible
+      named_bar_sync(kBarCompute, kMvComputeThreads);  // group factors visible
       bool xv[NB];
 #pragma unroll
       for (int h = 0; h < NB; ++h) xv[h] = (8 * h + g4) < p.rows;

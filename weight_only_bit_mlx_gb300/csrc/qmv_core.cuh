@@ -47,19 +47,46 @@ __device__ __forceinline__ void lds_lane_words(const uint8_t *p, uint32_t (&w)[G
   }
 }
 
-// bf16 pairs for MMA j: lo = codes (2j, 2j+1), hi = codes (8+2j, 9+2j)
+// bf16 pairs of centred codes q - z for MMA j: lo = codes (j, j+4) / (2j, 2j+1),
+// hi = codes (8+j, 12+j) / (8+2j, 9+2j) for 4 / 6 and 8 bits; zc is the row's offset
+// constant (group_factors)
 template <int BITS>
-__device__ __forceinline__ void lane_pairs(const uint32_t (&w)[Geo<BITS>::kLw], int j, uint32_t &lo, uint32_t &hi) {
+__device__ __forceinline__ void lane_pairs(const uint32_t (&w)[Geo<BITS>::kLw], int j, uint32_t zc, uint32_t &lo,
+                                           uint32_t &hi) {
   if constexpr (BITS == 4) {
-    lo = q4_pair(w[0], w[0] >> 4, j);
-    hi = q4_pair(w[1], w[1] >> 4, j);
+    lo = q4_split_pair(w[0], j, zc);
+    hi = q4_split_pair(w[1], j, zc);
   } else if constexpr (BITS == 8) {
-    lo = q8_pair(w[j >> 1], j & 1);
-    hi = q8_pair(w[2 + (j >> 1)], j & 1);
+    lo = q8_pair(w[j >> 1], j & 1, __uint_as_float(zc));
+    hi = q8_pair(w[2 + (j >> 1)], j & 1, __uint_as_float(zc));
   } else {
-    lo = q6_pair(bits96_at(w[0], w[1], w[2], 12 * j));
-    hi = q6_pair(bits96_at(w[0], w[1], w[2], 48 + 12 * j));
+    lo = q6_pair(bits96_at(w[0], w[1], w[2], 12 * j), zc);
+    hi = q6_pair(bits96_at(w[0], w[1], w[2], 48 + 12 * j), zc);
   }
+}
+
+// The factors of one (row, group): (scale s, centred bias b + s*z, offset constant, 0)
+// with the group's zero point z = round(-b / s) clamped to the code range.  The group
+// contributes s * sum (q - z) x + (b + s*z) * S, the same linear map as s*P + b*S, but
+// now |w_j| >= |b + s*z| and s*|q_j - z| <= 2|w_j| for every j of the group (the zero
+// point is the code nearest to where w changes sign, or an end of the range if w has
+// one sign), so no term of the factored sum exceeds twice sum |w x| and the fp32
+// rounding of every step is relative to |w x|.  Where the dequantized weights vanish
+// (q = c, b = -s*c) z = c and both terms are exactly zero.  The offset constant is
+// -(128 + z) as a bf16 pair (4 and 6 bits, exact for z <= 63) or 2^23 + z as fp32
+// (8 bits); a zero scale gives z = 0.
+template <int BITS>
+__device__ __forceinline__ float4 group_factors(float s, float b) {
+  constexpr float kMaxQ = (float)((1 << BITS) - 1);
+  const float z = fminf(fmaxf(rintf(__fdiv_rn(-b, s)), 0.0f), kMaxQ);  // a NaN quotient becomes 0
+  uint32_t zc;
+  if constexpr (BITS == 8) {
+    zc = __float_as_uint(__fadd_rn(8388608.0f, z));
+  } else {
+    const uint32_t h = f32_to_bf16_rn(-(128.0f + z));
+    zc = h | (h << 16);
+  }
+  return make_float4(s, __fmaf_rn(s, z, b), __uint_as_float(zc), 0.0f);
 }
 
 __device__ __forceinline__ uint32_t u4get(const uint4 &v, int j) {
@@ -94,16 +121,14 @@ __device__ __forceinline__ void load_x_frag(const uint16_t *px, uint4 &a, uint4 
 }
 
 // One group of one warp: S of the group for this lane's output columns (MMA with
-// A = 1), then for each of the NMAT matrices the exact integer codes of rows g4 and g4 + 8
+// A = 1), then for each of the NMAT matrices the exact centred codes q - z of rows g4 and g4 + 8
 // (wrow: the lane's bytes of row 0 of matrix 0 of the group; rows WP bytes apart,
 // matrices 16 rows apart) on the tensor cores with a fresh accumulator, and the
-// group's affine step y = fma(s, P, y); y = fma(b, S, y) with the (scale, bias) pairs
-// of rows g4 and g4 + 8 (fg: matrix 0's pairs of the group, 16 rows; matrices
-// fstride pairs apart).  With integer codes, P and S are exact up to the fp32
-// rounding of their sums, so a row whose dequantized weights vanish (q = 0, b = 0;
-// or q = c, b = -s*c) gets an error of the order of 2^-24 * s * |P|, not of s * |S|.
+// group's affine step y = fma(s, P', y); y = fma(b', S, y) with the factors of rows g4
+// and g4 + 8 (group_factors; fg: matrix 0's factors of the group, 16 rows; matrices
+// fstride apart).
 template <int BITS, int NB, int NMAT>
-__device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const float2 *fg, int fstride,
+__device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const float4 *fg, int fstride,
                                          const uint4 (&X0)[NB], const uint4 (&X1)[NB], int g4,
                                          float (&y)[NMAT * NB * 4]) {
   constexpr int LW = Geo<BITS>::kLw;
@@ -120,27 +145,22 @@ __device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const floa
     uint32_t W0[LW], W1[LW];
     lds_lane_words<BITS>(wrow + (t * 16 + g4) * WP, W0);
     lds_lane_words<BITS>(wrow + (t * 16 + g4 + 8) * WP, W1);
+    // offset constants of rows g4 and g4 + 8 now, their (scale, centred bias) after the MMAs
+    const uint32_t zc0 = __float_as_uint(fg[t * fstride + g4].z);
+    const uint32_t zc1 = __float_as_uint(fg[t * fstride + g4 + 8].z);
     float P[NB][4];
 #pragma unroll
     for (int h = 0; h < NB; ++h) P[h][0] = P[h][1] = P[h][2] = P[h][3] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t a[4];
-      if constexpr (BITS == 4) {
-        a[0] = q4_split_pair(W0[0], j);
-        a[1] = q4_split_pair(W1[0], j);
-        a[2] = q4_split_pair(W0[1], j);
-        a[3] = q4_split_pair(W1[1], j);
-      } else {
-        lane_pairs<BITS>(W0, j, a[0], a[2]);
-        lane_pairs<BITS>(W1, j, a[1], a[3]);
-      }
+      lane_pairs<BITS>(W0, j, zc0, a[0], a[2]);
+      lane_pairs<BITS>(W1, j, zc1, a[1], a[3]);
 #pragma unroll
       for (int h = 0; h < NB; ++h) mma_bf16_16816(P[h], a, u4get(X0[h], j), u4get(X1[h], j), P[h]);
     }
-    // (scale, bias) of rows g4 and g4 + 8
-    const float2 f0 = fg[t * fstride + g4];
-    const float2 f1 = fg[t * fstride + g4 + 8];
+    const float2 f0 = *reinterpret_cast<const float2 *>(&fg[t * fstride + g4]);
+    const float2 f1 = *reinterpret_cast<const float2 *>(&fg[t * fstride + g4 + 8]);
 #pragma unroll
     for (int h = 0; h < NB; ++h) {
       float *yy = &y[(t * NB + h) * 4];
