@@ -13,20 +13,17 @@
 namespace qlk {
 
 template <int BITS> struct Geo;
-// chunks per span, one mbarrier each (2, computing the first half while the second
-// lands, measured slower on the decode pass)
-constexpr int kNch = 1;
-// spans of 32 groups (4-bit) or 16 groups (6/8-bit), split over the compute warps and chunks
+// A span is the k-range of one ring slot: 32 groups (4-bit) or 16 groups (6/8-bit),
+// split over the kMvWarps warps (4 or 2 consecutive groups each).
 template <> struct Geo<4> {
-  static constexpr int kLw = 2;                          // words per lane per row per group
-  static constexpr int kGpw = 32 / (kMvWarps * kNch);    // groups per compute warp per chunk
+  static constexpr int kLw = 2;                      // words per lane per row per group
+  static constexpr int kGpw = 32 / kMvWarps;         // groups per warp per span
 };
-template <> struct Geo<6> { static constexpr int kLw = 3; static constexpr int kGpw = 16 / (kMvWarps * kNch); };
-template <> struct Geo<8> { static constexpr int kLw = 4; static constexpr int kGpw = 16 / (kMvWarps * kNch); };
-static_assert(Geo<6>::kGpw >= 1, "every compute warp owns at least one group per chunk");
+template <> struct Geo<6> { static constexpr int kLw = 3; static constexpr int kGpw = 16 / kMvWarps; };
+template <> struct Geo<8> { static constexpr int kLw = 4; static constexpr int kGpw = 16 / kMvWarps; };
+static_assert(Geo<6>::kGpw >= 1, "every warp owns at least one group per span");
 template <int BITS> __host__ __device__ constexpr int gbytes() { return 8 * BITS; }                  // bytes per row per group
-template <int BITS> __host__ __device__ constexpr int gpc() { return kMvWarps * Geo<BITS>::kGpw; }  // groups per chunk
-template <int BITS> __host__ __device__ constexpr int span_g() { return kNch * gpc<BITS>(); }        // groups per span
+template <int BITS> __host__ __device__ constexpr int span_g() { return kMvWarps * Geo<BITS>::kGpw; }  // groups per span
 template <int BITS> __host__ __device__ constexpr int wpitch() { return span_g<BITS>() * gbytes<BITS>() + 32; }  // padded row pitch
 
 // Lane (g4, c) of a warp holds, for each of its two rows (g4, g4 + 8), the 16 codes
@@ -100,9 +97,8 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                : "memory");
 }
 
-constexpr int kMvThreads = kMvWarps * 32;  // compute warps (warp 0 also starts the bulk copies)
-constexpr int kMvComputeThreads = kMvWarps * 32;
-constexpr int kBarCompute = 1;                   // named barrier of the compute warps
+constexpr int kMvThreads = kMvWarps * 32;  // every warp computes; warp 0 also issues the bulk copies
+constexpr int kBarSlot = 1;                      // named barrier: a ring slot is consumed
 constexpr uint64_t kMvDrainNs = 2000000000ull;
 
 // activation fragment of lane (g4, c) for one group: x[row][64g + 16c .. +16) as two
