@@ -84,8 +84,7 @@ int mv_resid_counter_reset() {
 //   ring[NS] slots, each: weights [NMAT][16 rows][wpitch] (one bulk copy per row),
 //            scales [NMAT][16][span] bf16, biases [NMAT][16][span] bf16
 //   red[2][kMvWarps][NV][32] fp32     warp partials of a tile (two tiles in flight)
-//   fac[kMvWarps][2][32] float4       each warp's group factors (lane l: matrix l / 16,
-//                                     row l % 16), two groups in flight
+//   fac[kMvWarps][gpw][NMAT][16] float4  each warp's group factors of the current slot
 //   full[NS]                          mbarrier per ring slot (bulk-copy bytes)
 template <int BITS, int NB, int MODE> struct MvLayout {
   static constexpr int NMAT = (MODE == kMvFfn) ? 2 : 1;
@@ -95,10 +94,10 @@ template <int BITS, int NB, int MODE> struct MvLayout {
   static constexpr int kSBRow = SPAN * 2;   // bytes of one row's scales (or biases) in a slot
   static constexpr int kSlot = kWBytes + 2 * NMAT * 16 * kSBRow;
   static constexpr int kRed = kMvWarps * NV * 32 * 4;
-  static constexpr int kFac = kMvWarps * 2 * 32 * 16;
-  // two weights (the fused FFN) may take 140 KB, one weight 80 KB: any two consecutive
+  static constexpr int kFac = kMvWarps * Geo<BITS>::kGpw * NMAT * 16 * 16;
+  // two weights (the fused FFN) may take 148 KB, one weight 76 KB: any two consecutive
   // launches of a decode layer fit one SM together
-  static constexpr int kBudget = (NMAT == 2 ? 140 : 80) * 1024;
+  static constexpr int kBudget = (NMAT == 2 ? 148 : 76) * 1024;
   static constexpr int NS = (kBudget - 2 * kRed - kFac - 256) / kSlot;
   static constexpr int kOffRed = NS * kSlot;
   static constexpr int kOffFac = kOffRed + 2 * kRed;
@@ -277,6 +276,14 @@ __global__ void __launch_bounds__(kMvThreads, 2) qmv_kernel(const __grid_constan
   for (int i = 0; i < NV; ++i) y[i] = 0.0f;
   bool ok = true;
 
+  // With one span per tile (k <= 2048 at 4 bits, k <= 1024 otherwise) every slot of the
+  // CTA covers the same groups: the activation fragments and sums of the warp's groups
+  // are loaded and formed once, at the first slot, and kept in registers.
+  const bool hoist = NB == 1 && nspan == 1;  // (two row blocks: kept per group, registers)
+  uint4 Xh0[GPW][NB], Xh1[GPW][NB];
+  float Sh[GPW][NB][4];
+  constexpr int NQ = GPW * NMAT * 16;  // group factors per warp per slot
+  float4 *fw = fac + warp * NQ;
   for (int j = 0; j < J; ++j) {
     const int ti = j / nspan, sp = j - ti * nspan, buf = j % NS;
     int mi, lt;
@@ -294,51 +301,67 @@ __global__ void __launch_bounds__(kMvThreads, 2) qmv_kernel(const __grid_constan
     const int gw0 = warp * GPW;  // this warp's first group of the span
     if (ok && gw0 < ng) {
       const int gcnt = min(GPW, ng - gw0);
-      uint4 Xa[NB], Xb[NB];
-#pragma unroll
-      for (int h = 0; h < NB; ++h) {
-        Xa[h] = make_uint4(0, 0, 0, 0);
-        Xb[h] = make_uint4(0, 0, 0, 0);
-        if (xv[h])
-          load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(g0 + gw0) * 64 + 16 * c, Xa[h], Xb[h]);
+      // the factors of the warp's groups of this slot (lane q: group q / (16 NMAT),
+      // matrix (q / 16) % NMAT, row q % 16)
+      for (int q = lane; q < NQ; q += 32) {
+        const int gi = q / (NMAT * 16), mt = (q >> 4) % NMAT, r = q & 15;
+        const int gl = gw0 + gi, row = lt * 16 + r;
+        float s1 = 0.0f, b1 = 0.0f;
+        if (gi < gcnt && row < p.m[mi + mt].n) {
+          if (p.sb_bulk) {
+            const uint16_t *sb = reinterpret_cast<const uint16_t *>(slot + Lay::kWBytes) + (mt * 16 + r) * SPAN + gl;
+            s1 = bf16_to_f32(sb[0]);
+            b1 = bf16_to_f32(sb[NMAT * 16 * SPAN]);
+          } else {
+            const size_t off = (size_t)row * G + g0 + gl;
+            s1 = bf16_to_f32(ldg_u16(p.m[mi + mt].s + off));
+            b1 = bf16_to_f32(ldg_u16(p.m[mi + mt].b + off));
+          }
+        }
+        fw[q] = group_factors<BITS>(s1, b1);
       }
+      __syncwarp();
+      if (hoist) {
+        if (j == 0) {
 #pragma unroll
-      for (int gi = 0; gi < GPW; ++gi) {
-        if (gi < gcnt) {
-          const int gl = gw0 + gi;  // group within the span
-          // the factors of this group for the warp's rows: lane l computes matrix l / 16, row l % 16
-          float4 *fw = fac + (warp * 2 + (gi & 1)) * 32;
-          {
-            const int mt = lane >> 4, r = lane & 15;
-            if (mt < NMAT) {
-              const MvMat &M = p.m[mi + mt];
-              const int row = lt * 16 + r;
-              float s1 = 0.0f, b1 = 0.0f;
-              if (row < M.n) {
-                if (p.sb_bulk) {
-                  const uint16_t *sb = reinterpret_cast<const uint16_t *>(slot + Lay::kWBytes) + (mt * 16 + r) * SPAN + gl;
-                  s1 = bf16_to_f32(sb[0]);
-                  b1 = bf16_to_f32(sb[NMAT * 16 * SPAN]);
-                } else {
-                  const size_t off = (size_t)row * G + g0 + gl;
-                  s1 = bf16_to_f32(ldg_u16(M.s + off));
-                  b1 = bf16_to_f32(ldg_u16(M.b + off));
-                }
-              }
-              fw[lane] = group_factors<BITS>(s1, b1);
+          for (int gi = 0; gi < GPW; ++gi) {
+#pragma unroll
+            for (int h = 0; h < NB; ++h) {
+              Xh0[gi][h] = make_uint4(0, 0, 0, 0);
+              Xh1[gi][h] = make_uint4(0, 0, 0, 0);
+              if (xv[h] && gi < gcnt)
+                load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(g0 + gw0 + gi) * 64 + 16 * c,
+                                    Xh0[gi][h], Xh1[gi][h]);
             }
           }
-          __syncwarp();
-          uint4 X0[NB], X1[NB];
 #pragma unroll
-          for (int h = 0; h < NB; ++h) {
-            X0[h] = Xa[h];
-            X1[h] = Xb[h];
-            if (xv[h] && gi + 1 < gcnt)  // the next group's activations are in flight during this group
-              load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(g0 + gl + 1) * 64 + 16 * c, Xa[h],
-                                  Xb[h]);
+          for (int gi = 0; gi < GPW; ++gi)
+            if (gi < gcnt) mv_sums<NB>(Xh0[gi], Xh1[gi], Sh[gi]);
+        }
+#pragma unroll
+        for (int gi = 0; gi < GPW; ++gi) {
+          if (gi < gcnt)
+            mv_group_s<BITS, NB, NMAT>(slot + (gw0 + gi) * GB + c * 4 * LW, WP, fw + gi * NMAT * 16, 16, Xh0[gi],
+                                       Xh1[gi], Sh[gi], g4, y);
+        }
+      } else {
+#pragma unroll
+        for (int gi = 0; gi < GPW; ++gi) {
+          if (gi < gcnt) {
+            uint4 X0[NB], X1[NB];
+            float S[NB][4];
+#pragma unroll
+            for (int h = 0; h < NB; ++h) {
+              X0[h] = make_uint4(0, 0, 0, 0);
+              X1[h] = make_uint4(0, 0, 0, 0);
+              if (xv[h])
+                load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(g0 + gw0 + gi) * 64 + 16 * c,
+                                    X0[h], X1[h]);
+            }
+            mv_sums<NB>(X0, X1, S);
+            mv_group_s<BITS, NB, NMAT>(slot + (gw0 + gi) * GB + c * 4 * LW, WP, fw + gi * NMAT * 16, 16, X0, X1, S,
+                                       g4, y);
           }
-          mv_group<BITS, NB, NMAT>(slot + gl * GB + c * 4 * LW, WP, fw, 16, X0, X1, g4, y);
         }
       }
     }

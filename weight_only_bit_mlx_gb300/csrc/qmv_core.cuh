@@ -116,26 +116,30 @@ __device__ __forceinline__ void load_x_frag(const uint16_t *px, uint4 &a, uint4 
   }
 }
 
-// One group of one warp: S of the group for this lane's output columns (MMA with
-// A = 1), then for each of the NMAT matrices the exact centred codes q - z of rows g4 and g4 + 8
-// (wrow: the lane's bytes of row 0 of matrix 0 of the group; rows WP bytes apart,
-// matrices 16 rows apart) on the tensor cores with a fresh accumulator, and the
-// group's affine step y = fma(s, P', y); y = fma(b', S, y) with the factors of rows g4
-// and g4 + 8 (group_factors; fg: matrix 0's factors of the group, 16 rows; matrices
-// fstride apart).
-template <int BITS, int NB, int NMAT>
-__device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const float4 *fg, int fstride,
-                                         const uint4 (&X0)[NB], const uint4 (&X1)[NB], int g4,
-                                         float (&y)[NMAT * NB * 4]) {
-  constexpr int LW = Geo<BITS>::kLw;
+// The activation sums S_g of one group for this lane's output columns: the tensor-core
+// path with A = 1, four MMAs in k order (a function of the activations alone).
+template <int NB>
+__device__ __forceinline__ void mv_sums(const uint4 (&X0)[NB], const uint4 (&X1)[NB], float (&S)[NB][4]) {
   const uint32_t ones[4] = {kBf16One2, kBf16One2, kBf16One2, kBf16One2};
-  float S[NB][4];
 #pragma unroll
   for (int h = 0; h < NB; ++h) {
     S[h][0] = S[h][1] = S[h][2] = S[h][3] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) mma_bf16_16816(S[h], ones, u4get(X0[h], j), u4get(X1[h], j), S[h]);
   }
+}
+
+// One group of one warp, given its activation sums S (mv_sums): for each of the NMAT
+// matrices the exact centred codes q - z of rows g4 and g4 + 8 (wrow: the lane's bytes
+// of row 0 of matrix 0 of the group; rows WP bytes apart, matrices 16 rows apart) on the
+// tensor cores with a fresh accumulator, then the group's affine step
+// y = fma(s, P', y); y = fma(b', S, y) with the factors of rows g4 and g4 + 8
+// (group_factors; fg: matrix 0's factors of the group, 16 rows; matrices fstride apart).
+template <int BITS, int NB, int NMAT>
+__device__ __forceinline__ void mv_group_s(const uint8_t *wrow, int WP, const float4 *fg, int fstride,
+                                           const uint4 (&X0)[NB], const uint4 (&X1)[NB], const float (&S)[NB][4],
+                                           int g4, float (&y)[NMAT * NB * 4]) {
+  constexpr int LW = Geo<BITS>::kLw;
 #pragma unroll
   for (int t = 0; t < NMAT; ++t) {
     uint32_t W0[LW], W1[LW];
