@@ -1,38 +1,41 @@
 // qmv.cu - decode matvecs over MLX affine 4/6/8-bit group-64 weights (sm_103a).
 //
 // One kernel template serves qlinear_mv / qlinear_mv_rows (one weight), the fused
-// w1 + w3 + SwiGLU step (two weights, bf16 output), the fused q/k/v/gate step (four
-// weights, one launch) and the matvec with the post-add / next-norm epilogue.
-// TensorFold PR #1696 (later revision), "What it adds": N-row matvecs summing each
-// row as the one-row kernels do; decode fuses w1 + w3 + SwiGLU and the four attention
-// matvecs.  PR #1514, "What changes": post-add/next-norm fusion.
+// w1 + w3 + SwiGLU step (two weights, bf16 output) and the fused q/k/v/gate step
+// (four weights, one launch).  TensorFold PR #1696 (later revision), "What it adds":
+// N-row matvecs summing each row as the one-row kernels do; decode fuses w1 + w3 +
+// SwiGLU and the four attention matvecs.
 //
-// Data movement: one CTA per SM.  CTA c owns a contiguous range of 16-row tiles (both
-// w1 and w3 rows of a tile in the fused FFN); a tile's k-range is cut into spans of 32
-// groups (4-bit) or 16 groups (6/8-bit), and every (tile, span) is one slot of a ring
-// in shared memory: the weight rows, and with them the span's scales and biases, each
-// arrive by one bulk copy (cp.async.bulk) per row straight from HBM.  Warp 0 fills the
-// whole ring at kernel start, before the programmatic-dependency wait, and refills a
-// slot as soon as every warp is done with it, so the weight stream of a launch runs
-// while the previous launch still computes.  The CTA is small enough (at most 140 KB
-// of shared memory for two weights, 80 KB for one; 256 threads) that the next launch's
-// CTA fits beside it on the same SM and starts streaming its own weights in turn.
-// Activations - the only input a preceding kernel writes - are read after
-// griddepcontrol.wait, straight into the registers of the MMA fragments.
-//
-// Arithmetic (qmv_core.cuh): warp w owns groups w*gpw .. w*gpw + gpw - 1 of every span
-// (gpw = 4 for 4-bit, 2 otherwise).  Per group the codes are converted exactly to bf16,
-// centred on the group's zero point z, and multiplied on the tensor cores with
-// mma.sync m16n8k16 (rows of W as A, activation rows as B), a fresh fp32 accumulator
-// per group; the affine step follows in group order:
-//   P'_g = sum_{j in g} (q_j - z) x_j;   y = fma(s, P'_g, y); y = fma(b + s*z, S_g, y)
-// with S_g = sum_{j in g} x_j from the same tensor-core path (A = 1).  A warp's partial
-// runs over its groups of every span of the tile in k order; the warps' partials are
-// then added in warp order.  This order is a function of k and bits only - never of
-// the number of activation rows, of n, of the tile-to-CTA assignment or of fused vs
-// unfused - and the tensor core computes every output column (activation row) from
-// that column's data alone, so a row's result does not depend on how many rows share
-// the call.
+// Work decomposition (a function of k and bits only, never of the number of rows R,
+// of n or of the fused/unfused choice):
+//   * a CTA owns a 16-row tile of W (both w1 and w3 in the fused FFN) and a k-span;
+//     CTAs of a cluster split k into spans;
+//   * the span is cut into kNch chunks of kGpc groups; warp 0 first starts, chunk by
+//     chunk, one bulk copy (cp.async.bulk) per weight row of the chunk, straight
+//     from HBM into shared memory, each chunk completing its own mbarrier, so the
+//     warps start on chunk 0 while later chunks are still streaming in and the
+//     weight stream leaves the SM as large requests issued at kernel start (no warp
+//     is kept only for copies, so the compute warps get 64 registers instead of 56);
+//   * scales and biases go in by bulk copy with chunk 0 (one copy for the whole tile
+//     when a CTA spans the full k), activations (the only input a preceding kernel
+//     may write) are loaded by the compute warps after griddepcontrol.wait, so with
+//     programmatic dependent launch the weight stream of this kernel overlaps the
+//     tail of the previous one;
+//   * compute warp w owns kGpw consecutive groups of every chunk.  Per group the
+//     codes are converted exactly to bf16 and multiplied on the tensor cores with
+//     mma.sync m16n8k16 (rows of W as A, activation rows as B), a fresh fp32
+//     accumulator per group, and the affine step follows in group order:
+//       P'_g = sum_{j in g} (q_j - z) x_j;   y = fma(s, P'_g, y); y = fma(b + s*z, S_g, y)
+//     with the group's zero point z = round(-b/s) in the code range (the codes are
+//     centred as they are converted, at no extra instruction; see group_factors)
+//     and S_g = sum_{j in g} x_j from the same tensor-core path (A = 1), once per
+//     activation row and group;
+//   * warp partials are added in warp order through shared memory, CTA partials in
+//     rank order through distributed shared memory.  No atomics, no scratch memory.
+// The tensor core computes every output column (activation row) from that column's
+// data alone, so a row's result does not depend on how many rows share the call.
+#include <cooperative_groups.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -41,9 +44,11 @@
 #include "qmv_core.cuh"
 #include "sync.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace qlk {
 
-// per-tile sums of squares and the finished-CTA counter of kMvResid launches (one per
+// per-tile sums of squares and the finished-tile counter of kMvResid launches (one per
 // device that loads the library; the counter is back at zero after every launch)
 __device__ float g_resid_part[kMvResidMaxTiles * 16];
 __device__ unsigned g_resid_counter = 0;
@@ -80,50 +85,67 @@ int mv_resid_counter_reset() {
   return cudaMemcpyToSymbol(g_resid_counter, &zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
 }
 
-// Shared-memory layout of one CTA (dynamic):
-//   ring[NS] slots, each: weights [NMAT][16 rows][wpitch] (one bulk copy per row),
-//            scales [NMAT][16][span] bf16, biases [NMAT][16][span] bf16
-//   red[2][kMvWarps][NV][32] fp32     warp partials of a tile (two tiles in flight)
-//   fac[kMvWarps][gpw][NMAT][16] float4  each warp's group factors of the current slot
-//   full[NS]                          mbarrier per ring slot (bulk-copy bytes)
+int mv_span_g(int bits) { return bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6>() : span_g<8>()); }
+
+// Shared-memory layout of one CTA (dynamic, 128-byte aligned):
+//   wsm [NMAT][16][wpitch]             weight rows of the span (one bulk copy per row and chunk);
+//                                      after the last group it holds the warp partials
+//                                      red[kMvWarps][NV][32] (without a cluster they are
+//                                      added in warp order where the outputs are stored)
+//   sbf [NMAT][span][16] float4        per (group, row): group_factors (scale, centred
+//                                      bias, offset constant)
+//   bars[kNch]                         one per chunk
+//   cpart[cs][NV][32] fp32             with a cluster of cs > 1 CTAs: every rank's CTA
+//                                      partial (only rank 0's copy is read); a region of
+//                                      its own, since other ranks write it while this
+//                                      CTA may still be reading its weights
+// Activations never pass through shared memory: each lane loads the 16-byte pieces
+// its MMA fragments take straight from global memory (L1/L2).
 template <int BITS, int NB, int MODE> struct MvLayout {
   static constexpr int NMAT = (MODE == kMvFfn) ? 2 : 1;
-  static constexpr int NV = NMAT * NB * 4;  // accumulators per lane
-  static constexpr int SPAN = span_g<BITS>();
-  static constexpr int kWBytes = NMAT * 16 * wpitch<BITS>();
-  static constexpr int kSBRow = SPAN * 2;   // bytes of one row's scales (or biases) in a slot
-  static constexpr int kSlot = kWBytes + 2 * NMAT * 16 * kSBRow;
-  static constexpr int kRed = kMvWarps * NV * 32 * 4;
-  static constexpr int kFac = kMvWarps * Geo<BITS>::kGpw * NMAT * 16 * 16;
-  // two weights (the fused FFN) may take 148 KB, one weight 76 KB: any two consecutive
-  // launches of a decode layer fit one SM together
-  static constexpr int kBudget = (NMAT == 2 ? 148 : 76) * 1024;
-  static constexpr int NS = (kBudget - 2 * kRed - kFac - 256) / kSlot;
-  static constexpr int kOffRed = NS * kSlot;
-  static constexpr int kOffFac = kOffRed + 2 * kRed;
-  static constexpr int kOffBar = kOffFac + kFac;
-  static constexpr int kBytes = kOffBar + NS * 8;
-  static_assert(NS >= 2, "at least two ring slots");
-  static_assert(kBytes <= kBudget, "shared-memory budget");
+  static constexpr int NV = NMAT * NB * 4;
+  static constexpr int kW = 0;
+  static constexpr int kRed = 0;                                // aliases wsm
+  static constexpr int kCsum = kRed + kMvWarps * NV * 32 * 4;   // aliases wsm
+  static constexpr int kPartBytes = kCsum + NV * 32 * 4;
+  static constexpr int kWBytes = NMAT * 16 * wpitch<BITS>() > kPartBytes ? NMAT * 16 * wpitch<BITS>() : kPartBytes;
+  static constexpr int kSbf = kWBytes;
+  static constexpr int kBar = kSbf + NMAT * span_g<BITS>() * 16 * 16;
+  static constexpr int kCpart = (kBar + kNch * 8 + 15) / 16 * 16;
+  static constexpr int kBytes = kCpart;  // without a cluster
+  static int bytes(int cs) { return cs > 1 ? kCpart + cs * NV * 32 * 4 : kBytes; }
+  static int max_bytes() { return bytes(kMvMaxCluster); }
 };
 
-// The post-add / next-norm epilogue after the last CTA has stored its tiles' residual
-// rows and their sums of squares (TensorFold PR #1514, "What changes": post-add/next-
-// norm fusion): the CTA that finishes last (a device counter) adds the per-tile slots in
-// tile order and normalises every channel of every row from the stored residual:
-// out = bf16(r' / sqrt(mean r'^2 + eps) * gamma).  No CTA waits for another; every order
-// is fixed, so the result is deterministic and each activation row's depends on that
-// row alone.
+// Four CTAs of 256 threads per SM: 64 registers a thread, and every variant (one or
+// two row blocks) equally resident.  Measured on the decode pass: 3 per SM (80
+// registers) and 5 per SM (48 registers, spills) are both slower.
+constexpr int kMvCtasPerSm = 4;
+
+// The post-add / next-norm epilogue after the tile's residual rows are stored
+// (TensorFold PR #1514, "What changes": post-add/next-norm fusion): the tile's sum of
+// squares per activation row (its 16 channels in order) goes to its slot; the CTA that
+// finishes last (a device counter) adds the slots in tile order, and normalises every
+// channel of every row from the stored residual: out = bf16(r' / sqrt(mean r'^2 + eps)
+// * gamma).  No CTA waits for another; every order is fixed, so the result is
+// deterministic and each activation row's depends on that row alone.
 template <int NB>
-__device__ __forceinline__ void resid_norm_tail(const MvParams &p) {
+__device__ __forceinline__ void resid_norm_tail(const MvParams &p, int tile, float (*s_sq)[17]) {
   __shared__ float s_wsum[kMvWarps][8 * NB];
   __shared__ float s_rstd[8 * NB];
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = p.m[0].n;
-  __threadfence();  // this CTA's residual rows and slots are visible device-wide
+  __syncthreads();  // s_sq complete
+  if (tid < p.rows) {
+    float sacc = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) sacc = __fadd_rn(sacc, s_sq[tid][c]);
+    p.part[(size_t)tile * 16 + tid] = sacc;
+  }
+  __threadfence();  // this tile's residual rows and slot are visible device-wide
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
+  if (tid == 0) s_last = atomicAdd(p.counter, 1u) == (unsigned)(p.ntiles - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -184,271 +206,261 @@ __device__ __forceinline__ void resid_norm_tail(const MvParams &p) {
 }
 
 template <int BITS, int NB, int MODE>
-__global__ void __launch_bounds__(kMvThreads, 2) qmv_kernel(const __grid_constant__ MvParams p) {
+__global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __grid_constant__ MvParams p) {
   using Lay = MvLayout<BITS, NB, MODE>;
   constexpr int NMAT = Lay::NMAT;
   constexpr int NV = Lay::NV;
-  constexpr int NO = NB * 4;  // outputs per lane per matrix
-  constexpr int NS = Lay::NS;
-  constexpr int SPAN = Lay::SPAN;
   constexpr int LW = Geo<BITS>::kLw;
   constexpr int GPW = Geo<BITS>::kGpw;
+  constexpr int GPC = gpc<BITS>();
+  constexpr int SPAN = span_g<BITS>();
   constexpr int GB = gbytes<BITS>();
   constexpr int WP = wpitch<BITS>();
   constexpr bool kPair4 = BITS == 4;  // 4-bit codes paired (t, t+4): activations in that order
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::kOffBar);
-  float *red = reinterpret_cast<float *>(smem + Lay::kOffRed);
-  float4 *fac = reinterpret_cast<float4 *>(smem + Lay::kOffFac);
-  __shared__ int s_abort;
-  __shared__ float s_sq[MODE == kMvResid ? 8 * NB : 1][17];  // [activation row][channel of the tile]
+  float4 *sbf = reinterpret_cast<float4 *>(smem + Lay::kSbf);
+  float *red = reinterpret_cast<float *>(smem + Lay::kRed);
+  float *csum = reinterpret_cast<float *>(smem + (p.cs > 1 ? Lay::kCpart : Lay::kCsum));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
+  uint8_t *wsm = smem + Lay::kW;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = p.cs > 1 ? (int)cluster.block_rank() : 0;
+  const int tile_g = blockIdx.x / p.cs;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g4 = lane >> 2, c = lane & 3;
-  const int G = p.groups, nspan = p.nspan;
-  const int t0 = (int)(((long long)blockIdx.x * p.ntiles) / gridDim.x);
-  const int t1 = (int)(((long long)(blockIdx.x + 1) * p.ntiles) / gridDim.x);
-  const int J = (t1 - t0) * nspan;  // ring slots this CTA consumes
-  const size_t row_bytes = (size_t)G * GB;
 
-  if (tid == 0) {
-    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+  int mi = 0, tile = tile_g;
+  if constexpr (MODE == kMvAttn) {
+    while (mi < 3 && tile_g >= p.tile_end[mi]) ++mi;
+    tile = tile_g - (mi ? p.tile_end[mi - 1] : 0);
+  }
+  const int n = p.m[mi].n;
+  const size_t row_bytes = (size_t)p.groups * GB;
+
+  // this CTA's k-span: groups [gs0, gs1), in spans of SPAN groups
+  const int gs0 = rank * p.span_g, gs1 = min(p.groups, gs0 + p.span_g);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNch; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
-    s_abort = 0;
   }
   __syncthreads();
 
-  // matrix and 16-row tile within it of a tile index of the launch
-  auto tile_mat = [&](int t, int &mi, int &lt) {
-    mi = 0;
-    if constexpr (MODE == kMvAttn) {
-      while (mi < 3 && t >= p.tile_end[mi]) ++mi;
-    }
-    lt = t - (mi ? p.tile_end[mi - 1] : 0);
-  };
-
-  // warp 0: one bulk copy per weight row of slot j (lane l: matrix l / 16, row l % 16),
-  // and of its scale and bias rows, into ring buffer j % NS
-  int issued = 0;  // slots issued so far (warp 0)
-  auto issue = [&](int j) {
-    const int t = t0 + j / nspan, sp = j - (j / nspan) * nspan;
-    int mi, lt;
-    tile_mat(t, mi, lt);
-    const int g0 = sp * SPAN, ng = min(SPAN, G - g0);
-    const int mt = lane >> 4, r = lane & 15;
-    const int row = lt * 16 + r;
-    const bool mine = mt < NMAT && row < p.m[mi + (mt < NMAT ? mt : 0)].n;
-    uint32_t bytes = mine ? (uint32_t)(ng * GB + (p.sb_bulk ? 4 * ng : 0)) : 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-    uint64_t *bar = &full[j % NS];
-    uint8_t *slot = smem + (j % NS) * Lay::kSlot;
-    if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-    __syncwarp();
-    if (mine) {
-      const MvMat &M = p.m[mi + mt];
-      bulk_g2s(slot + (mt * 16 + r) * WP, reinterpret_cast<const uint8_t *>(M.wq) + (size_t)row * row_bytes +
-                                              (size_t)g0 * GB,
-               (uint32_t)(ng * GB), bar);
-      if (p.sb_bulk) {
-        uint8_t *sb = slot + Lay::kWBytes + (mt * 16 + r) * Lay::kSBRow;
-        bulk_g2s(sb, M.s + (size_t)row * G + g0, (uint32_t)(2 * ng), bar);
-        bulk_g2s(sb + NMAT * 16 * Lay::kSBRow, M.b + (size_t)row * G + g0, (uint32_t)(2 * ng), bar);
-      }
-    }
-  };
-
-  // ---- the weight stream starts before the dependency wait: it reads nothing a
-  //      preceding kernel writes
-  if (warp == 0) {
-    const int first = J < NS ? J : NS;
-    for (int j = 0; j < first; ++j) issue(j);
-    issued = first;
-  }
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  bool xv[NB];
-#pragma unroll
-  for (int h = 0; h < NB; ++h) xv[h] = (8 * h + g4) < p.rows;
   float y[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) y[i] = 0.0f;
+  uint32_t phase = 0;
   bool ok = true;
+  int armed = 0;  // chunks of the last span whose copies were started (warp 0)
 
-  // With one span per tile (k <= 2048 at 4 bits, k <= 1024 otherwise) every slot of the
-  // CTA covers the same groups: the activation fragments and sums of the warp's groups
-  // are loaded and formed once, at the first slot, and kept in registers.
-  const bool hoist = NB == 1 && nspan == 1;  // (two row blocks: kept per group, registers)
-  uint4 Xh0[GPW][NB], Xh1[GPW][NB];
-  float Sh[GPW][NB][4];
-  constexpr int NQ = GPW * NMAT * 16;  // group factors per warp per slot
-  float4 *fw = fac + warp * NQ;
-  for (int j = 0; j < J; ++j) {
-    const int ti = j / nspan, sp = j - ti * nspan, buf = j % NS;
-    int mi, lt;
-    tile_mat(t0 + ti, mi, lt);
-    const int g0 = sp * SPAN, ng = min(SPAN, G - g0);
-    const uint8_t *slot = smem + buf * Lay::kSlot;
-    if (sp == 0) {
-#pragma unroll
-      for (int i = 0; i < NV; ++i) y[i] = 0.0f;
-    }
-    if (ok && !mbar_wait_bounded(&full[buf], (uint32_t)(j / NS) & 1u, p.budget_ns, &s_abort)) {
-      ok = false;
-      s_abort = 1;
-    }
-    const int gw0 = warp * GPW;  // this warp's first group of the span
-    if (ok && gw0 < ng) {
-      const int gcnt = min(GPW, ng - gw0);
-      // the factors of the warp's groups of this slot (lane q: group q / (16 NMAT),
-      // matrix (q / 16) % NMAT, row q % 16)
-      for (int q = lane; q < NQ; q += 32) {
-        const int gi = q / (NMAT * 16), mt = (q >> 4) % NMAT, r = q & 15;
-        const int gl = gw0 + gi, row = lt * 16 + r;
-        float s1 = 0.0f, b1 = 0.0f;
-        if (gi < gcnt && row < p.m[mi + mt].n) {
-          if (p.sb_bulk) {
-            const uint16_t *sb = reinterpret_cast<const uint16_t *>(slot + Lay::kWBytes) + (mt * 16 + r) * SPAN + gl;
-            s1 = bf16_to_f32(sb[0]);
-            b1 = bf16_to_f32(sb[NMAT * 16 * SPAN]);
-          } else {
-            const size_t off = (size_t)row * G + g0 + gl;
-            s1 = bf16_to_f32(ldg_u16(p.m[mi + mt].s + off));
-            b1 = bf16_to_f32(ldg_u16(p.m[mi + mt].b + off));
-          }
-        }
-        fw[q] = group_factors<BITS>(s1, b1);
+  for (int ch0 = gs0; ch0 < gs1; ch0 += SPAN) {
+    const int ch1 = min(gs1, ch0 + SPAN);
+    const int ng = ch1 - ch0;
+    if (warp == 0) {
+      // ---- warp 0 first starts the span's copies, chunk by chunk, one bulk copy per
+      //      weight row of the chunk (every warp has finished the previous span: the
+      //      barrier at the end of each span)
+      const int t = lane >> 4, r = lane & 15;
+      const int row = tile * 16 + r;
+      const bool mine = lane < NMAT * 16 && row < n;
+      if (ch0 != gs0 && lane == 0) {
+        // the previous span's copies have landed (its consumers waited for them, unless
+        // a wait gave up) before this span's copies reuse the buffers and barriers
+        for (int cc = 0; cc < armed; ++cc) (void)mbar_wait_bounded(&bars[cc], phase ^ 1u, kMvDrainNs, nullptr);
+        fence_proxy_async_smem();
       }
-      __syncwarp();
-      if (hoist) {
-        if (j == 0) {
+      armed = 0;
+      for (int cc = 0; cc < kNch; ++cc) {
+        const int ga = ch0 + cc * GPC;
+        if (ga >= ch1) break;
+        const int gb = min(ch1, ga + GPC);
+        const uint32_t wb = (uint32_t)((gb - ga) * GB);
+        uint32_t bytes = mine ? wb : 0u;
 #pragma unroll
-          for (int gi = 0; gi < GPW; ++gi) {
-#pragma unroll
-            for (int h = 0; h < NB; ++h) {
-              Xh0[gi][h] = make_uint4(0, 0, 0, 0);
-              Xh1[gi][h] = make_uint4(0, 0, 0, 0);
-              if (xv[h] && gi < gcnt)
-                load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(g0 + gw0 + gi) * 64 + 16 * c,
-                                    Xh0[gi][h], Xh1[gi][h]);
-            }
-          }
-#pragma unroll
-          for (int gi = 0; gi < GPW; ++gi)
-            if (gi < gcnt) mv_sums<NB>(Xh0[gi], Xh1[gi], Sh[gi]);
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[cc], bytes);
+        __syncwarp();
+        if (mine) {
+          const uint8_t *src = reinterpret_cast<const uint8_t *>(p.m[mi + t].wq) + (size_t)row * row_bytes +
+                               (size_t)ga * GB;
+          bulk_g2s(wsm + (t * 16 + r) * WP + (ga - ch0) * GB, src, wb, &bars[cc]);
         }
+        armed = cc + 1;
+      }
+    }
+    {
+      // ---- every warp computes
+      const int tid = threadIdx.x;  // 0 .. kMvComputeThreads-1
+      // Scales and biases of the span (not written by a preceding kernel, so read
+      // before the dependency wait) -> per-group factors (group_factors).  16-byte vectors of 8
+      // groups when the rows allow it, else one value at a time.
+      if (p.sb_bulk) {
+        const int v8 = ng >> 3;  // vectors per row
+        for (int e = tid; e < NMAT * 16 * v8; e += kMvComputeThreads) {
+          const int t = e / (16 * v8), rr = (e / v8) % 16, v = e % v8;
+          const int row = tile * 16 + rr;
+          uint4 sv = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
+          if (row < n) {
+            const size_t off = (size_t)row * p.groups + ch0 + 8 * v;
+            sv = ldg_v4(p.m[mi + t].s + off);
+            bv = ldg_v4(p.m[mi + t].b + off);
+          }
+          const uint32_t ss[4] = {sv.x, sv.y, sv.z, sv.w}, bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-        for (int gi = 0; gi < GPW; ++gi) {
-          if (gi < gcnt)
-            mv_group_s<BITS, NB, NMAT>(slot + (gw0 + gi) * GB + c * 4 * LW, WP, fw + gi * NMAT * 16, 16, Xh0[gi],
-                                       Xh1[gi], Sh[gi], g4, y);
+          for (int q2 = 0; q2 < 8; ++q2) {
+            const float s1 = bf16_to_f32((ss[q2 >> 1] >> (16 * (q2 & 1))) & 0xFFFFu);
+            const float b1 = bf16_to_f32((bb[q2 >> 1] >> (16 * (q2 & 1))) & 0xFFFFu);
+            sbf[(t * SPAN + 8 * v + q2) * 16 + rr] = group_factors<BITS>(s1, b1);
+          }
         }
       } else {
+        for (int e = tid; e < NMAT * 16 * ng; e += kMvComputeThreads) {
+          const int t = e / (16 * ng), rr = (e / ng) % 16, gg = e % ng;
+          const int row = tile * 16 + rr;
+          float s1 = 0.0f, b1 = 0.0f;
+          if (row < n) {
+            const size_t off = (size_t)row * p.groups + ch0 + gg;
+            s1 = bf16_to_f32(ldg_u16(p.m[mi + t].s + off));
+            b1 = bf16_to_f32(ldg_u16(p.m[mi + t].b + off));
+          }
+          sbf[(t * SPAN + gg) * 16 + rr] = group_factors<BITS>(s1, b1);
+        }
+      }
+      // Activations: a preceding kernel may write them, so they are read only after
+      // the programmatic-dependency wait.
+      if (ch0 == gs0) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+      }
+      named_bar_sync(kBarCompute, kMvComputeThreads);  // group factors visible
+      bool xv[NB];
+#pragma unroll
+      for (int h = 0; h < NB; ++h) xv[h] = (8 * h + g4) < p.rows;
+      for (int cc = 0; cc < kNch; ++cc) {
+        const int ga = ch0 + cc * GPC;
+        if (ga >= ch1) break;
+        const int gw0 = ga + warp * GPW;  // this warp's groups of the chunk
+        const int gcnt = max(0, min(GPW, ch1 - gw0));
+        // the first group's activations are in flight while the chunk's weights land
+        uint4 Xa[NB], Xb[NB];
+#pragma unroll
+        for (int h = 0; h < NB; ++h) {
+          Xa[h] = make_uint4(0, 0, 0, 0);
+          Xb[h] = make_uint4(0, 0, 0, 0);
+          if (xv[h] && gcnt > 0)
+            load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)gw0 * 64 + 16 * c, Xa[h], Xb[h]);
+        }
+        if (ok) ok = mbar_wait_bounded(&bars[cc], phase, p.budget_ns, nullptr);
+        if (!ok) continue;  // keep every barrier below matched; the status word records why
 #pragma unroll
         for (int gi = 0; gi < GPW; ++gi) {
           if (gi < gcnt) {
+            const int gl = gw0 + gi - ch0;  // group index within the span
             uint4 X0[NB], X1[NB];
-            float S[NB][4];
 #pragma unroll
             for (int h = 0; h < NB; ++h) {
-              X0[h] = make_uint4(0, 0, 0, 0);
-              X1[h] = make_uint4(0, 0, 0, 0);
-              if (xv[h])
-                load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(g0 + gw0 + gi) * 64 + 16 * c,
-                                    X0[h], X1[h]);
+              if (NB == 1 || gi == 0) {
+                // one activation row block: the next group's fragments are loaded a
+                // group ahead; with two blocks they are loaded when used (registers)
+                X0[h] = Xa[h];
+                X1[h] = Xb[h];
+                if (NB == 1 && xv[h] && gi + 1 < gcnt)
+                  load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi + 1) * 64 + 16 * c, Xa[h],
+                                    Xb[h]);
+              } else if (xv[h]) {
+                load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)(gw0 + gi) * 64 + 16 * c, X0[h], X1[h]);
+              } else {
+                X0[h] = make_uint4(0, 0, 0, 0);
+                X1[h] = make_uint4(0, 0, 0, 0);
+              }
             }
-            mv_sums<NB>(X0, X1, S);
-            mv_group_s<BITS, NB, NMAT>(slot + (gw0 + gi) * GB + c * 4 * LW, WP, fw + gi * NMAT * 16, 16, X0, X1, S,
-                                       g4, y);
+            mv_group<BITS, NB, NMAT>(wsm + gl * GB + c * 4 * LW, WP, sbf + gl * 16, SPAN * 16, X0, X1, g4, y);
           }
         }
       }
     }
-    const bool last = sp == nspan - 1;
-    float *rb = red + (ti & 1) * (kMvWarps * NV * 32);
-    if (last) {
-#pragma unroll
-      for (int i = 0; i < NV; ++i) rb[(warp * NV + i) * 32 + lane] = y[i];
-    }
-    // every warp is done with slot j (it may be refilled) and the tile's partials are visible
-    named_bar_sync(kBarSlot, kMvThreads);
-    if (s_abort) ok = false;
-    if (warp == 0 && ok && issued < J) {
-      if (lane == 0) fence_proxy_async_smem();
-      __syncwarp();
-      issue(issued);
-      ++issued;
-    }
-    if (last) {
-      // the tile's outputs: the warps' partials added in warp order
-      for (int v = tid; v < NO * 32; v += kMvThreads) {
-        const int i = v >> 5, ln = v & 31;
-        float acc[NMAT];
-#pragma unroll
-        for (int t = 0; t < NMAT; ++t) {
-          acc[t] = rb[(t * NO + i) * 32 + ln];
-#pragma unroll
-          for (int w = 1; w < kMvWarps; ++w) acc[t] = __fadd_rn(acc[t], rb[(w * NV + t * NO + i) * 32 + ln]);
-        }
-        // value i of lane ln: half h = i / 4, element e = i % 4
-        const int h = i >> 2, e = i & 3;
-        const int ch = (ln >> 2) + ((e & 2) ? 8 : 0);
-        const int row = lt * 16 + ch;
-        const int xr = 8 * h + 2 * (ln & 3) + (e & 1);
-        const MvMat &M = p.m[mi];
-        if constexpr (MODE == kMvResid) {
-          // post-add: the stored residual r' = bf16(r + y) and its square
-          float sq = 0.0f;
-          if (ok && row < M.n && xr < p.rows) {
-            uint16_t *rp = p.resid + (size_t)xr * p.ldr + row;
-            const uint16_t nb = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(*rp), acc[0]));
-            *rp = nb;
-            const float vv = bf16_to_f32(nb);
-            sq = __fmul_rn(vv, vv);
-          }
-          s_sq[xr][ch] = sq;
-        } else if (ok && row < M.n && xr < p.rows) {
-          if constexpr (MODE == kMvFfn) {
-            static_cast<uint16_t *>(M.out)[(size_t)xr * M.ldo + row] = swiglu_bf16(acc[0], acc[1]);
-          } else {
-            static_cast<float *>(M.out)[(size_t)xr * M.ldo + row] = acc[0];
-          }
-        }
-      }
-      if constexpr (MODE == kMvResid) {
-        // the tile's sum of squares per activation row, its 16 channels in order
-        __syncthreads();
-        if (tid < p.rows) {
-          float sacc = 0.0f;
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) sacc = __fadd_rn(sacc, s_sq[tid][ch]);
-          p.part[(size_t)(t0 + ti) * 16 + tid] = sacc;
-        }
-        __syncthreads();
-      }
-    }
+    phase ^= 1u;
+    if (ch1 < gs1) __syncthreads();  // the span's buffers are fully read before the next span refills them
   }
   if (!ok && lane == 0) record_status(p.status, kErrTimeout);
   if (warp == 0 && lane == 0) {
-    // copies issued but not consumed (only after a wait gave up) land before the CTA exits
-    for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
-      (void)mbar_wait_bounded(&full[j % NS], (uint32_t)(j / NS) & 1u, kMvDrainNs, nullptr);
+    // every copy this CTA started has landed before the partials reuse the weight area
+    // and before the CTA exits (immediate unless a wait gave up)
+    for (int cc = 0; cc < armed; ++cc) (void)mbar_wait_bounded(&bars[cc], phase ^ 1u, kMvDrainNs, nullptr);
   }
-  if constexpr (MODE == kMvResid) resid_norm_tail<NB>(p);
-}
 
-// SMs of the current device (cached per device)
-static int mv_sm_count() {
-  static std::atomic<int> cached[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  int c = cached[dev].load(std::memory_order_relaxed);
-  if (c == 0) {
-    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 1;
-    cached[dev].store(c, std::memory_order_relaxed);
+  // ---- partials: warps in order, then cluster ranks in order.  The partials reuse
+  //      the weight area, so every compute warp is past its last group first.  In a
+  //      cluster each rank writes its CTA partial into slot `rank` of rank 0's cpart
+  //      (distributed shared memory); after one cluster barrier rank 0 adds the slots
+  //      in rank order and the other ranks may exit (nobody reads their shared memory).
+  {
+    named_bar_sync(kBarCompute, kMvComputeThreads);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) red[(warp * NV + i) * 32 + lane] = y[i];
+    named_bar_sync(kBarCompute, kMvComputeThreads);
+    if (p.cs > 1) {
+      float *dst = cluster.map_shared_rank(csum, 0) + rank * NV * 32;
+      for (int v = threadIdx.x; v < NV * 32; v += kMvComputeThreads) {
+        const int i = v >> 5, ln = v & 31;
+        float acc = red[i * 32 + ln];
+#pragma unroll
+        for (int w = 1; w < kMvWarps; ++w) acc = __fadd_rn(acc, red[(w * NV + i) * 32 + ln]);
+        dst[i * 32 + ln] = acc;
+      }
+    }
   }
-  return c;
+  // without a cluster the warp partials are added in warp order right below, where
+  // they are stored (the same order; the barrier above made them visible)
+  if (p.cs > 1) cluster.sync();
+  if (rank == 0) {
+    constexpr int NO = NB * 4;  // outputs per lane per matrix
+    __shared__ float s_sq[MODE == kMvResid ? 8 * NB : 1][17];  // [activation row][channel of the tile]
+    for (int v = threadIdx.x; v < NO * 32; v += kMvThreads) {
+      const int i = v >> 5, ln = v & 31;
+      float acc[NMAT];
+      if (p.cs > 1) {
+#pragma unroll
+        for (int t = 0; t < NMAT; ++t) acc[t] = csum[(t * NO + i) * 32 + ln];
+        for (int r = 1; r < p.cs; ++r) {
+#pragma unroll
+          for (int t = 0; t < NMAT; ++t) acc[t] = __fadd_rn(acc[t], csum[r * NV * 32 + (t * NO + i) * 32 + ln]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < NMAT; ++t) {
+          acc[t] = red[(t * NO + i) * 32 + ln];
+#pragma unroll
+          for (int w = 1; w < kMvWarps; ++w) acc[t] = __fadd_rn(acc[t], red[(w * NV + t * NO + i) * 32 + ln]);
+        }
+      }
+      // value i of lane ln: half h = i / 4, element e = i % 4
+      const int h = i >> 2, e = i & 3;
+      const int row = tile * 16 + (ln >> 2) + ((e & 2) ? 8 : 0);
+      const int xr = 8 * h + 2 * (ln & 3) + (e & 1);
+      if constexpr (MODE == kMvResid) {
+        // post-add: the stored residual r' = bf16(r + y) and its square
+        float sq = 0.0f;
+        if (row < n && xr < p.rows) {
+          uint16_t *rp = p.resid + (size_t)xr * p.ldr + row;
+          const uint16_t nb = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(*rp), acc[0]));
+          *rp = nb;
+          const float v = bf16_to_f32(nb);
+          sq = __fmul_rn(v, v);
+        }
+        s_sq[xr][(ln >> 2) + ((e & 2) ? 8 : 0)] = sq;
+      } else if (row < n && xr < p.rows) {
+        const MvMat &M = p.m[mi];
+        if constexpr (MODE == kMvFfn) {
+          static_cast<uint16_t *>(M.out)[(size_t)xr * M.ldo + row] = swiglu_bf16(acc[0], acc[1]);
+        } else {
+          static_cast<float *>(M.out)[(size_t)xr * M.ldo + row] = acc[0];
+        }
+      }
+    }
+    if constexpr (MODE == kMvResid) resid_norm_tail<NB>(p, tile, s_sq);
+  }
 }
 
 template <int BITS, int NB, int MODE>
@@ -459,26 +471,29 @@ static cudaError_t launch_t(const MvParams &p, int tiles, cudaStream_t st) {
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev].load(std::memory_order_relaxed)) {
     cudaError_t e = cudaFuncSetAttribute(qmv_kernel<BITS, NB, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay::kBytes);
+                                         Lay::max_bytes());
     if (e != cudaSuccess) return e;
-    // the largest shared-memory carveout, so CTAs of consecutive launches (programmatic
-    // dependent launch) share an SM
+    // every decode kernel asks for the largest shared-memory carveout, so CTAs of
+    // consecutive launches (programmatic dependent launch) can share an SM
     e = cudaFuncSetAttribute(qmv_kernel<BITS, NB, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done[dev].store(true, std::memory_order_relaxed);
   }
-  const int sms = mv_sm_count();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));
+  cfg.gridDim = dim3((unsigned)(tiles * p.cs));
   cfg.blockDim = dim3((unsigned)kMvThreads);
-  cfg.dynamicSmemBytes = (size_t)Lay::kBytes;
+  cfg.dynamicSmemBytes = (size_t)Lay::bytes(p.cs);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, qmv_kernel<BITS, NB, MODE>, p);
 }
 
@@ -492,16 +507,28 @@ static cudaError_t launch_mode(const MvParams &p, int bits, int tiles, cudaStrea
   }
 }
 
+// k-decomposition used by every decode launch (a function of k and bits only):
+// CTAs per cluster cs = min(8, ceil(groups / span)), each CTA takes ceil(groups / cs)
+// groups in chunks of the span; warps = ceil(min(groups, span) / gpw) <= kMvWarps.
+void mv_geometry(int k, int bits, int &groups, int &span_g_out, int &nwarps, int &cs) {
+  groups = k / kGroup;
+  const int span = mv_span_g(bits);
+  const int gpw = span / kMvWarps;
+  const int need = (groups + span - 1) / span;
+  cs = need < kMvMaxCluster ? need : kMvMaxCluster;
+  span_g_out = (groups + cs - 1) / cs;
+  const int chunk = span_g_out < span ? span_g_out : span;
+  nwarps = (chunk + gpw - 1) / gpw;
+}
+
 cudaError_t launch_mv(MvParams &p, int mode, int bits, int tiles, cudaStream_t st) {
-  p.groups = p.k / kGroup;
-  const int span = bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6>() : span_g<8>());
-  p.nspan = (p.groups + span - 1) / span;
-  p.ntiles = tiles;
-  if (mode != kMvAttn) p.tile_end[0] = tiles;
-  // scale/bias rows of a span can be bulk-copied when every copy starts and ends on a
-  // 16-byte boundary: groups a multiple of 8 (spans are), pointers 16-byte aligned
+  int nwarps;
+  mv_geometry(p.k, bits, p.groups, p.span_g, nwarps, p.cs);
+  p.wpr = p.k * bits / 32;
+  // scale/bias rows of a chunk can be bulk-copied when every copy starts and ends on
+  // a 16-byte boundary: groups and the per-CTA span multiples of 8, pointers aligned
   const int nm = mode == kMvAttn ? 4 : (mode == kMvFfn ? 2 : 1);
-  bool sb = (p.groups % 8) == 0;
+  bool sb = (p.groups % 8) == 0 && (p.span_g % 8) == 0;
   for (int i = 0; i < nm; ++i)
     sb = sb && (reinterpret_cast<uintptr_t>(p.m[i].s) % 16) == 0 && (reinterpret_cast<uintptr_t>(p.m[i].b) % 16) == 0;
   p.sb_bulk = sb ? 1 : 0;

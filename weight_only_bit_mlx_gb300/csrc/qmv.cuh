@@ -6,8 +6,9 @@
 
 namespace qlk {
 
-// warps per CTA, each owning a slice of every k-span
+// warps per CTA, each owning a slice of the CTA's k-span (4 measured slower on the decode pass)
 constexpr int kMvWarps = 8;
+constexpr int kMvMaxCluster = 8;  // CTAs per cluster along k
 
 enum { kMvPlain = 0, kMvFfn = 1, kMvAttn = 2, kMvResid = 3 };
 
@@ -22,13 +23,13 @@ struct MvMat {
 
 struct MvParams {
   MvMat m[4];        // plain: m[0]; ffn: m[0] = w1, m[1] = w3; attn: q, k, v, gate
-  int tile_end[4];   // cumulative 16-row tile counts of m[0..3] (attn); tile_end[0] = tiles otherwise
+  int tile_end[4];   // attn: cumulative 16-row tile counts of m[0..3]
   const uint16_t *x;
   int64_t ldx;
   int rows;
   int k;
   int *status;           // device status word (bounded waits record QL_ERR_TIMEOUT)
-  int sb_bulk;           // scales/biases rows are 16-byte aligned: copied in bulk with the weights
+  int sb_bulk;           // scales/biases rows are 16-byte aligned: copied in bulk
   uint64_t budget_ns;    // bound of every device-side wait
   // kMvResid: the post-add / next-norm epilogue (one weight, like kMvPlain)
   uint16_t *resid;       // bf16 [rows, ldr], read and overwritten with bf16(resid + y)
@@ -38,15 +39,23 @@ struct MvParams {
   uint16_t *nout;        // bf16 [rows, ldn]: the normalised stored residual times gamma
   int64_t ldn;
   float *part;           // [tiles][16] per-tile sums of squares (library scratch)
-  unsigned *counter;     // CTAs finished (library scratch, zero between calls)
+  unsigned *counter;     // tiles finished (library scratch, zero between calls)
   int ntiles;            // 16-row tiles of the launch
   // filled by launch_mv from k and bits
   int groups;
-  int nspan;             // spans (ring slots) per tile
+  int wpr;
+  int span_g;            // groups per CTA (processed in chunks of the per-bits span)
+  int cs;                // CTAs per cluster along k
 };
 
+// groups per k-span of one CTA for the given code width
+int mv_span_g(int bits);
+
+// k-decomposition used by every decode launch (a function of k and bits only)
+void mv_geometry(int k, int bits, int &groups, int &span_g, int &nwarps, int &cs);
+
 // Maximum 16-row tiles of a kMvResid launch (n <= 65536) and the device addresses of its
-// per-tile partial sums and finished-CTA counter (current device); reset the counter.
+// per-tile partial sums and finished-tile counter (current device); reset the counter.
 constexpr int kMvResidMaxTiles = 4096;
 int mv_resid_scratch(float **part, unsigned **counter);
 int mv_resid_counter_reset();

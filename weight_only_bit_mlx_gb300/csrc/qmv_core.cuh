@@ -13,17 +13,20 @@
 namespace qlk {
 
 template <int BITS> struct Geo;
-// A span is the k-range of one ring slot: 32 groups (4-bit) or 16 groups (6/8-bit),
-// split over the kMvWarps warps (4 or 2 consecutive groups each).
+// chunks per span, one mbarrier each (2, computing the first half while the second
+// lands, measured slower on the decode pass)
+constexpr int kNch = 1;
+// spans of 32 groups (4-bit) or 16 groups (6/8-bit), split over the compute warps and chunks
 template <> struct Geo<4> {
-  static constexpr int kLw = 2;                      // words per lane per row per group
-  static constexpr int kGpw = 32 / kMvWarps;         // groups per warp per span
+  static constexpr int kLw = 2;                          // words per lane per row per group
+  static constexpr int kGpw = 32 / (kMvWarps * kNch);    // groups per compute warp per chunk
 };
-template <> struct Geo<6> { static constexpr int kLw = 3; static constexpr int kGpw = 16 / kMvWarps; };
-template <> struct Geo<8> { static constexpr int kLw = 4; static constexpr int kGpw = 16 / kMvWarps; };
-static_assert(Geo<6>::kGpw >= 1, "every warp owns at least one group per span");
+template <> struct Geo<6> { static constexpr int kLw = 3; static constexpr int kGpw = 16 / (kMvWarps * kNch); };
+template <> struct Geo<8> { static constexpr int kLw = 4; static constexpr int kGpw = 16 / (kMvWarps * kNch); };
+static_assert(Geo<6>::kGpw >= 1, "every compute warp owns at least one group per chunk");
 template <int BITS> __host__ __device__ constexpr int gbytes() { return 8 * BITS; }                  // bytes per row per group
-template <int BITS> __host__ __device__ constexpr int span_g() { return kMvWarps * Geo<BITS>::kGpw; }  // groups per span
+template <int BITS> __host__ __device__ constexpr int gpc() { return kMvWarps * Geo<BITS>::kGpw; }  // groups per chunk
+template <int BITS> __host__ __device__ constexpr int span_g() { return kNch * gpc<BITS>(); }        // groups per span
 template <int BITS> __host__ __device__ constexpr int wpitch() { return span_g<BITS>() * gbytes<BITS>() + 32; }  // padded row pitch
 
 // Lane (g4, c) of a warp holds, for each of its two rows (g4, g4 + 8), the 16 codes
@@ -97,8 +100,9 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                : "memory");
 }
 
-constexpr int kMvThreads = kMvWarps * 32;  // every warp computes; warp 0 also issues the bulk copies
-constexpr int kBarSlot = 1;                      // named barrier: a ring slot is consumed
+constexpr int kMvThreads = kMvWarps * 32;  // compute warps (warp 0 also starts the bulk copies)
+constexpr int kMvComputeThreads = kMvWarps * 32;
+constexpr int kBarCompute = 1;                   // named barrier of the compute warps
 constexpr uint64_t kMvDrainNs = 2000000000ull;
 
 // activation fragment of lane (g4, c) for one group: x[row][64g + 16c .. +16) as two
@@ -116,30 +120,26 @@ __device__ __forceinline__ void load_x_frag(const uint16_t *px, uint4 &a, uint4 
   }
 }
 
-// The activation sums S_g of one group for this lane's output columns: the tensor-core
-// path with A = 1, four MMAs in k order (a function of the activations alone).
-template <int NB>
-__device__ __forceinline__ void mv_sums(const uint4 (&X0)[NB], const uint4 (&X1)[NB], float (&S)[NB][4]) {
+// One group of one warp: S of the group for this lane's output columns (MMA with
+// A = 1), then for each of the NMAT matrices the exact centred codes q - z of rows g4 and g4 + 8
+// (wrow: the lane's bytes of row 0 of matrix 0 of the group; rows WP bytes apart,
+// matrices 16 rows apart) on the tensor cores with a fresh accumulator, and the
+// group's affine step y = fma(s, P', y); y = fma(b', S, y) with the factors of rows g4
+// and g4 + 8 (group_factors; fg: matrix 0's factors of the group, 16 rows; matrices
+// fstride apart).
+template <int BITS, int NB, int NMAT>
+__device__ __forceinline__ void mv_group(const uint8_t *wrow, int WP, const float4 *fg, int fstride,
+                                         const uint4 (&X0)[NB], const uint4 (&X1)[NB], int g4,
+                                         float (&y)[NMAT * NB * 4]) {
+  constexpr int LW = Geo<BITS>::kLw;
   const uint32_t ones[4] = {kBf16One2, kBf16One2, kBf16One2, kBf16One2};
+  float S[NB][4];
 #pragma unroll
   for (int h = 0; h < NB; ++h) {
     S[h][0] = S[h][1] = S[h][2] = S[h][3] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) mma_bf16_16816(S[h], ones, u4get(X0[h], j), u4get(X1[h], j), S[h]);
   }
-}
-
-// One group of one warp, given its activation sums S (mv_sums): for each of the NMAT
-// matrices the exact centred codes q - z of rows g4 and g4 + 8 (wrow: the lane's bytes
-// of row 0 of matrix 0 of the group; rows WP bytes apart, matrices 16 rows apart) on the
-// tensor cores with a fresh accumulator, then the group's affine step
-// y = fma(s, P', y); y = fma(b', S, y) with the factors of rows g4 and g4 + 8
-// (group_factors; fg: matrix 0's factors of the group, 16 rows; matrices fstride apart).
-template <int BITS, int NB, int NMAT>
-__device__ __forceinline__ void mv_group_s(const uint8_t *wrow, int WP, const float4 *fg, int fstride,
-                                           const uint4 (&X0)[NB], const uint4 (&X1)[NB], const float (&S)[NB][4],
-                                           int g4, float (&y)[NMAT * NB * 4]) {
-  constexpr int LW = Geo<BITS>::kLw;
 #pragma unroll
   for (int t = 0; t < NMAT; ++t) {
     uint32_t W0[LW], W1[LW];
