@@ -57,19 +57,21 @@ namespace qlk {
 
 namespace pg {
 
-constexpr int BM = 256;  // rows of X per tile (MMA N)
-constexpr int BN = 128;  // output channels per tile (MMA M, tensor-memory lanes)
+constexpr int BM = 256;   // rows of X per tile (MMA N)
+constexpr int BMH = 128;  // rows of X staged by each CTA of the pair (its half of the MMA's N)
+constexpr int BN = 128;   // output channels of each CTA (its half of the MMA's M = 256; tensor-memory lanes)
 constexpr int BK = 64;
+constexpr int kPairRing = 4;  // barriers on which the second CTA reports its staged halves
 constexpr int kScStages = 8;  // fp32 scale rows (deep enough to need no release barrier, see converters)
 constexpr int kConvWarps = 4;   // one channel row per thread
 constexpr int kEpiWarps = 16;   // four per tensor-memory lane quarter, 64 rows of X each
-constexpr int kRoleWarps = 3;   // producer, two MMA issuers (the first also allocates tensor memory)
+constexpr int kRoleWarps = 3;   // producer, two MMA issuers (second CTA: the relay) - warp 1 allocates tensor memory
 constexpr int kThreads = (kRoleWarps + kConvWarps + kEpiWarps) * 32;
 constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiRows = BM / (kEpiWarps / 4);  // rows of X per epilogue thread
-constexpr int kXBytes = BM * BK * 2;            // X tile: BM rows x 64 bf16, 128-byte swizzle
+constexpr int kXBytes = BMH * BK * 2;           // this CTA's half of the X tile: 128 rows x 64 bf16, 128-byte swizzle
 constexpr int kABytes = BN * BK * 2;            // converted W tile: 128 rows x 64 bf16, 128-byte swizzle
 constexpr int kABufs = 4;  // converted weight blocks the converters may run ahead of the MMA
 constexpr int kTmemCols = 512;  // two accumulators of BM fp32 columns
@@ -83,7 +85,7 @@ static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converte
 template <int BITS> struct Cfg {
   static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
   static constexpr int kWBytes = BN * kRowBytes;         // packed W tile
-  static constexpr int kStages = 3;                      // TMA stages in flight (X/S tile + packed W tile)
+  static constexpr int kStages = 4;                      // TMA stages in flight (X/S half tile + packed W tile)
   static constexpr int kOffX = 0;
   static constexpr int kOffW = kOffX + kStages * kXBytes;
   static constexpr int kOffA = (kOffW + kStages * kWBytes + 1023) / 1024 * 1024;
@@ -94,8 +96,8 @@ template <int BITS> struct Cfg {
   static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
   static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
   // barriers: tma_full, tma_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
-  //           sc_full, scb_full[2], scb_empty[2], bias_full, bias_empty, mma_done[2]
-  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 2 + 2;
+  //           sc_full, scb_full[2], scb_empty[2], bias_full, bias_empty, mma_done[2], pair_full[kPairRing]
+  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 2 + 2 + kPairRing;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;  // tmem address, abort flag
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -110,7 +112,7 @@ struct Params {
   float *Y;
   int64_t ldy;
   int M, N, G, NBB;
-  int tiles_n, tiles;  // 128-channel tiles per 256-row band; tiles in all
+  int tiles_n, tiles;  // 256-channel tiles per 256-row band; tiles in all
   int *status;
   uint64_t budget_ns;
 };
@@ -144,12 +146,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem]^T on the CTA pair: issued by the first CTA; A's 256
+// rows are the two CTAs' 128-row halves and B's N columns their two halves, both at the
+// same shared-memory offsets in either CTA; each CTA's tensor memory receives its rows
+__device__ __forceinline__ void mma_bf16_ss2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -158,9 +162,36 @@ __device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, u
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
+// one arrival, once this thread's earlier MMAs are complete, on the barrier at `bar`'s
+// offset in each CTA of the pair named by `mask` (bit r: CTA rank r)
+__device__ __forceinline__ void mma_commit2(uint64_t *bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+// the shared::cluster address of the same variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_rank(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+// arrive (release at cluster scope) on a barrier of another CTA of the cluster
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -250,12 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bias_full = scb_empty + 2;
   uint64_t *bias_empty = bias_full + 1;
   uint64_t *mma_done = bias_empty + 1;
+  uint64_t *pair_full = mma_done + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G, KB = p.G + p.NBB;
   const uint64_t budget = p.budget_ns;
+  // the CTA pair: rank 0 issues the MMAs for both; each CTA stages its own 128 channels
+  // of W and its own 128 rows of X and receives its 128 channels of the accumulator
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) { mbar_init(&tma_full[i], 1); mbar_init(&tma_empty[i], 1 + kConvThreads); }
@@ -265,10 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kEpiThreads);
+      // the first CTA's epilogue threads, and one arrival per epilogue warp of the second
+      mbar_init(&acc_empty[i], kEpiThreads + kEpiWarps);
       mbar_init(&scb_full[i], 1);
       mbar_init(&scb_empty[i], kConvThreads);
     }
+    for (int i = 0; i < kPairRing; ++i) mbar_init(&pair_full[i], 1);
     for (int i = 0; i < kScStages; ++i) mbar_init(&sc_full[i], kConvThreads);
     mbar_init(bias_full, 1);
     mbar_init(bias_empty, kConvThreads);
@@ -282,11 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.sc_tma) prefetch_tmap(&tmSc);
     if (p.bi_tma) prefetch_tmap(&tmBi);
   }
+  // both CTAs are running and their barriers initialised before either allocates tensor
+  // memory for the pair or arrives on the other's barriers
+  cluster_sync_all();
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+    // one warp of each CTA of the pair allocates, collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -303,8 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int g = 0, box = 0, tj = 0, bias_sets = 0;
       bool alive = true;
-      for (int t = blockIdx.x; t < p.tiles && alive; t += gridDim.x, ++tj) {
-        const int n0 = (t % p.tiles_n) * BN, m0 = (t / p.tiles_n) * BM;
+      for (int t = pair; t < p.tiles && alive; t += npairs, ++tj) {
+        // this CTA's channels and rows of X of tile t
+        const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN, m0 = (t / p.tiles_n) * BM + (int)rank * BMH;
         if (p.bi_tma) {
           // every bias of the tile's channels, once per tile (read only by its bias
           // blocks), after the previous tile's bias blocks are converted
@@ -358,20 +402,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers
-    // The k blocks of this CTA (all tiles, main and bias blocks) alternate between the
+    // ------------------------------------------------------------ MMA issuers (first CTA)
+    // The k blocks of the pair (all tiles, main and bias blocks) alternate between the
     // two issuers and the two accumulators by their running index g: issuer par takes
     // g % 2 == par into accumulator par.  A main block is one use of the accumulator;
     // the bias blocks of a tile that fall to one issuer chain into one use (so each
     // accumulator holds half of the bias contraction).  Strict alternation keeps each
     // issuer at most one block ahead of the other, so no wait is ever more than one
-    // phase ahead of a barrier's last completion.
+    // phase ahead of a barrier's last completion.  A block is issued once both CTAs
+    // have staged their halves: this CTA's own barriers, and pair_full, on which the
+    // second CTA's relay reports its halves.  Each commit arrives on the barrier at the
+    // same offset in both CTAs (mask 0b11).
+    // ------------------------------------------------------------ relay (second CTA)
+    // Warp 1 waits, block by block, for this CTA's X (or S) half and converted W tile
+    // and reports them on the first CTA's pair_full.
     const int par = warp - 1;
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BN, BM);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16(2 * BN, BM);
       bool any = false, alive = true;
-      int g = 0, uses = 0;  // k blocks of this CTA so far; uses of accumulator par so far
-      for (int t = blockIdx.x; t < p.tiles && alive; t += gridDim.x) {
+      int g = 0, uses = 0;  // k blocks of the pair so far; uses of accumulator par so far
+      for (int t = pair; t < p.tiles && alive; t += npairs) {
         const int g0 = g;
         // this issuer's first and last bias block of the tile
         const int kb_first = G + ((g0 + G) % 2 == par ? 0 : 1);
@@ -380,14 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((g & 1) != par) continue;
           const int s = g % C::kStages, ab = g % kABufs;
           if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
-              !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag)) {
+              !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag) ||
+              !mbar_wait_bounded(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget, abort_flag)) {
             give_up();
             alive = false;
             break;
           }
           const bool opens = kb < G || kb == kb_first;   // a new use of the accumulator
           const bool closes = kb < G || kb == kb_last;
-          if (opens) {  // the epilogue has read the accumulator's last use
+          if (opens) {  // both CTAs' epilogues have read the accumulator's last use
             if (!mbar_wait_bounded(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
               give_up();
               alive = false;
@@ -401,20 +452,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t acc = (kk > 0 || !opens) ? 1u : 0u;
-            mma_bf16_ss(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
+            mma_bf16_ss2(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
           }
           any = true;
-          mma_commit(&tma_empty[s]);
-          mma_commit(&a_empty[ab]);
+          mma_commit2(&tma_empty[s], 3);
+          mma_commit2(&a_empty[ab], 3);
           if (closes) {
-            mma_commit(&acc_full[par]);
+            mma_commit2(&acc_full[par], 3);
             ++uses;
           }
         }
       }
       if (any) {
-        mma_commit(&mma_done[par]);
+        mma_commit2(&mma_done[par], 1);
         (void)mbar_wait_bounded(&mma_done[par], 0u, kDrainBudgetNs, nullptr);
+      }
+    } else if (lane == 0 && par == 0) {
+      const uint32_t pf0 = mapa_rank(pair_full, 0);
+      bool alive = true;
+      int g = 0;
+      for (int t = pair; t < p.tiles && alive; t += npairs) {
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % C::kStages, ab = g % kABufs;
+          if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
+              !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag)) {
+            give_up();
+            alive = false;
+            break;
+          }
+          mbar_arrive_cluster(pf0 + (uint32_t)((g % kPairRing) * 8));
+        }
       }
     }
   } else if (warp < kEpiWarp0) {
@@ -429,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sw = (uint32_t)(ct & 7);
     bool alive = true;
     int g = 0, h = 0, box = 0, tj = 0;  // k blocks, main blocks, scale boxes, tiles
-    for (int t = blockIdx.x; t < p.tiles && alive; t += gridDim.x, ++tj) {
-      const int n = (t % p.tiles_n) * BN + ct;
+    for (int t = pair; t < p.tiles && alive; t += npairs, ++tj) {
+      const int n = (t % p.tiles_n) * (2 * BN) + (int)rank * BN + ct;
       const bool nvalid = n < p.N;
       const uint16_t *srow = p.scales + (size_t)(nvalid ? n : 0) * G;
       const uint16_t *brow = p.biases + (size_t)(nvalid ? n : 0) * G;
@@ -563,8 +630,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     int h = 0;             // main blocks so far
     int g0 = 0;            // running index of the tile's first k block (as the issuers count)
     bool ok = true;
-    for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, g0 += KB) {
-      const int n0 = (t % p.tiles_n) * BN, m0 = (t / p.tiles_n) * BM;
+    // an accumulator use is read: every thread of the first CTA arrives on its
+    // acc_empty, the second CTA's warps once each (after all their lanes' loads)
+    const uint32_t acc_empty0 = mapa_rank(acc_empty, 0);
+    auto release = [&](int buf) {
+      tc_fence_before();
+      if (leader) {
+        mbar_arrive(&acc_empty[buf]);
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)(buf * 8));
+      }
+    };
+    for (int t = pair; t < p.tiles && ok; t += npairs, g0 += KB) {
+      // this CTA's 128 channels; the accumulator holds all 256 rows of the tile
+      const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN, m0 = (t / p.tiles_n) * BM;
       float y[CW];
 #pragma unroll
       for (int i = 0; i < CW; ++i) y[i] = 0.0f;
@@ -594,8 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ffma2(y[8 * (ch + u) + 2 * i], y[8 * (ch + u) + 2 * i + 1], sv, sv, __uint_as_float(r[u][2 * i]),
                     __uint_as_float(r[u][2 * i + 1]));
         }
-        tc_fence_before();
-        mbar_arrive(&acc_empty[buf]);
+        release(buf);
         ++uses[buf];
       }
       if (!ok) break;
@@ -621,8 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) y[8 * ch + i] = __fadd_rn(y[8 * ch + i], __uint_as_float(r[i]));
         }
-        tc_fence_before();
-        mbar_arrive(&acc_empty[buf]);
+        release(buf);
         ++uses[buf];
       }
       if (!ok) break;
@@ -638,11 +716,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // neither CTA leaves (or frees the pair's tensor memory) while the other may still
+  // read its shared memory, write its barriers or run MMAs into its tensor memory
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                  : "memory");
   }
 }
@@ -758,13 +839,13 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   const int G = w->k / 64;
   CUtensorMap tmX, tmW, tmS, tmSc, tmBi;
   if (!make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)w->k, (uint64_t)m, (uint64_t)ldx * 2, pg::BK,
-                pg::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+                pg::BMH, CU_TENSOR_MAP_SWIZZLE_128B))
     return QL_ERR_CUDA;
   if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, w->wq, (uint64_t)w->k * BITS / 32, (uint64_t)w->n,
                 (uint64_t)w->k * BITS / 8, pg::BK * BITS / 32, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
     return QL_ERR_CUDA;
   if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, (uint64_t)(3 * G), (uint64_t)m, (uint64_t)lds * 2,
-                pg::BK, pg::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+                pg::BK, pg::BMH, CU_TENSOR_MAP_SWIZZLE_128B))
     return QL_ERR_CUDA;
   // scales/biases as TMA boxes of 8 groups when their rows are 16-byte aligned
   const bool sb_ok = (G % 8) == 0 && (reinterpret_cast<uintptr_t>(w->scales) & 15) == 0 &&
@@ -798,11 +879,27 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   p.NBB = (int)(lds / pg::BK);
   p.status = status;
   p.budget_ns = wait_budget_ns();
-  p.tiles_n = (w->n + pg::BN - 1) / pg::BN;
+  p.tiles_n = (w->n + 2 * pg::BN - 1) / (2 * pg::BN);
   p.tiles = p.tiles_n * ((m + pg::BM - 1) / pg::BM);
-  const int grid = p.tiles < sm_count() ? p.tiles : sm_count();  // persistent: one CTA per SM
-  pg::pgemm_kernel<BITS><<<grid, pg::kThreads, C::kAlloc, st>>>(tmX, tmW, tmS, tmSc, tmBi, p);
-  if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+  // persistent: one CTA pair per two SMs, as a cluster of two
+  const int pairs_max = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
+  const int pairs = p.tiles < pairs_max ? p.tiles : pairs_max;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.blockDim = dim3((unsigned)pg::kThreads);
+  cfg.dynamicSmemBytes = (size_t)C::kAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, pg::pgemm_kernel<BITS>, tmX, tmW, tmS, tmSc, tmBi, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return QL_ERR_LAUNCH;
+  }
   return QL_OK;
 }
 
