@@ -431,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = g % C::kStages, ab = g % kABufs;
           if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
               !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag) ||
-              !mbar_wait_bounded(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget, abort_flag)) {
+              !mbar_wait_bounded_cluster(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget,
+                                         abort_flag)) {
             give_up();
             alive = false;
             break;
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool opens = kb < G || kb == kb_first;   // a new use of the accumulator
           const bool closes = kb < G || kb == kb_last;
           if (opens) {  // both CTAs' epilogues have read the accumulator's last use
-            if (!mbar_wait_bounded(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
+            if (!mbar_wait_bounded_cluster(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
               give_up();
               alive = false;
               break;
