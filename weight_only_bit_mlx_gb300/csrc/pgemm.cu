@@ -179,9 +179,13 @@ __device__ __forceinline__ uint32_t mapa_rank(const void *p, uint32_t rank) {
   return r;
 }
 
-// arrive (release at cluster scope) on a barrier of another CTA of the cluster
+// arrive on a barrier of another CTA of the cluster, with the default semantics
+// (release at CTA scope): what the arrival publishes is tensor-memory reads ordered by
+// tcgen05.fence, or shared-memory tiles whose completion this thread observed; a
+// cluster-scope release would also wait for the thread's outstanding global stores
+// (the epilogue's output rows)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -431,8 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = g % C::kStages, ab = g % kABufs;
           if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
               !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag) ||
-              !mbar_wait_bounded_cluster(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget,
-                                         abort_flag)) {
+              !mbar_wait_bounded(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget, abort_flag)) {
             give_up();
             alive = false;
             break;
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool opens = kb < G || kb == kb_first;   // a new use of the accumulator
           const bool closes = kb < G || kb == kb_last;
           if (opens) {  // both CTAs' epilogues have read the accumulator's last use
-            if (!mbar_wait_bounded_cluster(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
+            if (!mbar_wait_bounded(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
               give_up();
               alive = false;
               break;
