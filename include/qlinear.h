@@ -164,6 +164,36 @@ int qlinear_pgemm_noalloc(const ql_weight *w, const uint16_t *X, int32_t m, int6
                           int64_t ldy, void *stream);
 
 /*
+ * qlinear_pgemm_swiglu - the prompt GEMM of the FFN's up projection (w3) with the SwiGLU
+ * as its epilogue: H[m][i] = bf16(silu(A[m][i]) * c[m][i]), c = X w3^T computed exactly as
+ * qlinear_pgemm computes it and A the gate projection's output (qlinear_pgemm with w1).
+ * [P1696] "What it adds" (decode fuses w1 + w3 + SwiGLU; the prompt GEMM); [P1514] "What
+ * changes" (paired FFN projections keep their retained rounding boundaries: h is bf16).
+ * Bit-equal to qswiglu(A, qlinear_pgemm(w3, X)); c is never written to memory.
+ *   X: bf16 [m, ldx] (16-byte aligned, ldx % 8 == 0); A: float [m, lda] (lda >= n);
+ *   H: bf16 bits [m, ldh] (ldh >= n).  m may be 0 (nothing enqueued).  Scratch and errors
+ *   as qlinear_pgemm.
+ */
+int qlinear_pgemm_swiglu(const ql_weight *w3, const uint16_t *X, int32_t m, int64_t ldx,
+                         const float *A, int64_t lda, uint16_t *H, int64_t ldh, void *stream);
+
+/*
+ * qlinear_pgemm_resid_norm - the prompt GEMM of w2 or o with the post-add / next-norm
+ * step: resid[m][i] <- bf16(resid[m][i] + y[m][i]) in the GEMM's epilogue (y = X w^T as
+ * qlinear_pgemm computes it, never written to memory), then out[m][i] =
+ * bf16(r'_i / sqrt(mean_i r'_i^2 + eps) * gamma_i) from the stored r' by the norm kernel of
+ * qresid_rmsnorm.  [P1514] "What changes" (post-add/next-norm fusion with the retained
+ * rounding boundaries); [P1696] "What it adds" (the prompt GEMM).  Both resid and out are
+ * bit-equal to qlinear_pgemm followed by qresid_rmsnorm.
+ *   X: bf16 [m, ldx]; resid: bf16 bits [m, ldr] (ldr >= n), read and overwritten; gamma:
+ *   bf16 [n]; out: bf16 bits [m, ldo] (ldo >= n, must not overlap resid).  m may be 0.
+ *   Errors as qlinear_pgemm, plus QL_ERR_SHAPE for eps < 0.
+ */
+int qlinear_pgemm_resid_norm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx,
+                             uint16_t *resid, int64_t ldr, const uint16_t *gamma, float eps,
+                             uint16_t *out, int64_t ldo, void *stream);
+
+/*
  * qswiglu - h[r][i] = bf16(silu(a[r][i]) * c[r][i]) (float32 math, nearest-even
  * rounding): the SwiGLU of qffn_swiglu_mv on its own, used as its "fusion off" control.
  *   a, c: float [rows, lda]; h: bf16 bits [rows, ldh]; rows >= 1, n >= 1.

@@ -166,3 +166,25 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
                        env={**os.environ, "PYTHONPATH": str(tmp_path)}, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0
     assert "ImportError" in r.stderr and "is not built" in r.stderr
+
+
+def test_fused_prompt_gemm_epilogues_reject_bad_arguments_on_host(q):
+    w = _w(q)
+    L = q.LIB
+    P = 0x40000
+    sw = L.qlinear_pgemm_swiglu
+    assert sw(ctypes.byref(w), P, 0, 128, 0, 64, 0, 64, None) == q.QL_OK  # an empty window enqueues nothing
+    assert sw(ctypes.byref(w), P, -1, 128, P, 64, P, 64, None) == q.QL_ERR_SHAPE
+    assert sw(ctypes.byref(w), P, 4, 128, 0, 64, P, 64, None) == q.QL_ERR_NULL
+    assert sw(ctypes.byref(w), P, 4, 128, P, 64, 0, 64, None) == q.QL_ERR_NULL
+    assert sw(ctypes.byref(w), P, 4, 128, P, 32, P, 64, None) == q.QL_ERR_ALIGN
+    assert sw(ctypes.byref(w), P, 4, 128, P, 64, P + 1, 64, None) == q.QL_ERR_ALIGN
+    assert sw(ctypes.byref(w), P + 8, 4, 128, P, 64, P, 64, None) == q.QL_ERR_ALIGN
+    rn = L.qlinear_pgemm_resid_norm
+    assert rn(ctypes.byref(w), P, 0, 128, 0, 64, 0, 1e-5, 0, 64, None) == q.QL_OK
+    assert rn(ctypes.byref(w), P, 4, 128, 0, 64, P, 1e-5, P, 64, None) == q.QL_ERR_NULL
+    assert rn(ctypes.byref(w), P, 4, 128, P, 64, P, -1.0, P, 64, None) == q.QL_ERR_SHAPE
+    assert rn(ctypes.byref(w), P, 4, 128, P, 32, P, 1e-5, P, 64, None) == q.QL_ERR_ALIGN
+    assert rn(ctypes.byref(w), P, 4, 120, P, 64, P, 1e-5, P, 64, None) == q.QL_ERR_ALIGN
+    w5 = _w(q, bits=5)
+    assert rn(ctypes.byref(w5), P, 4, 128, P, 64, P, 1e-5, P, 64, None) == q.QL_ERR_BITS

@@ -277,6 +277,43 @@ int qlinear_pgemm_noalloc(const ql_weight *w, const uint16_t *X, int32_t m, int6
   return pgemm_run_noalloc(w, X, m, ldx, Y, ldy, static_cast<cudaStream_t>(stream), status);
 }
 
+// The prompt GEMM of the FFN's up projection with the SwiGLU as its epilogue.
+int qlinear_pgemm_swiglu(const ql_weight *w3, const uint16_t *X, int32_t m, int64_t ldx, const float *A, int64_t lda,
+                         uint16_t *H, int64_t ldh, void *stream) {
+  int e = check_weight(w3);
+  if (e) return e;
+  if (m < 0) return QL_ERR_SHAPE;
+  if (m == 0) return QL_OK;
+  if (X == nullptr || A == nullptr || H == nullptr) return QL_ERR_NULL;
+  if (!aligned(X, 16) || (ldx % 8) != 0 || ldx < w3->k || lda < w3->n || ldh < w3->n || !aligned(A, 4) ||
+      !aligned(H, 2))
+    return QL_ERR_ALIGN;
+  int *status = nullptr;
+  if ((e = device_setup(&status))) return e;
+  PgEpilogue epi = {kPgSwiglu, A, lda, H, ldh};
+  return pgemm_run(w3, X, m, ldx, nullptr, 0, static_cast<cudaStream_t>(stream), status, &epi);
+}
+
+// The prompt GEMM of w2 / o with the post-add as its epilogue, then the next-norm.
+int qlinear_pgemm_resid_norm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, uint16_t *resid,
+                             int64_t ldr, const uint16_t *gamma, float eps, uint16_t *out, int64_t ldo, void *stream) {
+  int e = check_weight(w);
+  if (e) return e;
+  if (m < 0) return QL_ERR_SHAPE;
+  if (m == 0) return QL_OK;
+  if (X == nullptr || resid == nullptr || gamma == nullptr || out == nullptr) return QL_ERR_NULL;
+  if (!(eps >= 0.0f)) return QL_ERR_SHAPE;
+  if (!aligned(X, 16) || (ldx % 8) != 0 || ldx < w->k || ldr < w->n || ldo < w->n || !aligned(resid, 2) ||
+      !aligned(out, 2) || !aligned(gamma, 2))
+    return QL_ERR_ALIGN;
+  int *status = nullptr;
+  if ((e = device_setup(&status))) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PgEpilogue epi = {kPgResid, nullptr, 0, resid, ldr};
+  if ((e = pgemm_run(w, X, m, ldx, nullptr, 0, st, status, &epi))) return e;
+  return launch_status(launch_resid_rmsnorm(nullptr, 0, resid, ldr, m, w->n, gamma, eps, out, ldo, st));
+}
+
 int qswiglu(const float *a, const float *c, int32_t rows, int32_t n, int64_t lda, uint16_t *h, int64_t ldh,
             void *stream) {
   if (a == nullptr || c == nullptr || h == nullptr) return QL_ERR_NULL;

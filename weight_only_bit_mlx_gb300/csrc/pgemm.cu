@@ -111,6 +111,11 @@ struct Params {
   int bi_tma;  // biases arrive as TMA boxes too (additionally k <= 64 * kBiasG)
   float *Y;
   int64_t ldy;
+  int epi;         // kPgStore / kPgSwiglu / kPgResid
+  const float *A;  // kPgSwiglu: the gate projection's output
+  int64_t lda;
+  uint16_t *H;     // kPgSwiglu: output; kPgResid: the residual, read and overwritten
+  int64_t ldh;
   int M, N, G, NBB;
   int tiles_n, tiles;  // 256-channel tiles per 256-row band; tiles in all
   int *status;
@@ -712,10 +717,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = n0 + ch_row;
       if (n < p.N) {
         const int mb = m0 + slice * CW;
-        float *ycol = p.Y + (size_t)mb * p.ldy + n;
+        if (p.epi == kPgStore) {
+          float *ycol = p.Y + (size_t)mb * p.ldy + n;
 #pragma unroll
-        for (int i = 0; i < CW; ++i)
-          if (mb + i < p.M) ycol[(size_t)i * p.ldy] = y[i];
+          for (int i = 0; i < CW; ++i)
+            if (mb + i < p.M) ycol[(size_t)i * p.ldy] = y[i];
+        } else if (p.epi == kPgSwiglu) {
+          // the SwiGLU of the FFN: h = bf16(silu(a) * c), c = this output
+          const float *acol = p.A + (size_t)mb * p.lda + n;
+          uint16_t *hcol = p.H + (size_t)mb * p.ldh + n;
+#pragma unroll 8
+          for (int i = 0; i < CW; ++i)
+            if (mb + i < p.M) hcol[(size_t)i * p.ldh] = swiglu_bf16(acol[(size_t)i * p.lda], y[i]);
+        } else {
+          // the post-add of the residual stream: r' = bf16(r + y), stored in place
+          uint16_t *rcol = p.H + (size_t)mb * p.ldh + n;
+#pragma unroll 8
+          for (int i = 0; i < CW; ++i)
+            if (mb + i < p.M) {
+              uint16_t *rp = rcol + (size_t)i * p.ldh;
+              *rp = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(*rp), y[i]));
+            }
+        }
       }
     }
   }
@@ -838,7 +861,7 @@ static int sm_count() {
 
 template <int BITS>
 static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
-                        const uint16_t *S, int64_t lds, cudaStream_t st, int *status) {
+                        const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi) {
   using C = pg::Cfg<BITS>;
   const int G = w->k / 64;
   CUtensorMap tmX, tmW, tmS, tmSc, tmBi;
@@ -877,6 +900,11 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   p.bi_tma = bi_tma ? 1 : 0;
   p.Y = Y;
   p.ldy = ldy;
+  p.epi = epi ? epi->mode : kPgStore;
+  p.A = epi ? epi->a : nullptr;
+  p.lda = epi ? epi->lda : 0;
+  p.H = epi ? epi->h : nullptr;
+  p.ldh = epi ? epi->ldh : 0;
   p.M = m;
   p.N = w->n;
   p.G = G;
@@ -957,14 +985,14 @@ int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx,
   pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   switch (w->bits) {
-    case 4: return launch_pgemm<4>(w, X, m, ldx, Y, ldy, S, lds, st, status);
-    case 6: return launch_pgemm<6>(w, X, m, ldx, Y, ldy, S, lds, st, status);
-    default: return launch_pgemm<8>(w, X, m, ldx, Y, ldy, S, lds, st, status);
+    case 4: return launch_pgemm<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
+    case 6: return launch_pgemm<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
+    default: return launch_pgemm<8>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
   }
 }
 
 int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy, cudaStream_t st,
-              int *status) {
+              int *status, const PgEpilogue *epi) {
   const int G = w->k / 64;
   const int64_t lds = ((3 * (int64_t)G + 63) / 64) * 64;  // row pitch of the split sums (elements)
   uint16_t *S = static_cast<uint16_t *>(scratch_get((size_t)m * lds * 2));
@@ -975,9 +1003,9 @@ int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *
   pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   switch (w->bits) {
-    case 4: return launch_pgemm<4>(w, X, m, ldx, Y, ldy, S, lds, st, status);
-    case 6: return launch_pgemm<6>(w, X, m, ldx, Y, ldy, S, lds, st, status);
-    default: return launch_pgemm<8>(w, X, m, ldx, Y, ldy, S, lds, st, status);
+    case 4: return launch_pgemm<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    case 6: return launch_pgemm<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    default: return launch_pgemm<8>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
   }
 }
 

@@ -144,6 +144,9 @@ __device__ __forceinline__ float block_sum_fixed(float ss, float *wsum) {
   return tot;
 }
 
+// kAdd: r' = bf16(r + y) is stored first; otherwise r' is the stored residual as it is
+// (the post-add already done by the producing GEMM's epilogue) and y is not read.
+template <bool kAdd>
 __global__ void __launch_bounds__(kNormThreads) resid_rmsnorm_vec_kernel(const float *y, int64_t ldy, uint16_t *resid,
                                                                        int64_t ldr, int n, const uint16_t *gamma,
                                                                        float eps, uint16_t *out, int64_t ldo) {
@@ -158,22 +161,29 @@ __global__ void __launch_bounds__(kNormThreads) resid_rmsnorm_vec_kernel(const f
   // squares to ss in element order
   auto add_chunk = [&](int c, float &ss) -> uint4 {
     const uint4 rv = *reinterpret_cast<const uint4 *>(rr + 8 * c);
-    const float4 y0 = *reinterpret_cast<const float4 *>(yr + 8 * c);
-    const float4 y1 = *reinterpret_cast<const float4 *>(yr + 8 * c + 4);
     const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-    const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    float yv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    if constexpr (kAdd) {
+      const float4 y0 = *reinterpret_cast<const float4 *>(yr + 8 * c);
+      const float4 y1 = *reinterpret_cast<const float4 *>(yr + 8 * c + 4);
+      yv[0] = y0.x; yv[1] = y0.y; yv[2] = y0.z; yv[3] = y0.w;
+      yv[4] = y1.x; yv[5] = y1.y; yv[6] = y1.z; yv[7] = y1.w;
+    }
     uint32_t nw[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint16_t lo = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(rw[e] & 0xFFFFu), yv[2 * e]));
-      const uint16_t hi = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(rw[e] >> 16), yv[2 * e + 1]));
+      uint16_t lo = (uint16_t)(rw[e] & 0xFFFFu), hi = (uint16_t)(rw[e] >> 16);
+      if constexpr (kAdd) {
+        lo = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(lo), yv[2 * e]));
+        hi = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(hi), yv[2 * e + 1]));
+      }
       const float vl = bf16_to_f32(lo), vh = bf16_to_f32(hi);
       ss = __fmaf_rn(vl, vl, ss);
       ss = __fmaf_rn(vh, vh, ss);
       nw[e] = (uint32_t)lo | ((uint32_t)hi << 16);
     }
     const uint4 nv = make_uint4(nw[0], nw[1], nw[2], nw[3]);
-    *reinterpret_cast<uint4 *>(rr + 8 * c) = nv;
+    if constexpr (kAdd) *reinterpret_cast<uint4 *>(rr + 8 * c) = nv;
     return nv;
   };
   uint4 keep[kVecKeep];
@@ -210,6 +220,7 @@ __global__ void __launch_bounds__(kNormThreads) resid_rmsnorm_vec_kernel(const f
 }
 
 // Scalar form (any n, strides and alignment): the same arithmetic one element at a time.
+template <bool kAdd>
 __global__ void __launch_bounds__(kNormThreads) resid_rmsnorm_kernel(const float *y, int64_t ldy, uint16_t *resid,
                                                                    int64_t ldr, int n, const uint16_t *gamma, float eps,
                                                                    uint16_t *out, int64_t ldo) {
@@ -221,8 +232,11 @@ __global__ void __launch_bounds__(kNormThreads) resid_rmsnorm_kernel(const float
   uint16_t *rr = resid + (size_t)r * ldr;
   float ss = 0.0f;
   for (int j = threadIdx.x; j < n; j += kNormThreads) {
-    const uint16_t nb = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(rr[j]), yr[j]));
-    rr[j] = nb;
+    uint16_t nb = rr[j];
+    if constexpr (kAdd) {
+      nb = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(nb), yr[j]));
+      rr[j] = nb;
+    }
     const float v = bf16_to_f32(nb);
     ss = __fmaf_rn(v, v, ss);
   }
@@ -257,10 +271,14 @@ cudaError_t launch_resid_rmsnorm(const float *y, int64_t ldy, uint16_t *resid, i
                                  const uint16_t *gamma, float eps, uint16_t *out, int64_t ldo, cudaStream_t st) {
   void *args[] = {&y, &ldy, &resid, &ldr, &n, &gamma, &eps, &out, &ldo};
   auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0; };
-  const bool vec = (n % 8) == 0 && (ldy % 4) == 0 && (ldr % 8) == 0 && (ldo % 8) == 0 && a16(y) && a16(resid) &&
-                   a16(out) && a16(gamma);
-  const void *fn = vec ? reinterpret_cast<const void *>(&resid_rmsnorm_vec_kernel)
-                       : reinterpret_cast<const void *>(&resid_rmsnorm_kernel);
+  // y == nullptr: the residual already holds r' (added by the GEMM's epilogue); normalise only
+  const bool add = y != nullptr;
+  const bool vec = (n % 8) == 0 && (!add || ((ldy % 4) == 0 && a16(y))) && (ldr % 8) == 0 && (ldo % 8) == 0 &&
+                   a16(resid) && a16(out) && a16(gamma);
+  const void *fn = add ? (vec ? reinterpret_cast<const void *>(&resid_rmsnorm_vec_kernel<true>)
+                              : reinterpret_cast<const void *>(&resid_rmsnorm_kernel<true>))
+                       : (vec ? reinterpret_cast<const void *>(&resid_rmsnorm_vec_kernel<false>)
+                              : reinterpret_cast<const void *>(&resid_rmsnorm_kernel<false>));
   return launch_pdl(fn, dim3((unsigned)rows), dim3(kNormThreads), args, st);
 }
 

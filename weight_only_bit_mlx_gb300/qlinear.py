@@ -57,6 +57,8 @@ def _load() -> ctypes.CDLL:
         "qattn_proj_mv": (ctypes.c_int, [W, W, W, W, P, I32, I64, P, P, P, P, P]),
         "qlinear_pgemm": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
         "qlinear_pgemm_noalloc": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
+        "qlinear_pgemm_swiglu": (ctypes.c_int, [W, P, I32, I64, P, I64, P, I64, P]),
+        "qlinear_pgemm_resid_norm": (ctypes.c_int, [W, P, I32, I64, P, I64, P, ctypes.c_float, P, I64, P]),
         "qswiglu": (ctypes.c_int, [P, P, I32, I32, I64, P, I64, P]),
         "qattn_qknorm_rope_kv": (ctypes.c_int, [P, I64, P, I64, P, I64, I32, I32, I32, I32, I32, ctypes.c_float,
                                                 ctypes.c_float, P, P, P, P, I64, P, P, I32, P]),
@@ -205,6 +207,44 @@ def qlinear_pgemm_noalloc(w: QWeight, X: torch.Tensor, Y: torch.Tensor, stream=N
     _check(LIB.qlinear_pgemm_noalloc(ctypes.byref(w.c), X.data_ptr(), int(X.shape[0]), X.stride(0), Y.data_ptr(),
                                      Y.stride(0), _stream(stream)), "qlinear_pgemm_noalloc")
     return Y
+
+
+def _prompt(X: torch.Tensor, k: int) -> int:
+    if X.dtype != torch.bfloat16 or not X.is_cuda or X.dim() != 2 or X.shape[1] != k or X.stride(1) != 1:
+        raise ValueError(f"X must be a CUDA bfloat16 [m, {k}] tensor with unit column stride")
+    return int(X.shape[0])
+
+
+def qlinear_pgemm_swiglu(w3: QWeight, X: torch.Tensor, A: torch.Tensor, H: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """H = bf16(silu(A) * (X w3^T)): the up-projection prompt GEMM with the SwiGLU as its
+    epilogue.  A: float32 [m, n] (the gate projection's output)."""
+    m = _prompt(X, w3.k)
+    A = _rows2d(A, torch.float32, "A")
+    if tuple(A.shape) != (m, w3.n):
+        raise ValueError("A must be [m, n]")
+    if H is None:
+        H = torch.empty(m, w3.n, dtype=torch.bfloat16, device=X.device)
+    _check(LIB.qlinear_pgemm_swiglu(ctypes.byref(w3.c), X.data_ptr(), m, X.stride(0), A.data_ptr(), A.stride(0),
+                                    H.data_ptr(), H.stride(0), _stream(stream)), "qlinear_pgemm_swiglu")
+    return H
+
+
+def qlinear_pgemm_resid_norm(w: QWeight, X: torch.Tensor, resid: torch.Tensor, gamma: torch.Tensor, eps: float,
+                             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """resid <- bf16(resid + X w^T) in the prompt GEMM's epilogue; returns
+    out = bf16(rmsnorm(resid) * gamma).  resid: bfloat16 [m, n]; gamma: bfloat16 [n]."""
+    m = _prompt(X, w.k)
+    r = _rows2d(resid, torch.bfloat16, "resid")
+    if tuple(r.shape) != (m, w.n) or gamma.dtype != torch.bfloat16 or gamma.numel() != w.n or \
+            not gamma.is_contiguous():
+        raise ValueError("resid must be [m, n] and gamma a contiguous bfloat16 [n]")
+    if out is None:
+        out = torch.empty(m, w.n, dtype=torch.bfloat16, device=X.device)
+    _check(LIB.qlinear_pgemm_resid_norm(ctypes.byref(w.c), X.data_ptr(), m, X.stride(0), r.data_ptr(), r.stride(0),
+                                        gamma.data_ptr(), float(eps), out.data_ptr(), out.stride(0),
+                                        _stream(stream)), "qlinear_pgemm_resid_norm")
+    return out
 
 
 def qswiglu(a: torch.Tensor, c: torch.Tensor, h: torch.Tensor | None = None, stream=None) -> torch.Tensor:
