@@ -374,6 +374,9 @@ class Sweep:
         self.Pq = torch.empty(PROMPT, D_MODEL, device=dev)
         self.Pkv = torch.empty(PROMPT, D_KV, device=dev)
         self.Patt = rnd(PROMPT, D_MODEL)
+        self.Presid = rnd(PROMPT, D_MODEL)      # the residual stream of the prompt rows
+        self.Pnorm = torch.empty(PROMPT, D_MODEL, dtype=torch.bfloat16, device=dev)  # next layer's input
+        self.pgamma = (torch.rand(D_MODEL, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
         self.gemm_events = []  # (start, stop, flops, (m, n, k)) of the timed pgemm calls
         if with_post:
             self._post_buffers()
@@ -475,13 +478,42 @@ class Sweep:
         else:
             self.q.qlinear_pgemm(w, Xin, Y)
 
-    def prefill_pass(self, timed=False, lo=0, hi=PROMPT):
-        """Rows lo..hi-1 of the prompt through every linear (one pgemm per linear; SwiGLU
-        between w1/w3 and w2).  Returns the number of launches."""
-        W, n = self.W, 0
+    def _timed_call(self, fn, timed, flops, tag):
+        import torch
+        if not timed:
+            fn()
+            return
+        st = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        fn()
+        e1.record(st)
+        self.gemm_events.append((e0, e1, flops, tag))
+
+    def prefill_pass(self, timed=False, lo=0, hi=PROMPT, fused=True, post=None):
+        """Rows lo..hi-1 of the prompt through every linear: one pgemm per linear, the
+        SwiGLU as the up projection's epilogue (fused) or as a kernel of its own, and
+        with post="fused" / "unfused" the post-add / next-norm after o and w2 (as the
+        GEMM's epilogue plus the norm, or the plain GEMM plus qresid_rmsnorm).
+        Returns the number of launches."""
+        W, n, q = self.W, 0, self.q
         X, Patt = self.X[lo:hi], self.Patt[lo:hi]
         Pa, Pc, Ph = self.Pa[lo:hi], self.Pc[lo:hi], self.Ph[lo:hi]
         Pq, Pkv, Pout = self.Pq[lo:hi], self.Pkv[lo:hi], self.Pout[lo:hi]
+        R, Rn = self.Presid[lo:hi], self.Pnorm[lo:hi]
+
+        def down(w, Xin):  # o or w2, then the post-add / next-norm if asked for
+            nonlocal n
+            if post == "fused":
+                q.qlinear_pgemm_resid_norm(w, Xin, R, self.pgamma, 1e-5, out=Rn)
+                n += 3
+            else:
+                self._pgemm(w, Xin, Pout, timed)
+                n += 2
+                if post == "unfused":
+                    q.qresid_rmsnorm(Pout, R, self.pgamma, 1e-5, out=Rn)
+                    n += 1
+
         for layer in range(N_LAYERS):
             p = f"L{layer}."
             if layer in ATTN_LAYERS:
@@ -489,13 +521,19 @@ class Sweep:
                 self._pgemm(W[p + "k"], X, Pkv, timed)
                 self._pgemm(W[p + "v"], X, Pkv, timed)
                 self._pgemm(W[p + "g"], X, Pq, timed)
-                self._pgemm(W[p + "o"], Patt, Pout, timed)
-                n += 10
+                n += 8
+                down(W[p + "o"], Patt)
             self._pgemm(W[p + "w1"], X, Pa, timed)
-            self._pgemm(W[p + "w3"], X, Pc, timed)
-            self.q.qswiglu(Pa, Pc, Ph)
-            self._pgemm(W[p + "w2"], Ph, Pout, timed)
-            n += 7
+            n += 2
+            if fused:
+                self._timed_call(lambda: q.qlinear_pgemm_swiglu(W[p + "w3"], X, Pa, Ph), timed,
+                                 2 * X.shape[0] * W[p + "w3"].n * W[p + "w3"].k, "swiglu")
+                n += 2
+            else:
+                self._pgemm(W[p + "w3"], X, Pc, timed)
+                q.qswiglu(Pa, Pc, Ph)
+                n += 3
+            down(W[p + "w2"], Ph)
         return n
 
     def prefill_windows_pass(self, win):
@@ -507,7 +545,8 @@ class Sweep:
         return n
 
     def gemm_summary(self, shape=None):
-        """(ms, flops) summed over the timed pgemm calls (of one shape if given)."""
+        """(ms, flops) summed over the timed pgemm calls (of one shape, or one tag such as
+        "swiglu" for the up projections with the SwiGLU epilogue, if given)."""
         ev = [(a, b, f) for a, b, f, sh in self.gemm_events if shape is None or sh == shape]
         return sum(a.elapsed_time(b) for a, b, _ in ev), sum(f for _, _, f in ev)
 
@@ -702,6 +741,22 @@ def run_ours(args):
                                "layer_pass_fused_tok_s_modelled": R / (layer_ms[f"layer{R}f"] * 1e-3)}
     assert q.qlinear_last_error() == q.QL_OK
 
+    # ---------------- the prefill pass with the SwiGLU as a kernel of its own, and with the
+    #                  post-add / next-norm after o and w2 (unfused, and as the GEMM's epilogue)
+    def time_pass(**kw):
+        sw.prefill_pass(**kw)
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        sw.prefill_pass(**kw)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1))
+    pf_variants = {"swiglu_separate_ms": time_pass(fused=False),
+                   "post_unfused_ms": time_pass(post="unfused"),
+                   "post_fused_ms": time_pass(post="fused")}
+    assert q.qlinear_last_error() == q.QL_OK
+
     # ---------------- end to end: host buffers in pinned memory, copies inside the timed region
     xh = torch.empty(1, D_MODEL, dtype=torch.bfloat16).pin_memory()
     xh.copy_(sw.bufs[1]["x"].cpu())
@@ -726,6 +781,8 @@ def run_ours(args):
     win_tflops = job_throughput(prefill_flops(), args.steps, win_ms, world) / 1e12
     win_wbytes = (PROMPT // WIN) * sweep_weight_bytes(bits)
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12  # per GPU, all GEMM launches of the pass
+    sw_ms, sw_flops = sw.gemm_summary("swiglu")
+    sw_tflops = sw_flops / (sw_ms * 1e-3) / 1e12 if sw_ms > 0 else None
     ffn_tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12      # per GPU, the roofline kernel's launches
     src = source_hash(["pgemm.cu", "common.cuh", "sync.cuh"])
     traffic = NCU_TRAFFIC.get(src)
@@ -755,8 +812,16 @@ def run_ours(args):
                        "ms_per_pass": d16_ms / args.steps, "bytes_per_pass": d16_bytes,
                        "tok_s_modelled": 16.0 / (d16_ms / args.steps * 1e-3)},
         "prefill": {"TFLOP/s": pf_tflops / world, "ms_per_pass": pf_ms / args.steps,
-                    "flops_per_pass": prefill_flops(), "includes": "pgemm (row-sum pre-pass + GEMM) and SwiGLU",
-                    "tok_s_modelled": PROMPT / (gemm_ms / args.steps * 1e-3)},
+                    "flops_per_pass": prefill_flops(),
+                    "includes": "pgemm (row-sum pre-pass + GEMM), the up projections with the SwiGLU as their "
+                                "epilogue (qlinear_pgemm_swiglu)",
+                    "swiglu_epilogue_TFLOP/s": sw_tflops,
+                    "tok_s_modelled": PROMPT / (pf_ms / args.steps * 1e-3),
+                    "variants_ms_per_pass": dict(pf_variants, fused_swiglu_ms=pf_ms / args.steps,
+                                                 what="one pass each after the timed region: the SwiGLU as a kernel "
+                                                      "of its own; the post-add / next-norm after o and w2 as "
+                                                      "qlinear_pgemm + qresid_rmsnorm, and as "
+                                                      "qlinear_pgemm_resid_norm (the GEMM's epilogue + the norm)")},
         "prefill_windows": {"window_rows": WIN, "windows": PROMPT // WIN,
                             "TFLOP/s": win_tflops / world, "ms_per_pass": win_ms / args.steps,
                             "launches_per_pass": launches["win"],
@@ -769,7 +834,7 @@ def run_ours(args):
                                     "layers (78 pgemm + 16 SwiGLU per window, one CUDA graph) before the next: "
                                     "every window streams every weight again (64 x the sweep's weight bytes)"},
         "tok_s_note": "modelled from the linear layers only: decode R / (decode pass time), prefill "
-                      "prompt rows / (sum of the pass's pgemm times); attention, norms and sampling excluded",
+                      "prompt rows / (prefill pass time); attention, norms and sampling excluded",
         "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm (row-sum pre-pass + tcgen05 GEMM), "
                                                   f"M={PROMPT} N={D_FF} K={D_MODEL} launches (w1, w3)",
                      "achieved": ffn_tflops, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
