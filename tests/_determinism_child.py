@@ -35,6 +35,11 @@ def main():
         out[f"qlinear_pgemm/{bits}"] = _h(q.qlinear_pgemm(w, X))
         Y = torch.empty(300, 768, device="cuda")
         out[f"qlinear_pgemm_noalloc/{bits}"] = _h(q.qlinear_pgemm_noalloc(w, X, Y))
+        A = q.qlinear_pgemm(w3, X)
+        out[f"qlinear_pgemm_swiglu/{bits}"] = _h(q.qlinear_pgemm_swiglu(w, X, A))
+        rp = q.bf16_from_bits(synth.make_bf16((300, 768), config_id=142, tensor_id=1))
+        gp = q.bf16_from_bits(synth.make_bf16((768,), 0.5, 1.5, config_id=143, tensor_id=1))
+        out[f"qlinear_pgemm_resid_norm/{bits}"] = _h(q.qlinear_pgemm_resid_norm(w, X, rp, gp, 1e-5), rp)
         r = q.bf16_from_bits(synth.make_bf16((16, 768), config_id=142))
         g = q.bf16_from_bits(synth.make_bf16((768,), 0.5, 1.5, config_id=143))
         o = q.qlinear_mv_resid_norm(w, x, r, g, 1e-5)

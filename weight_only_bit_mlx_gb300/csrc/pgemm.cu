@@ -111,7 +111,6 @@ struct Params {
   int bi_tma;  // biases arrive as TMA boxes too (additionally k <= 64 * kBiasG)
   float *Y;
   int64_t ldy;
-  int epi;         // kPgStore / kPgSwiglu / kPgResid
   const float *A;  // kPgSwiglu: the gate projection's output
   int64_t lda;
   uint16_t *H;     // kPgSwiglu: output; kPgResid: the residual, read and overwritten
@@ -263,7 +262,7 @@ __device__ __forceinline__ void convert_chunk(const uint32_t (&w)[NW], int c, ui
 // X in L2).  Every role keeps running counters across tiles (k blocks g, main blocks
 // h, scale boxes, accumulator uses), so the next tile's copies, conversions and MMAs
 // overlap this tile's epilogue.
-template <int BITS>
+template <int BITS, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     pgemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                  const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmSc,
@@ -717,22 +716,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = n0 + ch_row;
       if (n < p.N) {
         const int mb = m0 + slice * CW;
-        if (p.epi == kPgStore) {
+        if constexpr (EPI == kPgStore) {
           float *ycol = p.Y + (size_t)mb * p.ldy + n;
 #pragma unroll
           for (int i = 0; i < CW; ++i)
             if (mb + i < p.M) ycol[(size_t)i * p.ldy] = y[i];
-        } else if (p.epi == kPgSwiglu) {
+        } else if constexpr (EPI == kPgSwiglu) {
           // the SwiGLU of the FFN: h = bf16(silu(a) * c), c = this output
           const float *acol = p.A + (size_t)mb * p.lda + n;
           uint16_t *hcol = p.H + (size_t)mb * p.ldh + n;
-#pragma unroll 8
+#pragma unroll
           for (int i = 0; i < CW; ++i)
             if (mb + i < p.M) hcol[(size_t)i * p.ldh] = swiglu_bf16(acol[(size_t)i * p.lda], y[i]);
         } else {
           // the post-add of the residual stream: r' = bf16(r + y), stored in place
           uint16_t *rcol = p.H + (size_t)mb * p.ldh + n;
-#pragma unroll 8
+#pragma unroll
           for (int i = 0; i < CW; ++i)
             if (mb + i < p.M) {
               uint16_t *rp = rcol + (size_t)i * p.ldh;
@@ -859,7 +858,7 @@ static int sm_count() {
   return c;
 }
 
-template <int BITS>
+template <int BITS, int EPI>
 static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
                         const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi) {
   using C = pg::Cfg<BITS>;
@@ -888,7 +887,7 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < kMaxDev && !attr_set[dev].load(std::memory_order_relaxed)) {
-    if (cudaFuncSetAttribute(pg::pgemm_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc) !=
+    if (cudaFuncSetAttribute(pg::pgemm_kernel<BITS, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc) !=
         cudaSuccess)
       return QL_ERR_LAUNCH;
     attr_set[dev].store(true, std::memory_order_relaxed);
@@ -900,7 +899,6 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   p.bi_tma = bi_tma ? 1 : 0;
   p.Y = Y;
   p.ldy = ldy;
-  p.epi = epi ? epi->mode : kPgStore;
   p.A = epi ? epi->a : nullptr;
   p.lda = epi ? epi->lda : 0;
   p.H = epi ? epi->h : nullptr;
@@ -928,7 +926,7 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, pg::pgemm_kernel<BITS>, tmX, tmW, tmS, tmSc, tmBi, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, pg::pgemm_kernel<BITS, EPI>, tmX, tmW, tmS, tmSc, tmBi, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return QL_ERR_LAUNCH;
   }
@@ -985,9 +983,19 @@ int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx,
   pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   switch (w->bits) {
-    case 4: return launch_pgemm<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
-    case 6: return launch_pgemm<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
-    default: return launch_pgemm<8>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
+    case 4: return launch_pgemm<4, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
+    case 6: return launch_pgemm<6, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
+    default: return launch_pgemm<8, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
+  }
+}
+
+template <int BITS>
+static int launch_epi(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
+                      const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi) {
+  switch (epi ? epi->mode : kPgStore) {
+    case kPgSwiglu: return launch_pgemm<BITS, kPgSwiglu>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    case kPgResid: return launch_pgemm<BITS, kPgResid>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    default: return launch_pgemm<BITS, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
   }
 }
 
@@ -1003,9 +1011,9 @@ int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *
   pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   switch (w->bits) {
-    case 4: return launch_pgemm<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
-    case 6: return launch_pgemm<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
-    default: return launch_pgemm<8>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    case 4: return launch_epi<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    case 6: return launch_epi<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    default: return launch_epi<8>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
   }
 }
 
