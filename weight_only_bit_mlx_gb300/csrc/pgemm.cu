@@ -80,6 +80,8 @@ constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
 constexpr int kPf = 2;       // k blocks of scale/bias prefetch (no-TMA path)
 constexpr int kLdChunks = 2;  // epilogue tensor-memory loads (8 columns each) per wait
+constexpr int kEpiBatch = 8;  // rows of the fused epilogues' global loads in flight together
+constexpr int kEpiPrefetchLead = 8;  // k blocks before a tile's end at which its epilogue inputs are prefetched
 static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
 
 template <int BITS> struct Cfg {
@@ -115,6 +117,7 @@ struct Params {
   int64_t lda;
   uint16_t *H;     // kPgSwiglu: output; kPgResid: the residual, read and overwritten
   int64_t ldh;
+  int epi_pf;      // the rows the fused epilogue reads may be prefetched in 16-byte pieces
   int M, N, G, NBB;
   int tiles_n, tiles;  // 256-channel tiles per 256-row band; tiles in all
   int *status;
@@ -128,6 +131,11 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
           smem_addr(dst)),
       "l"(map), "r"(smem_addr(bar)), "r"(x), "r"(y)
       : "memory");
+}
+
+// a hint: bring `bytes` (a multiple of 16) at the 16-byte aligned global `p` into L2
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
@@ -370,6 +378,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++bias_sets;
         }
         for (int kb = 0; kb < KB; ++kb) {
+          if (EPI != kPgStore && p.epi_pf && kb == (G > kEpiPrefetchLead ? G - kEpiPrefetchLead : 0)) {
+            // the tile's rows of the fused epilogue's input (the gate output, or the
+            // residual), this CTA's channels, into L2 ahead of the tile's end
+            const int mt = (t / p.tiles_n) * BM;
+            const int nch = min(BN, p.N - n0);
+            const uint32_t esz = EPI == kPgSwiglu ? 4u : 2u;
+            const uint32_t bytes = ((uint32_t)nch * esz) & ~15u;
+            if (nch > 0 && bytes > 0) {
+              for (int r = 0; r < BM && mt + r < p.M; ++r) {
+                const void *src = EPI == kPgSwiglu
+                                      ? static_cast<const void *>(p.A + (size_t)(mt + r) * p.lda + n0)
+                                      : static_cast<const void *>(p.H + (size_t)(mt + r) * p.ldh + n0);
+                prefetch_l2_bulk(src, bytes);
+              }
+            }
+          }
           if (p.sc_tma && kb < G && (kb & 7) == 0) {
             // scales of blocks kb .. kb+7 for the tile's channels, two boxes in flight
             const int slot = box & 1;
@@ -722,20 +746,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < CW; ++i)
             if (mb + i < p.M) ycol[(size_t)i * p.ldy] = y[i];
         } else if constexpr (EPI == kPgSwiglu) {
-          // the SwiGLU of the FFN: h = bf16(silu(a) * c), c = this output
+          // the SwiGLU of the FFN: h = bf16(silu(a) * c), c = this output.  The gate
+          // values are loaded kEpiBatch at a time before any store, so the loads are in
+          // flight together (a store to h could otherwise alias the next load of a).
           const float *acol = p.A + (size_t)mb * p.lda + n;
           uint16_t *hcol = p.H + (size_t)mb * p.ldh + n;
 #pragma unroll
-          for (int i = 0; i < CW; ++i)
-            if (mb + i < p.M) hcol[(size_t)i * p.ldh] = swiglu_bf16(acol[(size_t)i * p.lda], y[i]);
+          for (int i0 = 0; i0 < CW; i0 += kEpiBatch) {
+            float av[kEpiBatch];
+#pragma unroll
+            for (int i = 0; i < kEpiBatch; ++i)
+              av[i] = (mb + i0 + i < p.M) ? __ldg(acol + (size_t)(i0 + i) * p.lda) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < kEpiBatch; ++i)
+              if (mb + i0 + i < p.M) hcol[(size_t)(i0 + i) * p.ldh] = swiglu_bf16(av[i], y[i0 + i]);
+          }
         } else {
-          // the post-add of the residual stream: r' = bf16(r + y), stored in place
+          // the post-add of the residual stream: r' = bf16(r + y), stored in place, the
+          // residual read kEpiBatch rows at a time before the stores
           uint16_t *rcol = p.H + (size_t)mb * p.ldh + n;
 #pragma unroll
-          for (int i = 0; i < CW; ++i)
-            if (mb + i < p.M) {
-              uint16_t *rp = rcol + (size_t)i * p.ldh;
-              *rp = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(*rp), y[i]));
+          for (int i0 = 0; i0 < CW; i0 += kEpiBatch) {
+            uint16_t rv[kEpiBatch];
+#pragma unroll
+            for (int i = 0; i < kEpiBatch; ++i) rv[i] = (mb + i0 + i < p.M) ? rcol[(size_t)(i0 + i) * p.ldh] : 0;
+#pragma unroll
+            for (int i = 0; i < kEpiBatch; ++i)
+              if (mb + i0 + i < p.M)
+                rcol[(size_t)(i0 + i) * p.ldh] = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(rv[i]), y[i0 + i]));
             }
         }
       }
@@ -903,6 +941,13 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   p.lda = epi ? epi->lda : 0;
   p.H = epi ? epi->h : nullptr;
   p.ldh = epi ? epi->ldh : 0;
+  // the epilogue's input rows start on 16-byte boundaries (every tile's first channel is a
+  // multiple of 128): they can be prefetched
+  p.epi_pf = 0;
+  if (EPI == kPgSwiglu)
+    p.epi_pf = (reinterpret_cast<uintptr_t>(p.A) % 16) == 0 && (p.lda % 4) == 0;
+  else if (EPI == kPgResid)
+    p.epi_pf = (reinterpret_cast<uintptr_t>(p.H) % 16) == 0 && (p.ldh % 8) == 0;
   p.M = m;
   p.N = w->n;
   p.G = G;
