@@ -82,7 +82,6 @@ constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
 constexpr int kPf = 2;       // k blocks of scale/bias prefetch (no-TMA path)
 constexpr int kLdChunks = 2;  // epilogue tensor-memory loads (8 columns each) per wait
-constexpr int kBarEpi = 1;  // named barrier of the epilogue warps
 constexpr int kEpiBatch = 8;  // rows of the fused epilogues' global loads in flight together
 constexpr int kEpiPrefetchLead = 8;  // k blocks before a tile's end at which its epilogue inputs are prefetched
 static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
@@ -108,7 +107,7 @@ template <int BITS> struct Cfg {
   //           w_full[kWStages], w_empty[kWStages]
   static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 2 + 2 + kPairRing + 2 * kWStages;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16;  // tmem address, abort flag, epilogue stop flag
+  static constexpr int kBytes = kOffMisc + 16;  // tmem address, abort flag
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -309,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *w_empty = w_full + C::kWStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
-  volatile int *epi_stop = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G, KB = p.G + p.NBB;
@@ -341,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
     *abort_flag = 0;
-    *epi_stop = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
@@ -698,23 +695,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // an accumulator use is read: every thread of the first CTA arrives on its
     // acc_empty, the second CTA's warps once each (after all their lanes' loads)
     const uint32_t acc_empty0 = mapa_rank(acc_empty, 0);
-    // The accumulator's completion is polled by one epilogue warp (no suspend-time
-    // hint), which then releases the other fifteen through a hardware named barrier:
-    // sixteen warps asleep in mbarrier.try_wait woke about 0.4 us after the MMAs'
-    // commit, which sat on the loop MMA -> epilogue -> release -> MMA two blocks on.
-    auto acc_ready = [&](int buf, int sc, bool with_scale) -> bool {
-      if (warp == kEpiWarp0) {
-        bool w_ok = mbar_wait_spin_bounded(&acc_full[buf], (uint32_t)uses[buf] & 1u, budget, abort_flag) &&
-                    (!with_scale ||
-                     mbar_wait_spin_bounded(&sc_full[sc], (uint32_t)(h / kScStages) & 1u, budget, abort_flag));
-        if (!__all_sync(0xffffffffu, w_ok)) give_up();
-      }
-      if (warp == kEpiWarp0 && lane == 0) *epi_stop = *abort_flag;
-      named_bar_sync(kBarEpi, kEpiThreads);
-      // every epilogue warp takes the poller's decision (written before the barrier), so
-      // all of them leave the loop at the same barrier
-      return *epi_stop == 0;
-    };
     auto release = [&](int buf) {
       tc_fence_before();
       if (leader) {
@@ -732,7 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < CW; ++i) y[i] = 0.0f;
       for (int kb = 0; kb < G; ++kb, ++h) {
         const int buf = (g0 + kb) & 1, sc = h % kScStages;
-        if (!acc_ready(buf, sc, true)) {
+        bool w_ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)uses[buf] & 1u, budget, abort_flag) &&
+                    mbar_wait_bounded(&sc_full[sc], (uint32_t)(h / kScStages) & 1u, budget, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          give_up();
           ok = false;
           break;
         }
@@ -764,7 +747,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nparts = p.NBB >= 2 ? 2 : 1;
       for (int part = 0; part < nparts && ok; ++part) {
         const int buf = (g0 + G + part) & 1;
-        if (!acc_ready(buf, 0, false)) {
+        bool w_ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)uses[buf] & 1u, budget, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          give_up();
           ok = false;
           break;
         }
