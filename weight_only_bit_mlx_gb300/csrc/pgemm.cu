@@ -29,18 +29,16 @@
 // each output from its own row and column, tiles out of range are zero-filled by
 // TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
 //
-// Warp roles (CTA pairs; each CTA 768 threads):
-//   warp 0      X producer (TMA: this CTA's half of the X tile, or of the S-part tile,
-//               per k block; scale and bias boxes)
-//   warp 1      W producer (TMA: the packed W tile of each main block, into a ring
-//               of its own); allocates the pair's tensor memory (two accumulators of
-//               256 columns)
-//   warps 2-3   first CTA: MMA issuers (one thread each), warp 2 the even k blocks
-//               of the pair's running block count and accumulator 0, warp 3 the odd
-//               ones and accumulator 1; second CTA: warp 2 relays its staged halves
-//   warps 4-7   converters: one channel row per thread, packed codes -> bf16 A tile
+// Warp roles (one CTA per 128-channel x 256-row output tile, 736 threads):
+//   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block;
+//               scale and bias boxes)
+//   warps 1-2   MMA issuers (one thread each): warp 1 the even k blocks of the CTA's
+//               running block count and accumulator 0, warp 2 the odd ones and
+//               accumulator 1; warp 1 also allocates TMEM (two accumulators of 256
+//               columns)
+//   warps 3-6   converters: one channel row per thread, packed codes -> bf16 A tile
 //               in shared memory, scales -> fp32
-//   warps 8-23  epilogue: tensor memory -> registers, scale chain, bias add, store
+//   warps 7-22  epilogue: tensor memory -> registers, scale chain, bias add, store
 //               (four warps per lane quarter, 64 rows of X each)
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
 // QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees TMEM and returns.
@@ -67,7 +65,7 @@ constexpr int kPairRing = 4;  // barriers on which the second CTA reports its st
 constexpr int kScStages = 8;  // fp32 scale rows (deep enough to need no release barrier, see converters)
 constexpr int kConvWarps = 4;   // one channel row per thread
 constexpr int kEpiWarps = 16;   // four per tensor-memory lane quarter, 64 rows of X each
-constexpr int kRoleWarps = 4;   // X producer, W producer (allocates tensor memory), two MMA issuers (second CTA: the relay)
+constexpr int kRoleWarps = 3;   // producer, two MMA issuers (second CTA: the relay) - warp 1 allocates tensor memory
 constexpr int kThreads = (kRoleWarps + kConvWarps + kEpiWarps) * 32;
 constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;
 constexpr int kConvThreads = kConvWarps * 32;
@@ -89,23 +87,19 @@ static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converte
 template <int BITS> struct Cfg {
   static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
   static constexpr int kWBytes = BN * kRowBytes;         // packed W tile
-  static constexpr int kStages = 4;                      // X (or S) half tiles in flight, freed by the MMA
-  // packed W tiles in flight, freed by the converters alone: deep, so that their HBM
-  // latency is not on the loop MMA -> free stage -> load -> convert -> MMA
-  static constexpr int kWStages = BITS == 8 ? 6 : 8;
+  static constexpr int kStages = 4;                      // TMA stages in flight (X/S half tile + packed W tile)
   static constexpr int kOffX = 0;
   static constexpr int kOffW = kOffX + kStages * kXBytes;
-  static constexpr int kOffA = (kOffW + kWStages * kWBytes + 1023) / 1024 * 1024;
+  static constexpr int kOffA = (kOffW + kStages * kWBytes + 1023) / 1024 * 1024;
   static constexpr int kOffSc = kOffA + kABufs * kABytes;
   // biases of the tile's rows, bf16, boxes of 8 groups: [kBiasG / 8][BN][8]
   static constexpr int kOffBias = kOffSc + kScStages * BN * 4;
   // scale boxes streamed by TMA, bf16 [2][BN][8]
   static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
   static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
-  // barriers: x_full, x_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
-  //           sc_full, scb_full[2], scb_empty[2], bias_full, bias_empty, mma_done[2], pair_full[kPairRing],
-  //           w_full[kWStages], w_empty[kWStages]
-  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 2 + 2 + kPairRing + 2 * kWStages;
+  // barriers: tma_full, tma_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
+  //           sc_full, scb_full[2], scb_empty[2], bias_full, bias_empty, mma_done[2], pair_full[kPairRing]
+  static constexpr int kNumBars = 2 * kStages + 2 * kABufs + 4 + kScStages + 4 + 2 + 2 + kPairRing;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;  // tmem address, abort flag
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -291,9 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint16_t *sbias = reinterpret_cast<uint16_t *>(smem + C::kOffBias);
   uint16_t *scbox = reinterpret_cast<uint16_t *>(smem + C::kOffScBox);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-  uint64_t *x_full = bars;
-  uint64_t *x_empty = x_full + C::kStages;
-  uint64_t *a_full = x_empty + C::kStages;
+  uint64_t *tma_full = bars;
+  uint64_t *tma_empty = tma_full + C::kStages;
+  uint64_t *a_full = tma_empty + C::kStages;
   uint64_t *a_empty = a_full + kABufs;
   uint64_t *acc_full = a_empty + kABufs;
   uint64_t *acc_empty = acc_full + 2;
@@ -304,8 +298,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bias_empty = bias_full + 1;
   uint64_t *mma_done = bias_empty + 1;
   uint64_t *pair_full = mma_done + 2;
-  uint64_t *w_full = pair_full + kPairRing;
-  uint64_t *w_empty = w_full + C::kWStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -319,8 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
-    for (int i = 0; i < C::kWStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], kConvThreads); }
+    for (int i = 0; i < C::kStages; ++i) { mbar_init(&tma_full[i], 1); mbar_init(&tma_empty[i], 1 + kConvThreads); }
     for (int i = 0; i < kABufs; ++i) {
       mbar_init(&a_full[i], kConvThreads);
       mbar_init(&a_empty[i], 1);
@@ -417,14 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int s = g % C::kStages;
           const uint32_t ph = (uint32_t)(g / C::kStages) & 1u;
-          if (!mbar_wait_bounded(&x_empty[s], ph ^ 1u, budget, abort_flag)) {
+          if (!mbar_wait_bounded(&tma_empty[s], ph ^ 1u, budget, abort_flag)) {
             give_up();
             alive = false;
             break;
           }
-          mbar_arrive_expect_tx(&x_full[s], (uint32_t)kXBytes);
-          if (kb < G) tma_load_2d(sX + s * kXBytes, &tmX, &x_full[s], kb * BK, m0);
-          else tma_load_2d(sX + s * kXBytes, &tmS, &x_full[s], (kb - G) * BK, m0);
+          if (kb < G) {
+            mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
+            tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
+            tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
+          } else {
+            mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kXBytes);
+            tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
+          }
           ++g;
         }
       }
@@ -434,35 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (bias_sets > 0) (void)mbar_wait_bounded(bias_full, (uint32_t)((bias_sets - 1) & 1), kDrainBudgetNs, nullptr);
       for (int s = 0; s < C::kStages && s < g; ++s) {
         const int uses = (g - 1 - s) / C::kStages + 1;
-        (void)mbar_wait_bounded(&x_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
+        (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // the packed W tiles of the main blocks, as far ahead as the W ring allows (its
-      // stages are freed by the converters, not by the MMA); a warp of its own, so that
-      // it never waits behind the X producer's waits
-      int hw = 0;
-      bool alive = true;
-      for (int t = pair; t < p.tiles && alive; t += npairs) {
-        const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN;
-        for (int kb = 0; kb < G; ++kb, ++hw) {
-          const int sw = hw % C::kWStages;
-          if (!mbar_wait_bounded(&w_empty[sw], ((uint32_t)(hw / C::kWStages) & 1u) ^ 1u, budget, abort_flag)) {
-            give_up();
-            alive = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&w_full[sw], (uint32_t)C::kWBytes);
-          tma_load_2d(sW + sw * C::kWBytes, &tmW, &w_full[sw], kb * (BK * BITS / 32), n0);
-        }
-      }
-      for (int s = 0; s < C::kWStages && s < hw; ++s) {
-        const int uses = (hw - 1 - s) / C::kWStages + 1;
-        (void)mbar_wait_bounded(&w_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
-      }
-    }
-  } else if (warp == 2 || warp == 3) {
+  } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers (first CTA)
     // The k blocks of the pair (all tiles, main and bias blocks) alternate between the
     // two issuers and the two accumulators by their running index g: issuer par takes
@@ -477,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ relay (second CTA)
     // Warp 1 waits, block by block, for this CTA's X (or S) half and converted W tile
     // and reports them on the first CTA's pair_full.
-    const int par = warp - 2;
+    const int par = warp - 1;
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_bf16(2 * BN, BM);
       bool any = false, alive = true;
@@ -490,10 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < KB; ++kb, ++g) {
           if ((g & 1) != par) continue;
           const int s = g % C::kStages, ab = g % kABufs;
-          if (!mbar_wait_spin_bounded(&x_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
-              !mbar_wait_spin_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag) ||
-              !mbar_wait_spin_bounded(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget,
-                                      abort_flag)) {
+          if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
+              !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag) ||
+              !mbar_wait_bounded(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget, abort_flag)) {
             give_up();
             alive = false;
             break;
@@ -501,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool opens = kb < G || kb == kb_first;   // a new use of the accumulator
           const bool closes = kb < G || kb == kb_last;
           if (opens) {  // both CTAs' epilogues have read the accumulator's last use
-            if (!mbar_wait_spin_bounded(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
+            if (!mbar_wait_bounded(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
               give_up();
               alive = false;
               break;
@@ -517,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss2(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
           }
           any = true;
-          mma_commit2(&x_empty[s], 3);
+          mma_commit2(&tma_empty[s], 3);
           mma_commit2(&a_empty[ab], 3);
           if (closes) {
             mma_commit2(&acc_full[par], 3);
@@ -536,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = pair; t < p.tiles && alive; t += npairs) {
         for (int kb = 0; kb < KB; ++kb, ++g) {
           const int s = g % C::kStages, ab = g % kABufs;
-          if (!mbar_wait_spin_bounded(&x_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
-              !mbar_wait_spin_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag)) {
+          if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
+              !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag)) {
             give_up();
             alive = false;
             break;
@@ -577,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < kPf; ++u) {
           const int kb = kb0 + u;
           if (kb >= KB || !alive) break;
-          const int ab = g % kABufs, sw_ = h % C::kWStages;
+          const int s = g % C::kStages, ab = g % kABufs;
           uint32_t s_cur = 0u, b_cur = 0u;
           if (kb < G) {
             if (p.sc_tma) {
@@ -602,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               br[u] = (nvalid && kb + kPf < G) ? ldg_u16(brow + kb + kPf) : 0u;
             }
           }
-          if ((kb < G && !mbar_wait_bounded(&w_full[sw_], (uint32_t)(h / C::kWStages) & 1u, budget, abort_flag)) ||
+          if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
               !mbar_wait_bounded(&a_empty[ab], ((uint32_t)(g / kABufs) & 1u) ^ 1u, budget, abort_flag)) {
             give_up();
             alive = false;
@@ -612,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kb < G) {
             constexpr int NW = BK * BITS / 32;  // words of the row
             uint32_t w[NW];
-            const uint8_t *wp = sW + sw_ * C::kWBytes + ct * C::kRowBytes;
+            const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes;
 #pragma unroll
             for (int i = 0; i < NW / 4; ++i) {
               uint4 v = lds128(wp + 16 * i);
@@ -672,10 +642,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();  // the A tile is read by the tensor core (async proxy)
           mbar_arrive(&a_full[ab]);
           if (kb < G) {
-            mbar_arrive(&w_empty[sw_]);  // the packed W tile is read (its stage may be refilled)
             mbar_arrive(&sc_full[h % kScStages]);
             ++h;
           }
+          mbar_arrive(&tma_empty[s]);
           if (kb == KB - 1) mbar_arrive(bias_empty);  // the tile's bias boxes are read
           ++g;
         }

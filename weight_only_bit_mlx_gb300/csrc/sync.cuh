@@ -83,30 +83,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
-// The same, polling without a suspend-time hint: for the few single threads on a
-// pipeline's critical path (the MMA issuers), which must see a completed phase at once.
-__device__ __forceinline__ bool mbar_try_wait_nohint(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_spin_bounded(uint64_t *bar, uint32_t parity, uint64_t budget_ns,
-                                                       const volatile int *abort) {
-  const uint32_t addr = smem_addr(bar);
-  if (mbar_try_wait_nohint(addr, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (mbar_try_wait_nohint(addr, parity)) return true;
-    if (abort != nullptr && *abort != 0) return false;
-    if (globaltimer_ns() - t0 > budget_ns) return false;
-  }
-}
-
 // Named hardware barrier over `nthreads` threads (warps wait without issuing).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
