@@ -625,11 +625,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     launches = {}
 
-    # warm-up (also sizes the library's scratch before any capture)
+    # warm-up (also sizes the library's scratch before any capture); `pre` counts this
+    # library's launches before the timed region (the skip count of a launch-list capture)
+    pre = 0
     for _ in range(max(1, args.warmup)):
-        sw.decode_pass(1)
-        sw.decode_pass(16)
-        sw.prefill_pass()
+        pre += sw.decode_pass(1) + sw.decode_pass(16) + sw.prefill_pass()
     torch.cuda.synchronize()
 
     graphs = {}
@@ -638,7 +638,7 @@ def run_ours(args):
     for R in (1, 16):
         for fused in (False, True):
             key = f"layer{R}" + ("f" if fused else "")
-            sw.decode_layer_pass(R, fused)
+            pre += sw.decode_layer_pass(R, fused)
             graphs[key], launches[key] = graph_of(lambda: sw.decode_layer_pass(R, fused))
     # the prompt in windows of 128 rows (north of 10,000 launches: one graph)
     WIN = 128
@@ -646,9 +646,12 @@ def run_ours(args):
     for _ in range(args.warmup):
         graphs[1].replay()
         graphs[16].replay()
+        pre += launches["decode1"] + launches["decode16"]
         for key in ("layer1", "layer16", "layer1f", "layer16f"):
             graphs[key].replay()
+            pre += launches[key]
     graphs["win"].replay()
+    pre += launches["win"]
     torch.cuda.synchronize()
     assert q.qlinear_last_error() == q.QL_OK
 
@@ -859,6 +862,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": D_MODEL * 2, "d2h_bytes_per_step": D_MODEL * 4,
                 "what": "decode pass R=1 with x copied from pinned host memory and the last output copied back"},
         "gpu_launches": n_launch,
+        "launches_before_timed_region": pre,
         "clocks": clocks,
         "status": status,
     }
