@@ -116,11 +116,6 @@ def ffn_swiglu(x_bits, w1: dict, w3: dict):
     return a, aa, c, ac, silu(a) * c
 
 
-def attn_proj(x_bits, wq: dict, wk: dict, wv: dict, wg: dict):
-    """The four attention projections of one x: [(y64, A) for q, k, v, gate]."""
-    return [qlinear_w(x_bits, w) for w in (wq, wk, wv, wg)]
-
-
 def pgemm(X_bits, weight: dict):
     """Prompt-window GEMM: the same linear map applied to every row of X."""
     return qlinear_w(X_bits, weight)

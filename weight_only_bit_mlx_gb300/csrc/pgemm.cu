@@ -8,7 +8,7 @@
 //
 // For output Y[m][n] with 64-wide blocks b = 0..G-1:
 //   P_b[n][m] = sum_{j in b} q[n][j] * X[m][j]      tcgen05.mma, bf16 x bf16 -> fp32
-//               A = codes of 128 weight rows converted exactly to bf16 and written
+//               A = codes of the weight rows converted exactly to bf16 and written
 //                   into shared memory in the UMMA 128-byte-swizzle K-major layout;
 //               B = the X tile (256 rows), staged by TMA in shared memory; fresh
 //               accumulator per block, double-buffered in tensor memory
@@ -19,29 +19,36 @@
 // contraction (k' = 3G) instead of a second fma per element and block; its k blocks
 // alternate between the two accumulators like all others, giving two partial sums
 // B_0 (the part holding the first bias block) and B_1.
-// The tile is 128 channels x 256 rows: tcgen05.mma at M = 128, N = 256, K = 16 runs
-// close to the tensor peak, while N = 128 (or A read from tensor memory) reaches
-// well under half of it on this part.
-// The accumulator holds output channels in tensor-memory lanes, so an epilogue
-// thread owns one channel: one scale per block, and the 32 lanes of a warp store 32
-// consecutive channels of a row (coalesced).
+//
+// CTA pairs: a cluster of two CTAs computes a 256-channel x 256-row tile with
+// tcgen05.mma.cta_group::2 at M = 256, N = 256, K = 16, issued by the first CTA.
+// Each CTA stages its own 128 channels of W (A's half) and its own 128 rows of X (B's
+// half) at the same shared-memory offsets, and its tensor memory receives its 128
+// channels x all 256 rows; so each SM stages and reads half the X tile that a single
+// CTA would.  The accumulator holds output channels in tensor-memory lanes, so an
+// epilogue thread owns one channel: one scale per block, and the 32 lanes of a warp
+// store 32 consecutive channels of a row (coalesced).
 // Every quantity of row m depends only on X[m][:] and W: the tensor core computes
 // each output from its own row and column, tiles out of range are zero-filled by
 // TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
 //
-// Warp roles (one CTA per 128-channel x 256-row output tile, 736 threads):
-//   warp 0      TMA producer (X tile, packed W tile, or S-part tile per k block;
-//               scale and bias boxes)
-//   warps 1-2   MMA issuers (one thread each): warp 1 the even k blocks of the CTA's
-//               running block count and accumulator 0, warp 2 the odd ones and
-//               accumulator 1; warp 1 also allocates TMEM (two accumulators of 256
-//               columns)
+// Warp roles (each CTA of the pair, 736 threads):
+//   warp 0      TMA producer (this CTA's half of the X tile, or of the S-part tile,
+//               and its packed W tile, per k block; scale and bias boxes)
+//   warps 1-2   first CTA: MMA issuers (one thread each), warp 1 the even k blocks of
+//               the pair's running block count and accumulator 0, warp 2 the odd ones
+//               and accumulator 1; second CTA: warp 1 relays "my halves of block g are
+//               staged" to the first CTA's pair_full barriers.  Warp 1 of both CTAs
+//               allocates the pair's tensor memory (two accumulators of 256 columns).
 //   warps 3-6   converters: one channel row per thread, packed codes -> bf16 A tile
 //               in shared memory, scales -> fp32
-//   warps 7-22  epilogue: tensor memory -> registers, scale chain, bias add, store
+//   warps 7-22  epilogue: tensor memory -> registers, scale chain, bias add, and the
+//               store of the output (or the SwiGLU / post-add epilogue, template EPI)
 //               (four warps per lane quarter, 64 rows of X each)
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
-// QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees TMEM and returns.
+// QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, and both CTAs pass a final
+// cluster barrier (neither leaves while the other may still touch its shared memory)
+// before the pair's tensor memory is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
