@@ -32,19 +32,24 @@
 // each output from its own row and column, tiles out of range are zero-filled by
 // TMA, and nothing (split-K, tile shape, order) depends on m or on the window.
 //
-// Warp roles (each CTA of the pair, 736 threads):
-//   warp 0      TMA producer (this CTA's half of the X tile, or of the S-part tile,
+// Warp roles (each CTA of the pair, 512 threads = four warpgroups):
+//   warpgroup 0 (warps 0-3, 56 registers)
+//     warp 0    TMA producer (this CTA's half of the X tile, or of the S-part tile,
 //               and its packed W tile, per k block; scale and bias boxes)
-//   warps 1-2   first CTA: MMA issuers (one thread each), warp 1 the even k blocks of
+//     warps 1-2 first CTA: MMA issuers (one thread each), warp 1 the even k blocks of
 //               the pair's running block count and accumulator 0, warp 2 the odd ones
 //               and accumulator 1; second CTA: warp 1 relays "my halves of block g are
 //               staged" to the first CTA's pair_full barriers.  Warp 1 of both CTAs
 //               allocates the pair's tensor memory (two accumulators of 256 columns).
-//   warps 3-6   converters: one channel row per thread, packed codes -> bf16 A tile
-//               in shared memory, scales -> fp32
-//   warps 7-22  epilogue: tensor memory -> registers, scale chain, bias add, and the
-//               store of the output (or the SwiGLU / post-add epilogue, template EPI)
-//               (four warps per lane quarter, 64 rows of X each)
+//     warp 3    idle
+//   warpgroup 1 (warps 4-7, 88 registers): converters, one channel row per thread,
+//               packed codes -> bf16 A tile in shared memory, scales -> fp32
+//   warpgroups 2-3 (warps 8-15, 184 registers): epilogue, tensor memory -> registers,
+//               scale chain, bias add, and the store of the output (or the SwiGLU /
+//               post-add epilogue, template EPI); two warps per lane quarter, 128 rows
+//               of X each, held in registers across the k loop
+// The launch gives every thread 128 registers; setmaxnreg moves them from the first two
+// warpgroups to the epilogue, whose running sums (128 fp32 per thread) need them.
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
 // QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, and both CTAs pass a final
 // cluster barrier (neither leaves while the other may still touch its shared memory)
@@ -71,9 +76,17 @@ constexpr int BK = 64;
 constexpr int kPairRing = 4;  // barriers on which the second CTA reports its staged halves
 constexpr int kScStages = 8;  // fp32 scale rows (deep enough to need no release barrier, see converters)
 constexpr int kConvWarps = 4;   // one channel row per thread
-constexpr int kEpiWarps = 16;   // four per tensor-memory lane quarter, 64 rows of X each
-constexpr int kRoleWarps = 3;   // producer, two MMA issuers (second CTA: the relay) - warp 1 allocates tensor memory
+constexpr int kEpiWarps = 8;    // two per tensor-memory lane quarter, 128 rows of X each
+constexpr int kRoleWarps = 4;   // producer, two MMA issuers (second CTA: the relay), one idle - warp 1 allocates tensor memory
 constexpr int kThreads = (kRoleWarps + kConvWarps + kEpiWarps) * 32;
+// registers per thread: at launch, and per warpgroup after setmaxnreg (multiples of 8)
+constexpr int kRegsLaunch = 65536 / kThreads;
+constexpr int kRegsRole = 56;
+constexpr int kRegsConv = 88;
+constexpr int kRegsEpi = 184;
+static_assert(kThreads == 512 && kRoleWarps == 4 && kConvWarps == 4 && kEpiWarps == 8, "warpgroup layout");
+static_assert(128 * (kRegsRole + kRegsConv) + 256 * kRegsEpi <= kThreads * kRegsLaunch,
+              "the register split must fit in the registers the block is launched with");
 constexpr int kEpiWarp0 = kRoleWarps + kConvWarps;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
@@ -86,7 +99,8 @@ static_assert(2 * BM <= kTmemCols, "tensor memory budget");
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
 constexpr int kPf = 2;       // k blocks of scale/bias prefetch (no-TMA path)
-constexpr int kLdChunks = 2;  // epilogue tensor-memory loads (8 columns each) per wait
+constexpr int kLdCols = 32;   // accumulator columns per epilogue tensor-memory load (one wait each)
+static_assert(kEpiRows % kLdCols == 0, "epilogue loads cover the thread's rows");
 constexpr int kEpiBatch = 8;  // rows of the fused epilogues' global loads in flight together
 constexpr int kEpiPrefetchLead = 8;  // k blocks before a tile's end at which its epilogue inputs are prefetched
 static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
@@ -226,14 +240,26 @@ __device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]
                : "r"(taddr));
 }
 
+// 32 consecutive columns of this warp's 32 lanes: r[j] = column taddr + j of this thread's lane
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// (d0, d1) = (a0, a1) * (b0, b1) + (d0, d1), each rounded to nearest (packed fp32 fma)
-__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rd, {%0, %1};"
-      "\n\tfma.rn.f32x2 rd, ra, rb, rd;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+// per-warpgroup register budget (all four warps of the warpgroup execute it)
+template <int N> __device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N> __device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ uint4 lds128(const void *p) {
@@ -364,166 +390,172 @@ __global__ void __launch_bounds__(kThreads, 1)
     record_status(p.status, kErrTimeout);
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int g = 0, box = 0, tj = 0, bias_sets = 0;
-      bool alive = true;
-      for (int t = pair; t < p.tiles && alive; t += npairs, ++tj) {
-        // this CTA's channels and rows of X of tile t
-        const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN, m0 = (t / p.tiles_n) * BM + (int)rank * BMH;
-        if (p.bi_tma) {
-          // every bias of the tile's channels, once per tile (read only by its bias
-          // blocks), after the previous tile's bias blocks are converted
-          if (tj > 0 && !mbar_wait_bounded(bias_empty, (uint32_t)((tj - 1) & 1), budget, abort_flag)) {
-            give_up();
-            break;
+  // Each role first sets its warpgroup's register budget (the warpgroups that give
+  // registers up do so before the epilogue's increase can be granted).
+  if (warp < kRoleWarps) {
+    regs_dec<kRegsRole>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        int g = 0, box = 0, tj = 0, bias_sets = 0;
+        bool alive = true;
+        for (int t = pair; t < p.tiles && alive; t += npairs, ++tj) {
+          // this CTA's channels and rows of X of tile t
+          const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN, m0 = (t / p.tiles_n) * BM + (int)rank * BMH;
+          if (p.bi_tma) {
+            // every bias of the tile's channels, once per tile (read only by its bias
+            // blocks), after the previous tile's bias blocks are converted
+            if (tj > 0 && !mbar_wait_bounded(bias_empty, (uint32_t)((tj - 1) & 1), budget, abort_flag)) {
+              give_up();
+              break;
+            }
+            const int nbox = (G + 7) / 8;
+            mbar_arrive_expect_tx(bias_full, (uint32_t)(nbox * BN * 16));
+            for (int i = 0; i < nbox; ++i) tma_load_2d(sbias + i * BN * 8, &tmBi, bias_full, 8 * i, n0);
+            ++bias_sets;
           }
-          const int nbox = (G + 7) / 8;
-          mbar_arrive_expect_tx(bias_full, (uint32_t)(nbox * BN * 16));
-          for (int i = 0; i < nbox; ++i) tma_load_2d(sbias + i * BN * 8, &tmBi, bias_full, 8 * i, n0);
-          ++bias_sets;
-        }
-        for (int kb = 0; kb < KB; ++kb) {
-          if (EPI != kPgStore && p.epi_pf && kb == (G > kEpiPrefetchLead ? G - kEpiPrefetchLead : 0)) {
-            // the tile's rows of the fused epilogue's input (the gate output, or the
-            // residual), this CTA's channels, into L2 ahead of the tile's end
-            const int mt = (t / p.tiles_n) * BM;
-            const int nch = min(BN, p.N - n0);
-            const uint32_t esz = EPI == kPgSwiglu ? 4u : 2u;
-            const uint32_t bytes = ((uint32_t)nch * esz) & ~15u;
-            if (nch > 0 && bytes > 0) {
-              for (int r = 0; r < BM && mt + r < p.M; ++r) {
-                const void *src = EPI == kPgSwiglu
-                                      ? static_cast<const void *>(p.A + (size_t)(mt + r) * p.lda + n0)
-                                      : static_cast<const void *>(p.H + (size_t)(mt + r) * p.ldh + n0);
-                prefetch_l2_bulk(src, bytes);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (EPI != kPgStore && p.epi_pf && kb == (G > kEpiPrefetchLead ? G - kEpiPrefetchLead : 0)) {
+              // the tile's rows of the fused epilogue's input (the gate output, or the
+              // residual), this CTA's channels, into L2 ahead of the tile's end
+              const int mt = (t / p.tiles_n) * BM;
+              const int nch = min(BN, p.N - n0);
+              const uint32_t esz = EPI == kPgSwiglu ? 4u : 2u;
+              const uint32_t bytes = ((uint32_t)nch * esz) & ~15u;
+              if (nch > 0 && bytes > 0) {
+                for (int r = 0; r < BM && mt + r < p.M; ++r) {
+                  const void *src = EPI == kPgSwiglu
+                                        ? static_cast<const void *>(p.A + (size_t)(mt + r) * p.lda + n0)
+                                        : static_cast<const void *>(p.H + (size_t)(mt + r) * p.ldh + n0);
+                  prefetch_l2_bulk(src, bytes);
+                }
               }
             }
-          }
-          if (p.sc_tma && kb < G && (kb & 7) == 0) {
-            // scales of blocks kb .. kb+7 for the tile's channels, two boxes in flight
-            const int slot = box & 1;
-            if (!mbar_wait_bounded(&scb_empty[slot], ((uint32_t)(box >> 1) & 1u) ^ 1u, budget, abort_flag)) {
+            if (p.sc_tma && kb < G && (kb & 7) == 0) {
+              // scales of blocks kb .. kb+7 for the tile's channels, two boxes in flight
+              const int slot = box & 1;
+              if (!mbar_wait_bounded(&scb_empty[slot], ((uint32_t)(box >> 1) & 1u) ^ 1u, budget, abort_flag)) {
+                give_up();
+                alive = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&scb_full[slot], (uint32_t)(BN * 16));
+              tma_load_2d(scbox + slot * BN * 8, &tmSc, &scb_full[slot], kb, n0);
+              ++box;
+            }
+            const int s = g % C::kStages;
+            const uint32_t ph = (uint32_t)(g / C::kStages) & 1u;
+            if (!mbar_wait_bounded(&tma_empty[s], ph ^ 1u, budget, abort_flag)) {
               give_up();
               alive = false;
               break;
             }
-            mbar_arrive_expect_tx(&scb_full[slot], (uint32_t)(BN * 16));
-            tma_load_2d(scbox + slot * BN * 8, &tmSc, &scb_full[slot], kb, n0);
-            ++box;
+            if (kb < G) {
+              mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
+              tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
+              tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
+            } else {
+              mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kXBytes);
+              tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
+            }
+            ++g;
           }
-          const int s = g % C::kStages;
-          const uint32_t ph = (uint32_t)(g / C::kStages) & 1u;
-          if (!mbar_wait_bounded(&tma_empty[s], ph ^ 1u, budget, abort_flag)) {
-            give_up();
-            alive = false;
-            break;
-          }
-          if (kb < G) {
-            mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
-            tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
-            tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
-          } else {
-            mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kXBytes);
-            tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
-          }
-          ++g;
+        }
+        // drain: every copy this CTA started must land before its shared memory goes away
+        for (int j = (box > 2 ? box - 2 : 0); j < box; ++j)
+          (void)mbar_wait_bounded(&scb_full[j & 1], (uint32_t)(j >> 1) & 1u, kDrainBudgetNs, nullptr);
+        if (bias_sets > 0) (void)mbar_wait_bounded(bias_full, (uint32_t)((bias_sets - 1) & 1), kDrainBudgetNs, nullptr);
+        for (int s = 0; s < C::kStages && s < g; ++s) {
+          const int uses = (g - 1 - s) / C::kStages + 1;
+          (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
         }
       }
-      // drain: every copy this CTA started must land before its shared memory goes away
-      for (int j = (box > 2 ? box - 2 : 0); j < box; ++j)
-        (void)mbar_wait_bounded(&scb_full[j & 1], (uint32_t)(j >> 1) & 1u, kDrainBudgetNs, nullptr);
-      if (bias_sets > 0) (void)mbar_wait_bounded(bias_full, (uint32_t)((bias_sets - 1) & 1), kDrainBudgetNs, nullptr);
-      for (int s = 0; s < C::kStages && s < g; ++s) {
-        const int uses = (g - 1 - s) / C::kStages + 1;
-        (void)mbar_wait_bounded(&tma_full[s], (uint32_t)(uses - 1) & 1u, kDrainBudgetNs, nullptr);
-      }
-    }
-  } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers (first CTA)
-    // The k blocks of the pair (all tiles, main and bias blocks) alternate between the
-    // two issuers and the two accumulators by their running index g: issuer par takes
-    // g % 2 == par into accumulator par.  A main block is one use of the accumulator;
-    // the bias blocks of a tile that fall to one issuer chain into one use (so each
-    // accumulator holds half of the bias contraction).  Strict alternation keeps each
-    // issuer at most one block ahead of the other, so no wait is ever more than one
-    // phase ahead of a barrier's last completion.  A block is issued once both CTAs
-    // have staged their halves: this CTA's own barriers, and pair_full, on which the
-    // second CTA's relay reports its halves.  Each commit arrives on the barrier at the
-    // same offset in both CTAs (mask 0b11).
-    // ------------------------------------------------------------ relay (second CTA)
-    // Warp 1 waits, block by block, for this CTA's X (or S) half and converted W tile
-    // and reports them on the first CTA's pair_full.
-    const int par = warp - 1;
-    if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_bf16(2 * BN, BM);
-      bool any = false, alive = true;
-      int g = 0, uses = 0;  // k blocks of the pair so far; uses of accumulator par so far
-      for (int t = pair; t < p.tiles && alive; t += npairs) {
-        const int g0 = g;
-        // this issuer's first and last bias block of the tile
-        const int kb_first = G + ((g0 + G) % 2 == par ? 0 : 1);
-        const int kb_last = (g0 + KB - 1) % 2 == par ? KB - 1 : KB - 2;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
-          if ((g & 1) != par) continue;
-          const int s = g % C::kStages, ab = g % kABufs;
-          if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
-              !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag) ||
-              !mbar_wait_bounded(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget, abort_flag)) {
-            give_up();
-            alive = false;
-            break;
-          }
-          const bool opens = kb < G || kb == kb_first;   // a new use of the accumulator
-          const bool closes = kb < G || kb == kb_last;
-          if (opens) {  // both CTAs' epilogues have read the accumulator's last use
-            if (!mbar_wait_bounded(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
+    } else if (warp == 1 || warp == 2) {
+      // ------------------------------------------------------------ MMA issuers (first CTA)
+      // The k blocks of the pair (all tiles, main and bias blocks) alternate between the
+      // two issuers and the two accumulators by their running index g: issuer par takes
+      // g % 2 == par into accumulator par.  A main block is one use of the accumulator;
+      // the bias blocks of a tile that fall to one issuer chain into one use (so each
+      // accumulator holds half of the bias contraction).  Strict alternation keeps each
+      // issuer at most one block ahead of the other, so no wait is ever more than one
+      // phase ahead of a barrier's last completion.  A block is issued once both CTAs
+      // have staged their halves: this CTA's own barriers, and pair_full, on which the
+      // second CTA's relay reports its halves.  Each commit arrives on the barrier at the
+      // same offset in both CTAs (mask 0b11).
+      // ------------------------------------------------------------ relay (second CTA)
+      // Warp 1 waits, block by block, for this CTA's X (or S) half and converted W tile
+      // and reports them on the first CTA's pair_full.
+      const int par = warp - 1;
+      if (lane == 0 && leader) {
+        constexpr uint32_t idesc = idesc_bf16(2 * BN, BM);
+        bool any = false, alive = true;
+        int g = 0, uses = 0;  // k blocks of the pair so far; uses of accumulator par so far
+        for (int t = pair; t < p.tiles && alive; t += npairs) {
+          const int g0 = g;
+          // this issuer's first and last bias block of the tile
+          const int kb_first = G + ((g0 + G) % 2 == par ? 0 : 1);
+          const int kb_last = (g0 + KB - 1) % 2 == par ? KB - 1 : KB - 2;
+          for (int kb = 0; kb < KB; ++kb, ++g) {
+            if ((g & 1) != par) continue;
+            const int s = g % C::kStages, ab = g % kABufs;
+            if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
+                !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag) ||
+                !mbar_wait_bounded(&pair_full[g % kPairRing], (uint32_t)(g / kPairRing) & 1u, budget, abort_flag)) {
               give_up();
               alive = false;
               break;
             }
+            const bool opens = kb < G || kb == kb_first;   // a new use of the accumulator
+            const bool closes = kb < G || kb == kb_last;
+            if (opens) {  // both CTAs' epilogues have read the accumulator's last use
+              if (!mbar_wait_bounded(&acc_empty[par], ((uint32_t)uses & 1u) ^ 1u, budget, abort_flag)) {
+                give_up();
+                alive = false;
+                break;
+              }
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(par * BM);
+            const uint64_t ad = sw128_desc(smem_addr(sA + ab * kABytes));
+            const uint64_t bd = sw128_desc(smem_addr(sX + s * kXBytes));
+  #pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint32_t acc = (kk > 0 || !opens) ? 1u : 0u;
+              mma_bf16_ss2(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
+            }
+            any = true;
+            mma_commit2(&tma_empty[s], 3);
+            mma_commit2(&a_empty[ab], 3);
+            if (closes) {
+              mma_commit2(&acc_full[par], 3);
+              ++uses;
+            }
           }
-          tc_fence_after();
-          const uint32_t d = tmem_base + (uint32_t)(par * BM);
-          const uint64_t ad = sw128_desc(smem_addr(sA + ab * kABytes));
-          const uint64_t bd = sw128_desc(smem_addr(sX + s * kXBytes));
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t acc = (kk > 0 || !opens) ? 1u : 0u;
-            mma_bf16_ss2(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
-          }
-          any = true;
-          mma_commit2(&tma_empty[s], 3);
-          mma_commit2(&a_empty[ab], 3);
-          if (closes) {
-            mma_commit2(&acc_full[par], 3);
-            ++uses;
+        }
+        if (any) {
+          mma_commit2(&mma_done[par], 1);
+          (void)mbar_wait_bounded(&mma_done[par], 0u, kDrainBudgetNs, nullptr);
+        }
+      } else if (lane == 0 && par == 0) {
+        const uint32_t pf0 = mapa_rank(pair_full, 0);
+        bool alive = true;
+        int g = 0;
+        for (int t = pair; t < p.tiles && alive; t += npairs) {
+          for (int kb = 0; kb < KB; ++kb, ++g) {
+            const int s = g % C::kStages, ab = g % kABufs;
+            if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
+                !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag)) {
+              give_up();
+              alive = false;
+              break;
+            }
+            mbar_arrive_cluster(pf0 + (uint32_t)((g % kPairRing) * 8));
           }
         }
       }
-      if (any) {
-        mma_commit2(&mma_done[par], 1);
-        (void)mbar_wait_bounded(&mma_done[par], 0u, kDrainBudgetNs, nullptr);
-      }
-    } else if (lane == 0 && par == 0) {
-      const uint32_t pf0 = mapa_rank(pair_full, 0);
-      bool alive = true;
-      int g = 0;
-      for (int t = pair; t < p.tiles && alive; t += npairs) {
-        for (int kb = 0; kb < KB; ++kb, ++g) {
-          const int s = g % C::kStages, ab = g % kABufs;
-          if (!mbar_wait_bounded(&tma_full[s], (uint32_t)(g / C::kStages) & 1u, budget, abort_flag) ||
-              !mbar_wait_bounded(&a_full[ab], (uint32_t)(g / kABufs) & 1u, budget, abort_flag)) {
-            give_up();
-            alive = false;
-            break;
-          }
-          mbar_arrive_cluster(pf0 + (uint32_t)((g % kPairRing) * 8));
-        }
-      }
-    }
+    }     // warp 3: idle
   } else if (warp < kEpiWarp0) {
+    regs_dec<kRegsConv>();
     // ------------------------------------------------------------ converters
     // Thread = one channel row of the tile.  Its 64 codes of the block become 32 exact
     // bf16 pairs, written as eight 16-byte chunks of the row of the A tile in the
@@ -659,13 +691,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
+    regs_inc<kRegsEpi>();
     // ------------------------------------------------------------ epilogue
     constexpr int CW = kEpiRows;  // rows of X owned by one thread
     const int q = warp & 3;       // tensor-memory lane quarter this warp may access
     const int slice = (warp - kEpiWarp0) >> 2;
     const int ch_row = 32 * q + lane;  // output channel of this thread within the tile
     const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(slice * CW);
-    int uses[2] = {0, 0};  // completed uses of each accumulator
+    uint32_t phase = 0u;   // bit b: parity of the completed uses of accumulator b
     int h = 0;             // main blocks so far
     int g0 = 0;            // running index of the tile's first k block (as the issuers count)
     bool ok = true;
@@ -684,12 +717,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = pair; t < p.tiles && ok; t += npairs, g0 += KB) {
       // this CTA's 128 channels; the accumulator holds all 256 rows of the tile
       const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN, m0 = (t / p.tiles_n) * BM;
-      float y[CW];
+      // the running sums of the thread's CW rows, as pairs (rows 2j, 2j + 1) so that each
+      // step is one packed fp32 fma per pair (round to nearest in each lane)
+      float2 y[CW / 2];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) y[i] = 0.0f;
+      for (int i = 0; i < CW / 2; ++i) y[i] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < G; ++kb, ++h) {
         const int buf = (g0 + kb) & 1, sc = h % kScStages;
-        bool w_ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)uses[buf] & 1u, budget, abort_flag) &&
+        bool w_ok = mbar_wait_bounded(&acc_full[buf], (phase >> buf) & 1u, budget, abort_flag) &&
                     mbar_wait_bounded(&sc_full[sc], (uint32_t)(h / kScStages) & 1u, budget, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
           give_up();
@@ -697,24 +732,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const float sv = sSc[sc * BN + ch_row];
-        // kLdChunks loads of 8 columns in flight per wait: the tensor-memory load
-        // latency is paid CW / (8 * kLdChunks) times per block instead of CW / 8
+        const float s1 = sSc[sc * BN + ch_row];
+        const float2 sv = make_float2(s1, s1);
 #pragma unroll
-        for (int ch = 0; ch < CW / 8; ch += kLdChunks) {
-          uint32_t r[kLdChunks][8];
-#pragma unroll
-          for (int u = 0; u < kLdChunks; ++u) tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * (ch + u)), r[u]);
+        for (int c0 = 0; c0 < CW; c0 += kLdCols) {
+          uint32_t r[kLdCols];
+          tmem_ld32_nowait(lane_base + (uint32_t)(buf * BM + c0), r);
           tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < kLdChunks; ++u)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              ffma2(y[8 * (ch + u) + 2 * i], y[8 * (ch + u) + 2 * i + 1], sv, sv, __uint_as_float(r[u][2 * i]),
-                    __uint_as_float(r[u][2 * i + 1]));
+          for (int i = 0; i < kLdCols / 2; ++i)
+            y[c0 / 2 + i] =
+                __ffma2_rn(sv, make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), y[c0 / 2 + i]);
         }
         release(buf);
-        ++uses[buf];
+        phase ^= 1u << buf;
       }
       if (!ok) break;
       // the bias contraction of the tile: its blocks alternate between the two
@@ -724,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nparts = p.NBB >= 2 ? 2 : 1;
       for (int part = 0; part < nparts && ok; ++part) {
         const int buf = (g0 + G + part) & 1;
-        bool w_ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)uses[buf] & 1u, budget, abort_flag);
+        bool w_ok = mbar_wait_bounded(&acc_full[buf], (phase >> buf) & 1u, budget, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
           give_up();
           ok = false;
@@ -732,15 +763,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int ch = 0; ch < CW / 8; ++ch) {
-          uint32_t r[8];
-          tmem_ld8_nowait(lane_base + (uint32_t)(buf * BM + 8 * ch), r);
+        for (int c0 = 0; c0 < CW; c0 += kLdCols) {
+          uint32_t r[kLdCols];
+          tmem_ld32_nowait(lane_base + (uint32_t)(buf * BM + c0), r);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) y[8 * ch + i] = __fadd_rn(y[8 * ch + i], __uint_as_float(r[i]));
+          for (int i = 0; i < kLdCols / 2; ++i)
+            y[c0 / 2 + i] = __fadd2_rn(y[c0 / 2 + i], make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])));
         }
         release(buf);
-        ++uses[buf];
+        phase ^= 1u << buf;
       }
       if (!ok) break;
       // one channel per thread: lanes of a warp write 32 consecutive channels of a row
@@ -748,10 +780,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n < p.N) {
         const int mb = m0 + slice * CW;
         if constexpr (EPI == kPgStore) {
-          float *ycol = p.Y + (size_t)mb * p.ldy + n;
+          float *yp = p.Y + (size_t)mb * p.ldy + n;
+          if (mb + CW <= p.M) {
+            // the whole slice is in range: one store per row, the pointer stepped by the pitch
 #pragma unroll
-          for (int i = 0; i < CW; ++i)
-            if (mb + i < p.M) ycol[(size_t)i * p.ldy] = y[i];
+            for (int i = 0; i < CW / 2; ++i) {
+              yp[0] = y[i].x;
+              yp[p.ldy] = y[i].y;
+              yp += 2 * p.ldy;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+              if (mb + i < p.M) yp[(size_t)i * p.ldy] = (i & 1) ? y[i >> 1].y : y[i >> 1].x;
+          }
         } else if constexpr (EPI == kPgSwiglu) {
           // the SwiGLU of the FFN: h = bf16(silu(a) * c), c = this output.  The gate
           // values are loaded kEpiBatch at a time before any store, so the loads are in
@@ -766,7 +808,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               av[i] = (mb + i0 + i < p.M) ? __ldg(acol + (size_t)(i0 + i) * p.lda) : 0.0f;
 #pragma unroll
             for (int i = 0; i < kEpiBatch; ++i)
-              if (mb + i0 + i < p.M) hcol[(size_t)(i0 + i) * p.ldh] = swiglu_bf16(av[i], y[i0 + i]);
+              if (mb + i0 + i < p.M)
+                hcol[(size_t)(i0 + i) * p.ldh] = swiglu_bf16(av[i], ((i0 + i) & 1) ? y[(i0 + i) >> 1].y : y[(i0 + i) >> 1].x);
           }
         } else {
           // the post-add of the residual stream: r' = bf16(r + y), stored in place, the
@@ -780,7 +823,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kEpiBatch; ++i)
               if (mb + i0 + i < p.M)
-                rcol[(size_t)(i0 + i) * p.ldh] = f32_to_bf16_rn(__fadd_rn(bf16_to_f32(rv[i]), y[i0 + i]));
+                rcol[(size_t)(i0 + i) * p.ldh] = f32_to_bf16_rn(
+                    __fadd_rn(bf16_to_f32(rv[i]), ((i0 + i) & 1) ? y[(i0 + i) >> 1].y : y[(i0 + i) >> 1].x));
             }
         }
       }
@@ -935,6 +979,14 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
     if (cudaFuncSetAttribute(pg::pgemm_kernel<BITS, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc) !=
         cudaSuccess)
       return QL_ERR_LAUNCH;
+    // The warpgroups' setmaxnreg split assumes that the block is launched with exactly
+    // kRegsLaunch registers per thread: with fewer, the epilogue's increase could never
+    // be granted.  Refuse to launch a build that differs.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, pg::pgemm_kernel<BITS, EPI>) != cudaSuccess || fa.numRegs != pg::kRegsLaunch) {
+      (void)cudaGetLastError();
+      return QL_ERR_LAUNCH;
+    }
     attr_set[dev].store(true, std::memory_order_relaxed);
   }
   pg::Params p;
