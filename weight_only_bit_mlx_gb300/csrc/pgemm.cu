@@ -99,7 +99,7 @@ static_assert(2 * BM <= kTmemCols, "tensor memory budget");
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 constexpr int kBiasG = 128;  // groups of bias staged in shared memory (k <= 8192); larger k reads global
 constexpr int kPf = 2;       // k blocks of scale/bias prefetch (no-TMA path)
-constexpr int kLdCols = 32;   // accumulator columns per epilogue tensor-memory load (one wait each)
+constexpr int kLdCols = 16;   // accumulator columns per epilogue tensor-memory load (two in flight)
 static_assert(kEpiRows % kLdCols == 0, "epilogue loads cover the thread's rows");
 constexpr int kEpiBatch = 8;  // rows of the fused epilogues' global loads in flight together
 constexpr int kEpiPrefetchLead = 8;  // k blocks before a tile's end at which its epilogue inputs are prefetched
@@ -128,6 +128,8 @@ template <int BITS> struct Cfg {
 };
 
 struct Params {
+  const uint8_t *wq;     // packed codes, rows of w_row_bytes (for the L2 prefetch of a tile's rows)
+  int64_t w_row_bytes;
   const uint16_t *scales;
   const uint16_t *biases;
   int sc_tma;  // scales arrive as TMA boxes of 8 groups (k % 512 == 0, 16-byte aligned)
@@ -158,6 +160,10 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
 __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
+
+// programmatic dependent launch: wait until the preceding kernels of the stream are
+// complete and their writes visible (a no-op when launched without the attribute)
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -234,21 +240,13 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-}
-
-// 32 consecutive columns of this warp's 32 lanes: r[j] = column taddr + j of this thread's lane
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+// 16 consecutive columns of this warp's 32 lanes: r[j] = column taddr + j of this thread's lane
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 
@@ -399,9 +397,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         int g = 0, box = 0, tj = 0, bias_sets = 0;
         bool alive = true;
+        bool dep_done = false;  // griddep_wait() passed: X and the row sums may be read
         for (int t = pair; t < p.tiles && alive; t += npairs, ++tj) {
           // this CTA's channels and rows of X of tile t
           const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN, m0 = (t / p.tiles_n) * BM + (int)rank * BMH;
+          {
+            // the tile's packed rows (contiguous) into L2 ahead of their TMA loads: a
+            // prompt window reads each weight tile once, straight from HBM
+            const int rows = min(BN, p.N - n0);
+            if (rows > 0) prefetch_l2_bulk(p.wq + (size_t)n0 * p.w_row_bytes, (uint32_t)(rows * p.w_row_bytes));
+          }
           if (p.bi_tma) {
             // every bias of the tile's channels, once per tile (read only by its bias
             // blocks), after the previous tile's bias blocks are converted
@@ -452,10 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (kb < G) {
               mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
-              tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
               tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
+              if (!dep_done) {  // the weights are constant; X is written by earlier kernels
+                griddep_wait();
+                dep_done = true;
+              }
+              tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
             } else {
               mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kXBytes);
+              if (!dep_done) {
+                griddep_wait();
+                dep_done = true;
+              }
               tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
             }
             ++g;
@@ -693,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_inc<kRegsEpi>();
     // ------------------------------------------------------------ epilogue
+    griddep_wait();  // the outputs (and the fused epilogues' inputs) belong to earlier kernels until then
     constexpr int CW = kEpiRows;  // rows of X owned by one thread
     const int q = warp & 3;       // tensor-memory lane quarter this warp may access
     const int slice = (warp - kEpiWarp0) >> 2;
@@ -734,15 +748,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float s1 = sSc[sc * BN + ch_row];
         const float2 sv = make_float2(s1, s1);
+        // software-pipelined: the load of chunk c + 1 is in flight while chunk c is
+        // accumulated (tcgen05.wait::ld then waits only for that one load)
+        const uint32_t ta = lane_base + (uint32_t)(buf * BM);
+        uint32_t r[2][kLdCols];
+        tmem_ld16_nowait(ta, r[0]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c0 = 0; c0 < CW; c0 += kLdCols) {
-          uint32_t r[kLdCols];
-          tmem_ld32_nowait(lane_base + (uint32_t)(buf * BM + c0), r);
-          tmem_wait_ld();
+        for (int c = 0; c < CW / kLdCols; ++c) {
+          if (c + 1 < CW / kLdCols) tmem_ld16_nowait(ta + (uint32_t)((c + 1) * kLdCols), r[(c + 1) & 1]);
 #pragma unroll
           for (int i = 0; i < kLdCols / 2; ++i)
-            y[c0 / 2 + i] =
-                __ffma2_rn(sv, make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), y[c0 / 2 + i]);
+            y[c * (kLdCols / 2) + i] = __ffma2_rn(
+                sv, make_float2(__uint_as_float(r[c & 1][2 * i]), __uint_as_float(r[c & 1][2 * i + 1])),
+                y[c * (kLdCols / 2) + i]);
+          if (c + 1 < CW / kLdCols) tmem_wait_ld();
         }
         release(buf);
         phase ^= 1u << buf;
@@ -762,14 +782,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        const uint32_t ta = lane_base + (uint32_t)(buf * BM);
+        uint32_t r[2][kLdCols];
+        tmem_ld16_nowait(ta, r[0]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c0 = 0; c0 < CW; c0 += kLdCols) {
-          uint32_t r[kLdCols];
-          tmem_ld32_nowait(lane_base + (uint32_t)(buf * BM + c0), r);
-          tmem_wait_ld();
+        for (int c = 0; c < CW / kLdCols; ++c) {
+          if (c + 1 < CW / kLdCols) tmem_ld16_nowait(ta + (uint32_t)((c + 1) * kLdCols), r[(c + 1) & 1]);
 #pragma unroll
           for (int i = 0; i < kLdCols / 2; ++i)
-            y[c0 / 2 + i] = __fadd2_rn(y[c0 / 2 + i], make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])));
+            y[c * (kLdCols / 2) + i] = __fadd2_rn(
+                y[c * (kLdCols / 2) + i], make_float2(__uint_as_float(r[c & 1][2 * i]), __uint_as_float(r[c & 1][2 * i + 1])));
+          if (c + 1 < CW / kLdCols) tmem_wait_ld();
         }
         release(buf);
         phase ^= 1u << buf;
@@ -847,6 +871,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // S[m][b] = sum_{j in b} X[m][j] (fp32, j in increasing order); written as
 // out[m][p*G + b] = part p (p = 0: nearest bf16 of S, 1: of the remainder, 2: rest).
 __global__ void xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx, uint16_t *out, int64_t ldo) {
+  // the GEMM that follows may start its set-up now (it reads these sums only after
+  // this kernel completes)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t total = (int64_t)M * G;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t m = i / G;
@@ -990,6 +1017,8 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
     attr_set[dev].store(true, std::memory_order_relaxed);
   }
   pg::Params p;
+  p.wq = reinterpret_cast<const uint8_t *>(w->wq);
+  p.w_row_bytes = (int64_t)w->k * BITS / 8;
   p.scales = w->scales;
   p.biases = w->biases;
   p.sc_tma = sc_tma ? 1 : 0;
@@ -1023,13 +1052,18 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   cfg.blockDim = dim3((unsigned)pg::kThreads);
   cfg.dynamicSmemBytes = (size_t)C::kAlloc;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the CTAs start (barriers, tensor memory, tensor maps,
+  // the first weight tiles) while the row-sum pre-pass still runs; X, the row sums and
+  // the outputs are touched only after griddepcontrol.wait
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, pg::pgemm_kernel<BITS, EPI>, tmX, tmW, tmS, tmSc, tmBi, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return QL_ERR_LAUNCH;
