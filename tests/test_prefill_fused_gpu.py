@@ -34,7 +34,10 @@ def q():
     return qlinear
 
 
-SHAPES = [(4, 300, 1000, 2048), (6, 517, 512, 1024), (8, 64, 768, 2048), (4, 1024, 8192, 2048)]
+# the last shape is past the row count from which the codes are converted once per call
+# (the window of 100 rows below it is converted inside the GEMM: the two paths meet there)
+SHAPES = [(4, 300, 1000, 2048), (6, 517, 512, 1024), (8, 64, 768, 2048), (4, 1024, 8192, 2048),
+          (6, 2100, 1024, 2048)]
 
 
 @pytest.mark.parametrize("bits,m,n,k", SHAPES)
@@ -59,7 +62,8 @@ def test_pgemm_swiglu(q, bits, m, n, k):
     assert (np.abs(hg - h64) <= U.h_bound(a64, aa, c64, ac, h64)).all(), "h out of propagated bound"
 
 
-@pytest.mark.parametrize("bits,m,n,k", [(4, 300, 2048, 8192), (6, 1030, 1000, 2048), (8, 5, 2048, 2048)])
+@pytest.mark.parametrize("bits,m,n,k", [(4, 300, 2048, 8192), (6, 1030, 1000, 2048), (8, 5, 2048, 2048),
+                                        (8, 2200, 768, 2048)])
 def test_pgemm_resid_norm(q, bits, m, n, k):
     cid = 170 + bits
     w = U.weight(n, k, bits, config_id=cid, tensor_id=1)

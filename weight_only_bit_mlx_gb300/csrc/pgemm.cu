@@ -105,18 +105,22 @@ constexpr int kEpiBatch = 8;  // rows of the fused epilogues' global loads in fl
 constexpr int kEpiPrefetchLead = 8;  // k blocks before a tile's end at which its epilogue inputs are prefetched
 static_assert(kScStages >= kABufs + 2 + 1, "scale ring must outlast the converter/epilogue lag");
 
+// BITS = 4, 6, 8: packed W tiles, converted in the kernel.  BITS = 0 (kPre): the A
+// operand arrives ready as bf16 (codes converted once per call by wconv_kernel, bias
+// blocks appended), loaded by TMA with the 128-byte swizzle straight into the stage.
 template <int BITS> struct Cfg {
-  static constexpr int kRowBytes = BK * BITS / 8;        // packed bytes of one row per k block
-  static constexpr int kWBytes = BN * kRowBytes;         // packed W tile
-  static constexpr int kStages = 4;                      // TMA stages in flight (X/S half tile + packed W tile)
+  static constexpr bool kPre = BITS == 0;
+  static constexpr int kRowBytes = kPre ? BK * 2 : BK * BITS / 8;  // bytes of one row per k block
+  static constexpr int kWBytes = BN * kRowBytes;         // packed W tile (kPre: the bf16 A tile)
+  static constexpr int kStages = 4;                      // TMA stages in flight (X/S half tile + W tile)
   static constexpr int kOffX = 0;
   static constexpr int kOffW = kOffX + kStages * kXBytes;
   static constexpr int kOffA = (kOffW + kStages * kWBytes + 1023) / 1024 * 1024;
-  static constexpr int kOffSc = kOffA + kABufs * kABytes;
+  static constexpr int kOffSc = kOffA + (kPre ? 0 : kABufs * kABytes);
   // biases of the tile's rows, bf16, boxes of 8 groups: [kBiasG / 8][BN][8]
   static constexpr int kOffBias = kOffSc + kScStages * BN * 4;
   // scale boxes streamed by TMA, bf16 [2][BN][8]
-  static constexpr int kOffScBox = kOffBias + BN * kBiasG * 2;
+  static constexpr int kOffScBox = kOffBias + (kPre ? 0 : BN * kBiasG * 2);
   static constexpr int kOffBar = kOffScBox + 2 * BN * 8 * 2;
   // barriers: tma_full, tma_empty, a_full[kABufs], a_empty[kABufs], acc_full[2], acc_empty[2],
   //           sc_full, scb_full[2], scb_empty[2], bias_full, bias_empty, mma_done[2], pair_full[kPairRing]
@@ -307,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmSc,
                  const __grid_constant__ CUtensorMap tmBi, const __grid_constant__ Params p) {
   using C = Cfg<BITS>;
+  constexpr bool kPre = C::kPre;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sX = smem + C::kOffX;
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = pair; t < p.tiles && alive; t += npairs, ++tj) {
           // this CTA's channels and rows of X of tile t
           const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN, m0 = (t / p.tiles_n) * BM + (int)rank * BMH;
-          {
+          if constexpr (!kPre) {
             // the tile's packed rows (contiguous) into L2 ahead of their TMA loads: a
             // prompt window reads each weight tile once, straight from HBM
             const int rows = min(BN, p.N - n0);
@@ -455,7 +460,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               alive = false;
               break;
             }
-            if (kb < G) {
+            if constexpr (kPre) {
+              // the bf16 A tile (main or bias block) and X or the row-sum parts; A is
+              // written by the conversion pre-pass, so both wait for the earlier kernels
+              if (!dep_done) {
+                griddep_wait();
+                dep_done = true;
+              }
+              mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
+              tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * BK, n0);
+              if (kb < G)
+                tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
+              else
+                tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
+            } else if (kb < G) {
               mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
               tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
               if (!dep_done) {  // the weights are constant; X is written by earlier kernels
@@ -529,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(par * BM);
-            const uint64_t ad = sw128_desc(smem_addr(sA + ab * kABytes));
+            const uint64_t ad = sw128_desc(smem_addr(kPre ? sW + s * C::kWBytes : sA + ab * kABytes));
             const uint64_t bd = sw128_desc(smem_addr(sX + s * kXBytes));
   #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
@@ -575,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // UMMA 128-byte-swizzle K-major layout: 8-row groups 1024 bytes apart, rows 128
     // bytes apart, chunk c of row r at position c ^ (r % 8).
     const int ct = 32 * (warp & 3) + lane;  // channel (row of the W tile)
-    const bool bias_smem = G <= kBiasG;
+    // (kPre: the A tiles arrive ready by TMA; the converters only stage the scales)
+    const bool bias_smem = !kPre && G <= kBiasG;
     const uint32_t a_row = smem_addr(sA) + (uint32_t)((ct >> 3) * 1024 + (ct & 7) * 128);
     const uint32_t sw = (uint32_t)(ct & 7);
     bool alive = true;
@@ -632,28 +651,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t dst = a_row + (uint32_t)(ab * kABytes);
           if (kb < G) {
-            constexpr int NW = BK * BITS / 32;  // words of the row
-            uint32_t w[NW];
-            const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes;
+            if constexpr (!kPre) {
+              constexpr int NW = BK * BITS / 32;  // words of the row
+              uint32_t w[NW];
+              const uint8_t *wp = sW + s * C::kWBytes + ct * C::kRowBytes;
 #pragma unroll
-            for (int i = 0; i < NW / 4; ++i) {
-              uint4 v = lds128(wp + 16 * i);
-              w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-            }
+              for (int i = 0; i < NW / 4; ++i) {
+                uint4 v = lds128(wp + 16 * i);
+                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+              }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint32_t o[4];
-              convert_chunk<BITS, NW>(w, c, o);
-              sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+              for (int c = 0; c < 8; ++c) {
+                uint32_t o[4];
+                convert_chunk<BITS, NW>(w, c, o);
+                sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+              }
+              if (!p.bi_tma && bias_smem) sbias[((kb >> 3) * BN + ct) * 8 + (kb & 7)] = (uint16_t)b_cur;
             }
-            if (!p.bi_tma && bias_smem) sbias[((kb >> 3) * BN + ct) * 8 + (kb & 7)] = (uint16_t)b_cur;
             // Scale slot h % kScStages was last read by the epilogue for main block
             // h - kScStages.  Passing a_empty for this block means the MMA of the block
             // kABufs earlier finished, which waited for the epilogue to release the
             // accumulator use two main blocks before that; kScStages >= kABufs + 3 keeps
             // the slot free.
             sSc[(h % kScStages) * BN + ct] = bf16_to_f32(s_cur);
-          } else {
+          } else if constexpr (!kPre) {
             // bias block: column t of block jb is k' = 64*jb + t of the [part][group]
             // layout; its A value is bias[n][k' mod G] (zero past 3G)
             if (kb == G && p.bi_tma && !mbar_wait_bounded(bias_full, (uint32_t)(tj & 1), budget, abort_flag)) {
@@ -691,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               sts128(dst + ((((uint32_t)c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
             }
           }
-          fence_proxy_async_smem();  // the A tile is read by the tensor core (async proxy)
+          if constexpr (!kPre) fence_proxy_async_smem();  // the A tile is read by the tensor core (async proxy)
           mbar_arrive(&a_full[ab]);
           if (kb < G) {
             mbar_arrive(&sc_full[h % kScStages]);
@@ -902,6 +923,54 @@ __global__ void xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx, 
   }
 }
 
+// ---- the codes as exact bf16, once per call (large prompt windows) ------------------
+// A[r][j], rows kp = k + lds apart: for j < k the code q[r][j] as an exact bf16; for
+// k <= j < kp column j - k of the bias blocks, bias[r][(j - k) mod G] while j - k < 3G and
+// 0 after.  These are the values the converters write into the A tiles, so the GEMM
+// computes the same bits from either.
+template <int BITS>
+__global__ void wconv_kernel(const uint32_t *wq, const uint16_t *biases, int n, int k, int64_t kp, uint16_t *A) {
+  const int G = k / 64;
+  const int64_t per_row = kp / 8;  // 8-value chunks per row
+  const int64_t total = (int64_t)n * per_row;
+  const int64_t wpr = (int64_t)k * BITS / 32;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / per_row;
+    const int j0 = (int)(i - r * per_row) * 8;
+    uint32_t q[8];
+    if (j0 < k) {
+      const uint32_t *row = wq + r * wpr;
+      if constexpr (BITS == 4) {
+        const uint32_t w = row[j0 / 8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = (w >> (4 * e)) & 15u;
+      } else if constexpr (BITS == 8) {
+        const uint32_t w0 = row[j0 / 4], w1 = row[j0 / 4 + 1];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = ((e < 4 ? w0 : w1) >> (8 * (e & 3))) & 255u;
+      } else {
+        // bits 6 j0 .. 6 j0 + 47 lie in words wi, wi + 1 (the shift is 0 or 16)
+        const int64_t bit = (int64_t)6 * j0;
+        const int64_t wi = bit >> 5;
+        const int sh = (int)(bit & 31);
+        const uint64_t v = (uint64_t)row[wi] | ((uint64_t)row[wi + 1] << 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = (uint32_t)(v >> (sh + 6 * e)) & 63u;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[e] = f32_to_bf16_rn((float)q[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int jj = j0 - k + e;
+        q[e] = jj < 3 * G ? (uint32_t)biases[r * G + jj % G] : 0u;
+      }
+    }
+    *reinterpret_cast<uint4 *>(A + r * kp + j0) =
+        make_uint4(q[0] | (q[1] << 16), q[2] | (q[3] << 16), q[4] | (q[5] << 16), q[6] | (q[7] << 16));
+  }
+}
+
 }  // namespace pg
 
 // ---- host side -----------------------------------------------------------------------
@@ -931,23 +1000,25 @@ static bool make_map(CUtensorMap *map, CUtensorMapDataType dt, const void *base,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Library-owned scratch for the split row sums: one growable buffer per device.
+// Library-owned scratch: one growable buffer per device and use (slot 0: the split row
+// sums; slot 1: the codes converted once per call for large windows).
 constexpr int kMaxDev = 64;
+constexpr int kScratchSlots = 2;
 static std::mutex g_scratch_mu;
-static void *g_scratch[kMaxDev];
-static size_t g_scratch_bytes[kMaxDev];
+static void *g_scratch[kScratchSlots][kMaxDev];
+static size_t g_scratch_bytes[kScratchSlots][kMaxDev];
 
-static void *scratch_get(size_t bytes) {
+static void *scratch_get(int slot, size_t bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_bytes[dev] < bytes) {
-    if (g_scratch[dev] != nullptr) {
+  if (g_scratch_bytes[slot][dev] < bytes) {
+    if (g_scratch[slot][dev] != nullptr) {
       // earlier launches may still read the old buffer
       if (cudaDeviceSynchronize() != cudaSuccess) return nullptr;
-      cudaFree(g_scratch[dev]);
-      g_scratch[dev] = nullptr;
-      g_scratch_bytes[dev] = 0;
+      cudaFree(g_scratch[slot][dev]);
+      g_scratch[slot][dev] = nullptr;
+      g_scratch_bytes[slot][dev] = 0;
     }
     size_t cap = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
     void *p = nullptr;
@@ -955,10 +1026,10 @@ static void *scratch_get(size_t bytes) {
       (void)cudaGetLastError();
       return nullptr;
     }
-    g_scratch[dev] = p;
-    g_scratch_bytes[dev] = cap;
+    g_scratch[slot][dev] = p;
+    g_scratch_bytes[slot][dev] = cap;
   }
-  return g_scratch[dev];
+  return g_scratch[slot][dev];
 }
 
 // SMs of the current device (cached per device)
@@ -976,16 +1047,26 @@ static int sm_count() {
 
 template <int BITS, int EPI>
 static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
-                        const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi) {
+                        const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi,
+                        const uint16_t *apre = nullptr) {
   using C = pg::Cfg<BITS>;
   const int G = w->k / 64;
   CUtensorMap tmX, tmW, tmS, tmSc, tmBi;
   if (!make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)w->k, (uint64_t)m, (uint64_t)ldx * 2, pg::BK,
                 pg::BMH, CU_TENSOR_MAP_SWIZZLE_128B))
     return QL_ERR_CUDA;
-  if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, w->wq, (uint64_t)w->k * BITS / 32, (uint64_t)w->n,
-                (uint64_t)w->k * BITS / 8, pg::BK * BITS / 32, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return QL_ERR_CUDA;
+  if constexpr (C::kPre) {
+    // the converted codes and bias blocks, bf16 [n][k + lds], boxes of 64 x 128 rows in
+    // the 128-byte swizzle the tensor core reads
+    const uint64_t kp = (uint64_t)w->k + (uint64_t)lds;
+    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, apre, kp, (uint64_t)w->n, kp * 2, pg::BK, pg::BN,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+      return QL_ERR_CUDA;
+  } else {
+    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, w->wq, (uint64_t)w->k * BITS / 32, (uint64_t)w->n,
+                  (uint64_t)w->k * BITS / 8, pg::BK * BITS / 32, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return QL_ERR_CUDA;
+  }
   if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, (uint64_t)(3 * G), (uint64_t)m, (uint64_t)lds * 2,
                 pg::BK, pg::BMH, CU_TENSOR_MAP_SWIZZLE_128B))
     return QL_ERR_CUDA;
@@ -994,7 +1075,7 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
                      (reinterpret_cast<uintptr_t>(w->biases) & 15) == 0;
   const bool sc_tma = sb_ok && make_map(&tmSc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w->scales, (uint64_t)G,
                                         (uint64_t)w->n, (uint64_t)G * 2, 8, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
-  const bool bi_tma = sc_tma && G <= pg::kBiasG &&
+  const bool bi_tma = !C::kPre && sc_tma && G <= pg::kBiasG &&
                       make_map(&tmBi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w->biases, (uint64_t)G, (uint64_t)w->n,
                                (uint64_t)G * 2, 8, pg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!sc_tma) tmSc = tmX;  // never read
@@ -1018,7 +1099,7 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   }
   pg::Params p;
   p.wq = reinterpret_cast<const uint8_t *>(w->wq);
-  p.w_row_bytes = (int64_t)w->k * BITS / 8;
+  p.w_row_bytes = C::kPre ? 0 : (int64_t)w->k * BITS / 8;
   p.scales = w->scales;
   p.biases = w->biases;
   p.sc_tma = sc_tma ? 1 : 0;
@@ -1129,25 +1210,47 @@ int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx,
 
 template <int BITS>
 static int launch_epi(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
-                      const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi) {
+                      const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi,
+                      const uint16_t *apre = nullptr) {
   switch (epi ? epi->mode : kPgStore) {
-    case kPgSwiglu: return launch_pgemm<BITS, kPgSwiglu>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
-    case kPgResid: return launch_pgemm<BITS, kPgResid>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
-    default: return launch_pgemm<BITS, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    case kPgSwiglu: return launch_pgemm<BITS, kPgSwiglu>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
+    case kPgResid: return launch_pgemm<BITS, kPgResid>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
+    default: return launch_pgemm<BITS, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
   }
 }
+
+// From this many rows on, the codes are converted once per call (wconv_kernel) and the
+// GEMM loads them ready (Cfg<0>): the conversion then costs one pass over W instead of
+// one per 256-row band.  Smaller windows convert inside the GEMM.  Both give the same bits.
+constexpr int kPreRows = 2048;
 
 int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy, cudaStream_t st,
               int *status, const PgEpilogue *epi) {
   const int G = w->k / 64;
   const int64_t lds = ((3 * (int64_t)G + 63) / 64) * 64;  // row pitch of the split sums (elements)
-  uint16_t *S = static_cast<uint16_t *>(scratch_get((size_t)m * lds * 2));
+  uint16_t *S = static_cast<uint16_t *>(scratch_get(0, (size_t)m * lds * 2));
   if (S == nullptr) return QL_ERR_NOMEM;
+  uint16_t *apre = nullptr;
+  if (m >= kPreRows) {
+    const int64_t kp = (int64_t)w->k + lds;
+    apre = static_cast<uint16_t *>(scratch_get(1, (size_t)w->n * (size_t)kp * 2));
+    if (apre == nullptr) return QL_ERR_NOMEM;
+    const int64_t chunks = (int64_t)w->n * (kp / 8);
+    int cblocks = (int)((chunks + 255) / 256);
+    if (cblocks > 16384) cblocks = 16384;
+    switch (w->bits) {
+      case 4: pg::wconv_kernel<4><<<cblocks, 256, 0, st>>>(w->wq, w->biases, w->n, w->k, kp, apre); break;
+      case 6: pg::wconv_kernel<6><<<cblocks, 256, 0, st>>>(w->wq, w->biases, w->n, w->k, kp, apre); break;
+      default: pg::wconv_kernel<8><<<cblocks, 256, 0, st>>>(w->wq, w->biases, w->n, w->k, kp, apre); break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+  }
   const int64_t total = (int64_t)m * G;
   int blocks = (int)((total + 255) / 256);
   if (blocks > 8192) blocks = 8192;
   pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+  if (apre != nullptr) return launch_epi<0>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
   switch (w->bits) {
     case 4: return launch_epi<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
     case 6: return launch_epi<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
