@@ -49,7 +49,9 @@ PROMPT = 8192
 
 # DRAM traffic per launch of the dominant kernels from one ncu capture, keyed to the
 # hash of the kernel source it was taken on; reported as null once the source changes.
-NCU_TRAFFIC = {"48270a3c5b8728c1": 46427648 + 208977920}  # pgemm M=8192 N=8192 K=2048, 4-bit (device code as captured)
+# rows from which the library converts the codes once per prompt-GEMM call (one more launch)
+PRE_ROWS = 2048
+NCU_TRAFFIC = {"cd46dfba42df64d6": 130175232 + 231619584}  # pgemm M=8192 N=8192 K=2048, 4-bit (device code as captured)
 
 
 def parse():
@@ -497,6 +499,9 @@ class Sweep:
         GEMM's epilogue plus the norm, or the plain GEMM plus qresid_rmsnorm).
         Returns the number of launches."""
         W, n, q = self.W, 0, self.q
+        # launches of one prompt-GEMM call: the row-sum pre-pass and the GEMM, plus the
+        # once-per-call code conversion from PRE_ROWS rows on
+        pg = 3 if hi - lo >= PRE_ROWS else 2
         X, Patt = self.X[lo:hi], self.Patt[lo:hi]
         Pa, Pc, Ph = self.Pa[lo:hi], self.Pc[lo:hi], self.Ph[lo:hi]
         Pq, Pkv, Pout = self.Pq[lo:hi], self.Pkv[lo:hi], self.Pout[lo:hi]
@@ -506,10 +511,10 @@ class Sweep:
             nonlocal n
             if post == "fused":
                 q.qlinear_pgemm_resid_norm(w, Xin, R, self.pgamma, 1e-5, out=Rn)
-                n += 3
+                n += pg + 1
             else:
                 self._pgemm(w, Xin, Pout, timed)
-                n += 2
+                n += pg
                 if post == "unfused":
                     q.qresid_rmsnorm(Pout, R, self.pgamma, 1e-5, out=Rn)
                     n += 1
@@ -521,18 +526,18 @@ class Sweep:
                 self._pgemm(W[p + "k"], X, Pkv, timed)
                 self._pgemm(W[p + "v"], X, Pkv, timed)
                 self._pgemm(W[p + "g"], X, Pq, timed)
-                n += 8
+                n += 4 * pg
                 down(W[p + "o"], Patt)
             self._pgemm(W[p + "w1"], X, Pa, timed)
-            n += 2
+            n += pg
             if fused:
                 self._timed_call(lambda: q.qlinear_pgemm_swiglu(W[p + "w3"], X, Pa, Ph), timed,
                                  2 * X.shape[0] * W[p + "w3"].n * W[p + "w3"].k, "swiglu")
-                n += 2
+                n += pg
             else:
                 self._pgemm(W[p + "w3"], X, Pc, timed)
                 q.qswiglu(Pa, Pc, Ph)
-                n += 3
+                n += pg + 1
             down(W[p + "w2"], Ph)
         return n
 
@@ -839,8 +844,9 @@ def run_ours(args):
                                     "every window streams every weight again (64 x the sweep's weight bytes)"},
         "tok_s_note": "modelled from the linear layers only: decode R / (decode pass time), prefill "
                       "prompt rows / (prefill pass time); attention, norms and sampling excluded",
-        "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm (row-sum pre-pass + tcgen05 GEMM), "
-                                                  f"M={PROMPT} N={D_FF} K={D_MODEL} launches (w1, w3)",
+        "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm (code conversion + row-sum pre-pass + tcgen05 "
+                                                  f"GEMM, timed together), M={PROMPT} N={D_FF} K={D_MODEL} launches "
+                                                  "(w1, w3)",
                      "achieved": ffn_tflops, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                      "frac": ffn_tflops / pk["bf16_sus"], "frac_of_burst": ffn_tflops / pk["bf16"],
                      "traffic": traffic,

@@ -130,10 +130,13 @@ int qattn_proj_mv(const ql_weight *wq, const ql_weight *wk, const ql_weight *wv,
  *   X: bf16 [m, ldx] (16-byte aligned, ldx % 8 == 0); Y: float [m, ldy] (ldy >= n).
  *   m may be 0: then nothing is checked beyond the weight and nothing is enqueued
  *   (X and Y may be NULL).  Uses a library-owned device scratch buffer of
- *   m * round_up(3*k/64, 64) bf16 values for the split row sums, allocated with
+ *   m * round_up(3*k/64, 64) bf16 values for the split row sums and, when m >= 2048,
+ *   a second one of n * (k + round_up(3*k/64, 64)) bf16 values into which the codes
+ *   are converted once per call (exactly the values the kernel converts for smaller
+ *   m, so the result is the same bits either way).  Both are allocated with
  *   cudaMalloc on first need per device and grown on demand (growth synchronizes
  *   the device); calls on one device must be ordered on one stream because they
- *   share that buffer.
+ *   share them.
  */
 int qlinear_pgemm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, float *Y,
                   int64_t ldy, void *stream);
