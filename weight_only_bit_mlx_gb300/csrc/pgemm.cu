@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t d = tmem_base + (uint32_t)(par * BM);
             const uint64_t ad = sw128_desc(smem_addr(kPre ? sW + s * C::kWBytes : sA + ab * kABytes));
             const uint64_t bd = sw128_desc(smem_addr(sX + s * kXBytes));
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint32_t acc = (kk > 0 || !opens) ? 1u : 0u;
               mma_bf16_ss2(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
