@@ -136,7 +136,7 @@ int qattn_proj_mv(const ql_weight *wq, const ql_weight *wk, const ql_weight *wv,
  *   m, so the result is the same bits either way).  Both are allocated with
  *   cudaMalloc on first need per device and grown on demand (growth synchronizes
  *   the device); calls on one device must be ordered on one stream because they
- *   share them.
+ *   share them.  QL_ERR_TOO_LARGE if m * k/64 >= 2^31.
  */
 int qlinear_pgemm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, float *Y,
                   int64_t ldy, void *stream);

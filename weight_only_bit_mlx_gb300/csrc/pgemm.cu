@@ -891,36 +891,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---- row sums, split exactly into three bf16 parts ------------------------------
 // S[m][b] = sum_{j in b} X[m][j] (fp32, j in increasing order); written as
 // out[m][p*G + b] = part p (p = 0: nearest bf16 of S, 1: of the remainder, 2: rest).
-__global__ void xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx, uint16_t *out, int64_t ldo) {
+// A CTA takes kXsumPairs consecutive (m, b) pairs: it first stages their 128-byte blocks
+// of X in shared memory with coalesced 16-byte loads (16-byte chunk c of pair q at
+// position c ^ (q % 8), so neither the stores nor the reads below collide on a bank),
+// then each thread sums its own block in order.
+constexpr int kXsumPairs = 256;
+__global__ void __launch_bounds__(kXsumPairs) xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx,
+                                                                uint16_t *out, int64_t ldo) {
   // the GEMM that follows may start its set-up now (it reads these sums only after
   // this kernel completes)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t total = (int64_t)M * G;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t m = i / G;
-    const int b = (int)(i % G);
-    const uint16_t *xr = X + m * ldx + (int64_t)b * 64;
-    float s = 0.0f;
+  __shared__ __align__(16) uint4 stage[kXsumPairs * 8];
+  const int total = M * G;  // the host keeps this below 2^31
+  const int p0 = blockIdx.x * kXsumPairs;
 #pragma unroll
-    for (int v = 0; v < 8; ++v) {
-      const uint4 u = ldg_v4(xr + 8 * v);
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s = __fadd_rn(s, bf16_to_f32(wv[e] & 0xFFFFu));
-        s = __fadd_rn(s, bf16_to_f32(wv[e] >> 16));
-      }
+  for (int v = 0; v < 8; ++v) {
+    const int qi = threadIdx.x + kXsumPairs * v;  // chunk qi % 8 of pair qi / 8
+    const int q = qi >> 3, c = qi & 7;
+    const int pr = p0 + q;
+    if (pr < total) {
+      const int m = pr / G, b = pr - m * G;
+      stage[q * 8 + (c ^ (q & 7))] = ldg_v4(X + (int64_t)m * ldx + (int64_t)b * 64 + 8 * c);
     }
-    const uint16_t h0 = f32_to_bf16_rn(s);
-    const float r1 = __fsub_rn(s, bf16_to_f32(h0));
-    const uint16_t h1 = f32_to_bf16_rn(r1);
-    const float r2 = __fsub_rn(r1, bf16_to_f32(h1));
-    const uint16_t h2 = f32_to_bf16_rn(r2);
-    uint16_t *o = out + m * ldo + b;
-    o[0] = h0;
-    o[G] = h1;
-    o[2 * G] = h2;
   }
+  __syncthreads();
+  const int q = threadIdx.x, pr = p0 + q;
+  if (pr >= total) return;
+  float s = 0.0f;
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const uint4 u = stage[q * 8 + (v ^ (q & 7))];
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s = __fadd_rn(s, bf16_to_f32(wv[e] & 0xFFFFu));
+      s = __fadd_rn(s, bf16_to_f32(wv[e] >> 16));
+    }
+  }
+  const uint16_t h0 = f32_to_bf16_rn(s);
+  const float r1 = __fsub_rn(s, bf16_to_f32(h0));
+  const uint16_t h1 = f32_to_bf16_rn(r1);
+  const float r2 = __fsub_rn(r1, bf16_to_f32(h1));
+  const uint16_t h2 = f32_to_bf16_rn(r2);
+  const int m = pr / G, b = pr - m * G;
+  uint16_t *o = out + (int64_t)m * ldo + b;
+  o[0] = h0;
+  o[G] = h1;
+  o[2 * G] = h2;
 }
 
 // ---- the codes as exact bf16, once per call (large prompt windows) ------------------
@@ -931,15 +948,15 @@ __global__ void xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx, 
 template <int BITS>
 __global__ void wconv_kernel(const uint32_t *wq, const uint16_t *biases, int n, int k, int64_t kp, uint16_t *A) {
   const int G = k / 64;
-  const int64_t per_row = kp / 8;  // 8-value chunks per row
-  const int64_t total = (int64_t)n * per_row;
+  const int per_row = (int)(kp / 8);  // 8-value chunks per row
+  const int total = n * per_row;      // the host keeps this below 2^31
   const int64_t wpr = (int64_t)k * BITS / 32;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / per_row;
-    const int j0 = (int)(i - r * per_row) * 8;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int r = i / per_row;
+    const int j0 = (i - r * per_row) * 8;
     uint32_t q[8];
     if (j0 < k) {
-      const uint32_t *row = wq + r * wpr;
+      const uint32_t *row = wq + (int64_t)r * wpr;
       if constexpr (BITS == 4) {
         const uint32_t w = row[j0 / 8];
 #pragma unroll
@@ -963,10 +980,10 @@ __global__ void wconv_kernel(const uint32_t *wq, const uint16_t *biases, int n, 
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int jj = j0 - k + e;
-        q[e] = jj < 3 * G ? (uint32_t)biases[r * G + jj % G] : 0u;
+        q[e] = jj < 3 * G ? (uint32_t)biases[(int64_t)r * G + jj % G] : 0u;
       }
     }
-    *reinterpret_cast<uint4 *>(A + r * kp + j0) =
+    *reinterpret_cast<uint4 *>(A + (int64_t)r * kp + j0) =
         make_uint4(q[0] | (q[1] << 16), q[2] | (q[3] << 16), q[4] | (q[5] << 16), q[6] | (q[7] << 16));
   }
 }
@@ -1197,9 +1214,9 @@ int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx,
   // every scratch value the GEMM reads is written by this pre-pass first, so nothing
   // left by an earlier call needs clearing
   const int64_t total = (int64_t)m * G;
-  int blocks = (int)((total + 255) / 256);
-  if (blocks > 8192) blocks = 8192;
-  pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
+  if (total >= (int64_t(1) << 31)) return QL_ERR_TOO_LARGE;
+  const int blocks = (int)((total + pg::kXsumPairs - 1) / pg::kXsumPairs);
+  pg::xsum_split_kernel<<<blocks, pg::kXsumPairs, 0, st>>>(X, m, G, ldx, S, lds);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   switch (w->bits) {
     case 4: return launch_pgemm<4, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
@@ -1231,7 +1248,7 @@ int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *
   uint16_t *S = static_cast<uint16_t *>(scratch_get(0, (size_t)m * lds * 2));
   if (S == nullptr) return QL_ERR_NOMEM;
   uint16_t *apre = nullptr;
-  if (m >= kPreRows) {
+  if (m >= kPreRows && (int64_t)w->n * (((int64_t)w->k + lds) / 8) < (int64_t(1) << 31)) {
     const int64_t kp = (int64_t)w->k + lds;
     apre = static_cast<uint16_t *>(scratch_get(1, (size_t)w->n * (size_t)kp * 2));
     if (apre == nullptr) return QL_ERR_NOMEM;
@@ -1246,9 +1263,9 @@ int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *
     if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   }
   const int64_t total = (int64_t)m * G;
-  int blocks = (int)((total + 255) / 256);
-  if (blocks > 8192) blocks = 8192;
-  pg::xsum_split_kernel<<<blocks, 256, 0, st>>>(X, m, G, ldx, S, lds);
+  if (total >= (int64_t(1) << 31)) return QL_ERR_TOO_LARGE;
+  const int blocks = (int)((total + pg::kXsumPairs - 1) / pg::kXsumPairs);
+  pg::xsum_split_kernel<<<blocks, pg::kXsumPairs, 0, st>>>(X, m, G, ldx, S, lds);
   if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   if (apre != nullptr) return launch_epi<0>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
   switch (w->bits) {
