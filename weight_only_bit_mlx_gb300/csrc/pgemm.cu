@@ -896,11 +896,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // position c ^ (q % 8), so neither the stores nor the reads below collide on a bank),
 // then each thread sums its own block in order.
 constexpr int kXsumPairs = 256;
-__global__ void __launch_bounds__(kXsumPairs) xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx,
-                                                                uint16_t *out, int64_t ldo) {
-  // the GEMM that follows may start its set-up now (it reads these sums only after
-  // this kernel completes)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+__device__ __forceinline__ void xsum_body(const uint16_t *X, int M, int G, int64_t ldx, uint16_t *out,
+                                          int64_t ldo) {
   __shared__ __align__(16) uint4 stage[kXsumPairs * 8];
   const int total = M * G;  // the host keeps this below 2^31
   const int p0 = blockIdx.x * kXsumPairs;
@@ -940,6 +937,20 @@ __global__ void __launch_bounds__(kXsumPairs) xsum_split_kernel(const uint16_t *
   o[2 * G] = h2;
 }
 
+__global__ void __launch_bounds__(kXsumPairs) xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx,
+                                                                uint16_t *out, int64_t ldo) {
+  // the GEMM that follows may start its set-up now (it reads these sums only after
+  // this kernel completes)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  xsum_body(X, M, G, ldx, out, ldo);
+  // When launched right after the code conversion with programmatic dependent launch,
+  // this kernel runs beside it (it reads only X, which the kernels before the conversion
+  // wrote); it ends only after the conversion has, so that the GEMM's dependency wait
+  // covers both.  Launched plainly, the wait returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+
 // ---- the codes as exact bf16, once per call (large prompt windows) ------------------
 // A[r][j], rows kp = k + lds apart: for j < k the code q[r][j] as an exact bf16; for
 // k <= j < kp column j - k of the bias blocks, bias[r][(j - k) mod G] while j - k < 3G and
@@ -947,6 +958,8 @@ __global__ void __launch_bounds__(kXsumPairs) xsum_split_kernel(const uint16_t *
 // computes the same bits from either.
 template <int BITS>
 __global__ void wconv_kernel(const uint32_t *wq, const uint16_t *biases, int n, int k, int64_t kp, uint16_t *A) {
+  // the row-sum pre-pass that follows reads only X: it may run beside this kernel
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int G = k / 64;
   const int per_row = (int)(kp / 8);  // 8-value chunks per row
   const int total = n * per_row;      // the host keeps this below 2^31
@@ -1203,6 +1216,28 @@ static int noalloc_scratch_addr(uint16_t **out) {
 
 int64_t pgemm_noalloc_max_elems() { return kNoAllocScratchElems; }
 
+// The row-sum pre-pass over m rows; with `beside` it is launched with programmatic
+// dependent launch right after the code conversion, so the two run together.
+static int launch_xsum(const uint16_t *X, int m, int G, int64_t ldx, uint16_t *S, int64_t lds, cudaStream_t st,
+                       bool beside) {
+  const int64_t total = (int64_t)m * G;
+  if (total >= (int64_t(1) << 31)) return QL_ERR_TOO_LARGE;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((total + pg::kXsumPairs - 1) / pg::kXsumPairs));
+  cfg.blockDim = dim3((unsigned)pg::kXsumPairs);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = beside ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, pg::xsum_split_kernel, X, m, G, ldx, S, lds) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return QL_ERR_LAUNCH;
+  }
+  return QL_OK;
+}
+
 int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
                       cudaStream_t st, int *status) {
   const int G = w->k / 64;
@@ -1213,11 +1248,7 @@ int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx,
   if (e) return e;
   // every scratch value the GEMM reads is written by this pre-pass first, so nothing
   // left by an earlier call needs clearing
-  const int64_t total = (int64_t)m * G;
-  if (total >= (int64_t(1) << 31)) return QL_ERR_TOO_LARGE;
-  const int blocks = (int)((total + pg::kXsumPairs - 1) / pg::kXsumPairs);
-  pg::xsum_split_kernel<<<blocks, pg::kXsumPairs, 0, st>>>(X, m, G, ldx, S, lds);
-  if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+  if (int e2 = launch_xsum(X, m, G, ldx, S, lds, st, false)) return e2;
   switch (w->bits) {
     case 4: return launch_pgemm<4, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
     case 6: return launch_pgemm<6, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
@@ -1262,11 +1293,7 @@ int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *
     }
     if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
   }
-  const int64_t total = (int64_t)m * G;
-  if (total >= (int64_t(1) << 31)) return QL_ERR_TOO_LARGE;
-  const int blocks = (int)((total + pg::kXsumPairs - 1) / pg::kXsumPairs);
-  pg::xsum_split_kernel<<<blocks, pg::kXsumPairs, 0, st>>>(X, m, G, ldx, S, lds);
-  if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+  if (int e2 = launch_xsum(X, m, G, ldx, S, lds, st, apre != nullptr)) return e2;
   if (apre != nullptr) return launch_epi<0>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
   switch (w->bits) {
     case 4: return launch_epi<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
