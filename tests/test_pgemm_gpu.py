@@ -128,3 +128,23 @@ def test_several_tiles_per_cta_long_k(q, bits, k):
     rows.sort()
     y64, A = orc.pgemm(X[rows], w)
     U.assert_close(Y[torch.from_numpy(rows).cuda()], y64, A, f"pgemm several tiles bits={bits} k={k}")
+
+
+@pytest.mark.parametrize("bits,m,n,k", [(4, 2300, 1000, 1024), (6, 2049, 333, 2048), (8, 2200, 520, 512)])
+def test_large_windows_ragged_against_windows(q, bits, m, n, k):
+    # From 2048 rows on the codes are converted once per call; below, inside the GEMM.
+    # Ragged m and n (partial row and channel tiles) on the first path against the same
+    # rows cut into windows of 512 (the second path), bit for bit, and sampled rows
+    # against the float64 oracle.
+    w = U.weight(n, k, bits, config_id=62, tensor_id=bits)
+    X = synth.make_x(m, k, config_id=62)
+    wd, Xd = U.dev_weight(w), U.dev_x(X)
+    Y = q.qlinear_pgemm(wd, Xd)
+    Yw = torch.cat([q.qlinear_pgemm(wd, Xd[lo:lo + 512]) for lo in range(0, m, 512)])
+    torch.cuda.synchronize()
+    assert q.qlinear_last_error() == q.QL_OK
+    assert torch.equal(Yw, Y), "windows of 512 differ from one call"
+    rows = np.sort(np.random.default_rng(bits).choice(m, size=24, replace=False))
+    rows[-1] = m - 1  # the last, partial row tile
+    y64, A = orc.pgemm(X[rows], w)
+    U.assert_close(Y[torch.from_numpy(rows).cuda()], y64, A, f"pgemm bits={bits} m={m} n={n} k={k}")
