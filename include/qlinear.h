@@ -131,12 +131,16 @@ int qattn_proj_mv(const ql_weight *wq, const ql_weight *wk, const ql_weight *wv,
  *   m may be 0: then nothing is checked beyond the weight and nothing is enqueued
  *   (X and Y may be NULL).  Uses a library-owned device scratch buffer of
  *   m * round_up(3*k/64, 64) bf16 values for the split row sums and, when m >= 2048,
- *   a second one of n * (k + round_up(3*k/64, 64)) bf16 values into which the codes
- *   are converted once per call (exactly the values the kernel converts for smaller
- *   m, so the result is the same bits either way).  Both are allocated with
- *   cudaMalloc on first need per device and grown on demand (growth synchronizes
- *   the device); calls on one device must be ordered on one stream because they
- *   share them.  QL_ERR_TOO_LARGE if m * k/64 >= 2^31.
+ *   two more of n * (k + round_up(3*k/64, 64)) bf16 values into which the codes are
+ *   converted once per call (exactly the values the kernel converts for smaller m, so
+ *   the result is the same bits either way); such calls alternate between the two, so
+ *   that a call's conversion may run on the SMs the previous call's GEMM leaves idle
+ *   in its last tiles.  All are allocated with cudaMalloc on first need per device and
+ *   grown on demand (growth synchronizes the device); calls on one device must be
+ *   ordered on one stream because they share them.  A kernel the caller launches
+ *   between two calls with programmatic dependent launch must wait for the kernel
+ *   before it (griddepcontrol.wait) before it ends, as the library's own kernels do.
+ *   QL_ERR_TOO_LARGE if m * k/64 >= 2^31.
  */
 int qlinear_pgemm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, float *Y,
                   int64_t ldy, void *stream);

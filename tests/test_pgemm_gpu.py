@@ -148,3 +148,49 @@ def test_large_windows_ragged_against_windows(q, bits, m, n, k):
     rows[-1] = m - 1  # the last, partial row tile
     y64, A = orc.pgemm(X[rows], w)
     U.assert_close(Y[torch.from_numpy(rows).cuda()], y64, A, f"pgemm bits={bits} m={m} n={n} k={k}")
+
+
+def test_back_to_back_large_calls_bit_exact(q):
+    # Calls of 2048 rows and more convert their codes in a kernel that may start while
+    # the previous call's GEMM still runs its last tiles (calls alternate between two
+    # buffers of converted codes), and the row sums wait for the kernel before them.
+    # Here large calls follow each other with no synchronization, on weights of other
+    # shapes and widths, and one call's fused epilogue writes the next call's X.  Every
+    # output must equal the same call made alone.
+    m, eps = 2048, 1e-5
+    specs = [(8192, 8192, 4), (4096, 2048, 6), (2048, 4096, 8), (8192, 2048, 4), (1000, 1024, 8)]
+    ws = [U.dev_weight(U.weight(n, k, b, config_id=64, tensor_id=i)) for i, (n, k, b) in enumerate(specs)]
+    X8 = U.dev_x(synth.make_x(m, 8192, config_id=64))
+    X2 = U.dev_x(synth.make_x(m, 2048, config_id=65))
+    X4 = U.dev_x(synth.make_x(m, 4096, config_id=66))
+    r0 = U.dev_x(synth.make_bf16((m, 4096), config_id=64, tensor_id=9))
+    gamma = U.dev_x(synth.make_bf16((4096,), 0.5, 1.5, config_id=64, tensor_id=10))
+
+    def run():
+        r = r0.clone()
+        ys = [q.qlinear_pgemm(ws[0], X8)]
+        ys.append(q.qlinear_pgemm(ws[1], X2))
+        h = q.qlinear_pgemm_resid_norm(ws[1], X2, r, gamma, eps)  # h: [m, 4096] bf16
+        ys.append(q.qlinear_pgemm(ws[2], h))                       # X written just before
+        ys.append(q.qlinear_pgemm(ws[3], X2))
+        ys.append(q.qlinear_pgemm(ws[4], X2[:, :1024].contiguous()))
+        ys.append(q.qlinear_pgemm(ws[2], X4))
+        return ys, h, r
+
+    ys, h, r = run()  # back to back
+    torch.cuda.synchronize()
+    assert q.qlinear_last_error() == q.QL_OK
+    ref = []
+    rr = r0.clone()
+    for fn in [lambda: q.qlinear_pgemm(ws[0], X8), lambda: q.qlinear_pgemm(ws[1], X2),
+               lambda: q.qlinear_pgemm_resid_norm(ws[1], X2, rr, gamma, eps)]:
+        ref.append(fn())
+        torch.cuda.synchronize()
+    h_ref = ref.pop()
+    for w, x in [(ws[2], h_ref), (ws[3], X2), (ws[4], X2[:, :1024].contiguous()), (ws[2], X4)]:
+        ref.append(q.qlinear_pgemm(w, x))
+        torch.cuda.synchronize()
+    assert torch.equal(h.view(torch.int16), h_ref.view(torch.int16)), "fused epilogue output"
+    assert torch.equal(r.view(torch.int16), rr.view(torch.int16)), "stored residual"
+    for i, (a, b) in enumerate(zip(ys, ref)):
+        assert torch.equal(a, b), f"call {i} differs from the same call made alone"

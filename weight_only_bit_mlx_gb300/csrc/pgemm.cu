@@ -403,7 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0, box = 0, tj = 0, bias_sets = 0;
         bool alive = true;
         bool dep_done = false;  // griddep_wait() passed: X and the row sums may be read
+        bool released = false;  // the kernels launched after this one may start
         for (int t = pair; t < p.tiles && alive; t += npairs, ++tj) {
+          const bool last_tile = t + npairs >= p.tiles;
           // this CTA's channels and rows of X of tile t
           const int n0 = (t % p.tiles_n) * (2 * BN) + (int)rank * BN, m0 = (t / p.tiles_n) * BM + (int)rank * BMH;
           if constexpr (!kPre) {
@@ -490,6 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
             }
             ++g;
+            if (last_tile && dep_done && !released) {
+              // This CTA has started its last tile: a kernel launched after this one
+              // with programmatic dependent launch (the next call's code conversion)
+              // may take the SMs that the pairs without a tile left leave idle.  Only
+              // after griddep_wait(), so that every kernel before this one has ended.
+              asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+              released = true;
+            }
           }
         }
         // drain: every copy this CTA started must land before its shared memory goes away
@@ -891,63 +901,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---- row sums, split exactly into three bf16 parts ------------------------------
 // S[m][b] = sum_{j in b} X[m][j] (fp32, j in increasing order); written as
 // out[m][p*G + b] = part p (p = 0: nearest bf16 of S, 1: of the remainder, 2: rest).
-// A CTA takes kXsumPairs consecutive (m, b) pairs: it first stages their 128-byte blocks
+// A tile is kXsumPairs consecutive (m, b) pairs.  A CTA stages a tile's 128-byte blocks
 // of X in shared memory with coalesced 16-byte loads (16-byte chunk c of pair q at
 // position c ^ (q % 8), so neither the stores nor the reads below collide on a bank),
-// then each thread sums its own block in order.
+// then each thread sums its own block in order.  The grid is at most one wave: a CTA
+// walks tiles gridDim.x apart and loads its next tile into registers while it sums the
+// current one.
 constexpr int kXsumPairs = 256;
-__device__ __forceinline__ void xsum_body(const uint16_t *X, int M, int G, int64_t ldx, uint16_t *out,
-                                          int64_t ldo) {
-  __shared__ __align__(16) uint4 stage[kXsumPairs * 8];
-  const int total = M * G;  // the host keeps this below 2^31
-  const int p0 = blockIdx.x * kXsumPairs;
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    const int qi = threadIdx.x + kXsumPairs * v;  // chunk qi % 8 of pair qi / 8
-    const int q = qi >> 3, c = qi & 7;
-    const int pr = p0 + q;
-    if (pr < total) {
-      const int m = pr / G, b = pr - m * G;
-      stage[q * 8 + (c ^ (q & 7))] = ldg_v4(X + (int64_t)m * ldx + (int64_t)b * 64 + 8 * c);
-    }
-  }
-  __syncthreads();
-  const int q = threadIdx.x, pr = p0 + q;
-  if (pr >= total) return;
-  float s = 0.0f;
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    const uint4 u = stage[q * 8 + (v ^ (q & 7))];
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      s = __fadd_rn(s, bf16_to_f32(wv[e] & 0xFFFFu));
-      s = __fadd_rn(s, bf16_to_f32(wv[e] >> 16));
-    }
-  }
-  const uint16_t h0 = f32_to_bf16_rn(s);
-  const float r1 = __fsub_rn(s, bf16_to_f32(h0));
-  const uint16_t h1 = f32_to_bf16_rn(r1);
-  const float r2 = __fsub_rn(r1, bf16_to_f32(h1));
-  const uint16_t h2 = f32_to_bf16_rn(r2);
-  const int m = pr / G, b = pr - m * G;
-  uint16_t *o = out + (int64_t)m * ldo + b;
-  o[0] = h0;
-  o[G] = h1;
-  o[2 * G] = h2;
-}
-
 __global__ void __launch_bounds__(kXsumPairs) xsum_split_kernel(const uint16_t *X, int M, int G, int64_t ldx,
                                                                 uint16_t *out, int64_t ldo) {
   // the GEMM that follows may start its set-up now (it reads these sums only after
   // this kernel completes)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  xsum_body(X, M, G, ldx, out, ldo);
-  // When launched right after the code conversion with programmatic dependent launch,
-  // this kernel runs beside it (it reads only X, which the kernels before the conversion
-  // wrote); it ends only after the conversion has, so that the GEMM's dependency wait
-  // covers both.  Launched plainly, the wait returns at once.
+  // Launched after the code conversion with programmatic dependent launch, this waits
+  // until the conversion has ended, and with it the kernel before the conversion,
+  // which may have written X (a fused epilogue of the previous GEMM).  Launched
+  // plainly, the wait returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ __align__(16) uint4 stage[kXsumPairs * 8];
+  const int total = M * G;  // the host keeps this below 2^31
+  const int tiles = (total + kXsumPairs - 1) / kXsumPairs;
+  uint4 v[8];
+  auto load = [&](int t) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int qi = threadIdx.x + kXsumPairs * i;  // chunk qi % 8 of pair qi / 8
+      const int pr = t * kXsumPairs + (qi >> 3);
+      if (pr < total) {
+        const int m = pr / G, b = pr - m * G;
+        v[i] = ldg_v4(X + (int64_t)m * ldx + (int64_t)b * 64 + 8 * (qi & 7));
+      }
+    }
+  };
+  if ((int)blockIdx.x < tiles) load(blockIdx.x);
+  for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int qi = threadIdx.x + kXsumPairs * i;
+      const int q = qi >> 3, c = qi & 7;
+      if (t * kXsumPairs + q < total) stage[q * 8 + (c ^ (q & 7))] = v[i];
+    }
+    __syncthreads();
+    if (t + (int)gridDim.x < tiles) load(t + gridDim.x);
+    const int q = threadIdx.x, pr = t * kXsumPairs + q;
+    if (pr < total) {
+      float s = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 u = stage[q * 8 + (i ^ (q & 7))];
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s = __fadd_rn(s, bf16_to_f32(wv[e] & 0xFFFFu));
+          s = __fadd_rn(s, bf16_to_f32(wv[e] >> 16));
+        }
+      }
+      const uint16_t h0 = f32_to_bf16_rn(s);
+      const float r1 = __fsub_rn(s, bf16_to_f32(h0));
+      const uint16_t h1 = f32_to_bf16_rn(r1);
+      const float r2 = __fsub_rn(r1, bf16_to_f32(h1));
+      const uint16_t h2 = f32_to_bf16_rn(r2);
+      const int m = pr / G, b = pr - m * G;
+      uint16_t *o = out + (int64_t)m * ldo + b;
+      o[0] = h0;
+      o[G] = h1;
+      o[2 * G] = h2;
+    }
+    __syncthreads();  // the stage is refilled next
+  }
 }
 
 
@@ -956,34 +977,65 @@ __global__ void __launch_bounds__(kXsumPairs) xsum_split_kernel(const uint16_t *
 // k <= j < kp column j - k of the bias blocks, bias[r][(j - k) mod G] while j - k < 3G and
 // 0 after.  These are the values the converters write into the A tiles, so the GEMM
 // computes the same bits from either.
+// A thread writes kWconvChunks 8-value chunks, kWconvThreads chunks apart (so each load and store
+// instruction of a warp covers consecutive words and chunks); all code words are loaded
+// before the first chunk is converted, so one launch of a single wave keeps the whole of
+// W in flight instead of one word per thread.
+constexpr int kWconvThreads = 256;
+constexpr int kWconvChunks = 4;
 template <int BITS>
-__global__ void wconv_kernel(const uint32_t *wq, const uint16_t *biases, int n, int k, int64_t kp, uint16_t *A) {
-  // the row-sum pre-pass that follows reads only X: it may run beside this kernel
+__global__ void __launch_bounds__(kWconvThreads) wconv_kernel(const uint32_t *wq, const uint16_t *biases, int n,
+                                                             int k, int64_t kp, uint16_t *A) {
+  // It is launched with programmatic dependent launch: it may run while the GEMM before
+  // it (which triggers on its last tiles) still works, on the SMs that GEMM leaves
+  // idle.  It reads only W and writes only its own A buffer, which the GEMM before it
+  // does not read (calls alternate between two buffers).  The row-sum pass that
+  // follows may be launched at once; it waits for this kernel to end.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int G = k / 64;
   const int per_row = (int)(kp / 8);  // 8-value chunks per row
   const int total = n * per_row;      // the host keeps this below 2^31
   const int64_t wpr = (int64_t)k * BITS / 32;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+  const int i0 = blockIdx.x * (kWconvThreads * kWconvChunks) + threadIdx.x;
+  uint32_t raw[kWconvChunks][2];
+#pragma unroll
+  for (int u = 0; u < kWconvChunks; ++u) {
+    const int i = i0 + u * kWconvThreads;
+    raw[u][0] = raw[u][1] = 0u;
+    if (i >= total) continue;
+    const int r = i / per_row;
+    const int j0 = (i - r * per_row) * 8;
+    if (j0 >= k) continue;
+    const uint32_t *row = wq + (int64_t)r * wpr;
+    if constexpr (BITS == 4) {
+      raw[u][0] = __ldg(row + j0 / 8);
+    } else if constexpr (BITS == 8) {
+      raw[u][0] = __ldg(row + j0 / 4);
+      raw[u][1] = __ldg(row + j0 / 4 + 1);
+    } else {
+      // bits 6 j0 .. 6 j0 + 47 lie in words wi, wi + 1 (the shift below is 0 or 16)
+      const int64_t wi = ((int64_t)6 * j0) >> 5;
+      raw[u][0] = __ldg(row + wi);
+      raw[u][1] = __ldg(row + wi + 1);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kWconvChunks; ++u) {
+    const int i = i0 + u * kWconvThreads;
+    if (i >= total) continue;
     const int r = i / per_row;
     const int j0 = (i - r * per_row) * 8;
     uint32_t q[8];
     if (j0 < k) {
-      const uint32_t *row = wq + (int64_t)r * wpr;
       if constexpr (BITS == 4) {
-        const uint32_t w = row[j0 / 8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = (w >> (4 * e)) & 15u;
+        for (int e = 0; e < 8; ++e) q[e] = (raw[u][0] >> (4 * e)) & 15u;
       } else if constexpr (BITS == 8) {
-        const uint32_t w0 = row[j0 / 4], w1 = row[j0 / 4 + 1];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = ((e < 4 ? w0 : w1) >> (8 * (e & 3))) & 255u;
+        for (int e = 0; e < 8; ++e) q[e] = (raw[u][e >> 2] >> (8 * (e & 3))) & 255u;
       } else {
-        // bits 6 j0 .. 6 j0 + 47 lie in words wi, wi + 1 (the shift is 0 or 16)
-        const int64_t bit = (int64_t)6 * j0;
-        const int64_t wi = bit >> 5;
-        const int sh = (int)(bit & 31);
-        const uint64_t v = (uint64_t)row[wi] | ((uint64_t)row[wi + 1] << 32);
+        const int sh = (6 * j0) & 31;
+        const uint64_t v = (uint64_t)raw[u][0] | ((uint64_t)raw[u][1] << 32);
 #pragma unroll
         for (int e = 0; e < 8; ++e) q[e] = (uint32_t)(v >> (sh + 6 * e)) & 63u;
       }
@@ -999,6 +1051,9 @@ __global__ void wconv_kernel(const uint32_t *wq, const uint16_t *biases, int n, 
     *reinterpret_cast<uint4 *>(A + (int64_t)r * kp + j0) =
         make_uint4(q[0] | (q[1] << 16), q[2] | (q[3] << 16), q[4] | (q[5] << 16), q[6] | (q[7] << 16));
   }
+  // The grid ends only after the kernel before it has: one CTA waits for it, the
+  // others leave their SMs as soon as their chunks are written.
+  if (blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace pg
@@ -1033,7 +1088,7 @@ static bool make_map(CUtensorMap *map, CUtensorMapDataType dt, const void *base,
 // Library-owned scratch: one growable buffer per device and use (slot 0: the split row
 // sums; slot 1: the codes converted once per call for large windows).
 constexpr int kMaxDev = 64;
-constexpr int kScratchSlots = 2;
+constexpr int kScratchSlots = 3;  // 0: split row sums; 1, 2: converted codes (alternating)
 static std::mutex g_scratch_mu;
 static void *g_scratch[kScratchSlots][kMaxDev];
 static size_t g_scratch_bytes[kScratchSlots][kMaxDev];
@@ -1216,21 +1271,36 @@ static int noalloc_scratch_addr(uint16_t **out) {
 
 int64_t pgemm_noalloc_max_elems() { return kNoAllocScratchElems; }
 
-// The row-sum pre-pass over m rows; with `beside` it is launched with programmatic
-// dependent launch right after the code conversion, so the two run together.
+// The row-sum pre-pass over m rows; with `after_conv` it is launched with programmatic
+// dependent launch right after the code conversion (it then waits for the conversion to
+// end before it reads X).
 static int launch_xsum(const uint16_t *X, int m, int G, int64_t ldx, uint16_t *S, int64_t lds, cudaStream_t st,
-                       bool beside) {
+                       bool after_conv) {
   const int64_t total = (int64_t)m * G;
   if (total >= (int64_t(1) << 31)) return QL_ERR_TOO_LARGE;
+  // at most one wave of CTAs (resident CTAs per SM, by the kernel's shared memory)
+  static std::atomic<int> per_sm{0};
+  int occ = per_sm.load(std::memory_order_relaxed);
+  if (occ == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pg::xsum_split_kernel, pg::kXsumPairs, 0) !=
+            cudaSuccess ||
+        occ <= 0) {
+      (void)cudaGetLastError();
+      occ = 1;
+    }
+    per_sm.store(occ, std::memory_order_relaxed);
+  }
+  const int64_t tiles = (total + pg::kXsumPairs - 1) / pg::kXsumPairs;
+  const int64_t wave = (int64_t)occ * sm_count();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((total + pg::kXsumPairs - 1) / pg::kXsumPairs));
+  cfg.gridDim = dim3((unsigned)(tiles < wave ? tiles : wave));
   cfg.blockDim = dim3((unsigned)pg::kXsumPairs);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = beside ? 1 : 0;
+  cfg.numAttrs = after_conv ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, pg::xsum_split_kernel, X, m, G, ldx, S, lds) != cudaSuccess) {
     (void)cudaGetLastError();
     return QL_ERR_LAUNCH;
@@ -1272,6 +1342,12 @@ static int launch_epi(const ql_weight *w, const uint16_t *X, int m, int64_t ldx,
 // one per 256-row band.  Smaller windows convert inside the GEMM.  Both give the same bits.
 constexpr int kPreRows = 2048;
 
+// Per device, how many calls have converted their codes (the parity picks the buffer).
+static unsigned apre_flip(int dev) {
+  static std::atomic<unsigned> calls[kMaxDev];
+  return calls[dev].fetch_add(1u, std::memory_order_relaxed);
+}
+
 int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy, cudaStream_t st,
               int *status, const PgEpilogue *epi) {
   const int G = w->k / 64;
@@ -1281,17 +1357,34 @@ int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *
   uint16_t *apre = nullptr;
   if (m >= kPreRows && (int64_t)w->n * (((int64_t)w->k + lds) / 8) < (int64_t(1) << 31)) {
     const int64_t kp = (int64_t)w->k + lds;
-    apre = static_cast<uint16_t *>(scratch_get(1, (size_t)w->n * (size_t)kp * 2));
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return QL_ERR_LAUNCH;
+    // Consecutive calls write alternate buffers: this call's conversion may run while
+    // the previous call's GEMM (reading the other buffer) finishes.
+    const int slot = 1 + (int)(apre_flip(dev) & 1u);
+    apre = static_cast<uint16_t *>(scratch_get(slot, (size_t)w->n * (size_t)kp * 2));
     if (apre == nullptr) return QL_ERR_NOMEM;
     const int64_t chunks = (int64_t)w->n * (kp / 8);
-    int cblocks = (int)((chunks + 255) / 256);
-    if (cblocks > 16384) cblocks = 16384;
+    constexpr int per_block = pg::kWconvThreads * pg::kWconvChunks;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((chunks + per_block - 1) / per_block));
+    cfg.blockDim = dim3((unsigned)pg::kWconvThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t ce;
     switch (w->bits) {
-      case 4: pg::wconv_kernel<4><<<cblocks, 256, 0, st>>>(w->wq, w->biases, w->n, w->k, kp, apre); break;
-      case 6: pg::wconv_kernel<6><<<cblocks, 256, 0, st>>>(w->wq, w->biases, w->n, w->k, kp, apre); break;
-      default: pg::wconv_kernel<8><<<cblocks, 256, 0, st>>>(w->wq, w->biases, w->n, w->k, kp, apre); break;
+      case 4: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<4>, w->wq, w->biases, w->n, w->k, kp, apre); break;
+      case 6: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<6>, w->wq, w->biases, w->n, w->k, kp, apre); break;
+      default: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<8>, w->wq, w->biases, w->n, w->k, kp, apre); break;
     }
-    if (cudaGetLastError() != cudaSuccess) return QL_ERR_LAUNCH;
+    if (ce != cudaSuccess) {
+      (void)cudaGetLastError();
+      return QL_ERR_LAUNCH;
+    }
   }
   if (int e2 = launch_xsum(X, m, G, ldx, S, lds, st, apre != nullptr)) return e2;
   if (apre != nullptr) return launch_epi<0>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
