@@ -130,10 +130,12 @@ def test_several_tiles_per_cta_long_k(q, bits, k):
     U.assert_close(Y[torch.from_numpy(rows).cuda()], y64, A, f"pgemm several tiles bits={bits} k={k}")
 
 
-@pytest.mark.parametrize("bits,m,n,k", [(4, 2300, 1000, 1024), (6, 2049, 333, 2048), (8, 2200, 520, 512)])
+@pytest.mark.parametrize("bits,m,n,k", [(4, 2300, 1000, 1024), (6, 2049, 333, 2048), (8, 2200, 520, 512),
+                                        (4, 2050, 130, 64), (6, 2048, 256, 192), (8, 2100, 300, 8192)])
 def test_large_windows_ragged_against_windows(q, bits, m, n, k):
     # From 2048 rows on the codes are converted once per call; below, inside the GEMM.
-    # Ragged m and n (partial row and channel tiles) on the first path against the same
+    # Ragged m and n (partial row and channel tiles), one group (k = 64: three
+    # split-sum columns), three groups and 128 groups on the first path against the same
     # rows cut into windows of 512 (the second path), bit for bit, and sampled rows
     # against the float64 oracle.
     w = U.weight(n, k, bits, config_id=62, tensor_id=bits)
