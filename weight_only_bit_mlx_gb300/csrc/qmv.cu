@@ -10,15 +10,15 @@
 // of n or of the fused/unfused choice):
 //   * a CTA owns a 16-row tile of W (both w1 and w3 in the fused FFN) and a k-span;
 //     CTAs of a cluster split k into spans;
-//   * the span is cut into kNch chunks of kGpc groups; warp 0 first starts, chunk by
-//     chunk, one bulk copy (cp.async.bulk) per weight row of the chunk, straight
-//     from HBM into shared memory, each chunk completing its own mbarrier, so the
-//     warps start on chunk 0 while later chunks are still streaming in and the
-//     weight stream leaves the SM as large requests issued at kernel start (no warp
-//     is kept only for copies, so the compute warps get 64 registers instead of 56);
-//   * scales and biases go in by bulk copy with chunk 0 (one copy for the whole tile
-//     when a CTA spans the full k), activations (the only input a preceding kernel
-//     may write) are loaded by the compute warps after griddepcontrol.wait, so with
+//   * compute warp w owns kGpw consecutive groups of the span; at kernel start it copies
+//     exactly those bytes of every row of the tile from HBM into shared memory with
+//     16-byte cp.async pieces (a warp instruction reads four whole 128-byte lines), and
+//     waits only for its own copies.  Measured against one bulk copy (cp.async.bulk)
+//     per row, all issued by warp 0 (32 per CTA in the fused FFN): 0.269 against
+//     0.283-0.287 ms per 4-bit R = 1 decode pass;
+//   * scales and biases are read by the compute threads (16-byte vectors of 8 groups
+//     when the rows allow it) before the dependency wait; activations (the only input
+//     a preceding kernel may write) are loaded after griddepcontrol.wait, so with
 //     programmatic dependent launch the weight stream of this kernel overlaps the
 //     tail of the previous one;
 //   * compute warp w owns kGpw consecutive groups of every chunk.  Per group the
@@ -88,13 +88,12 @@ int mv_resid_counter_reset() {
 int mv_span_g(int bits) { return bits == 4 ? span_g<4>() : (bits == 6 ? span_g<6>() : span_g<8>()); }
 
 // Shared-memory layout of one CTA (dynamic, 128-byte aligned):
-//   wsm [NMAT][16][wpitch]             weight rows of the span (one bulk copy per row and chunk);
+//   wsm [NMAT][16][wpitch]             weight rows of the span (each warp copies its groups);
 //                                      after the last group it holds the warp partials
 //                                      red[kMvWarps][NV][32] (without a cluster they are
 //                                      added in warp order where the outputs are stored)
 //   sbf [NMAT][span][16] float4        per (group, row): group_factors (scale, centred
 //                                      bias, offset constant)
-//   bars[kNch]                         one per chunk
 //   cpart[cs][NV][32] fp32             with a cluster of cs > 1 CTAs: every rank's CTA
 //                                      partial (only rank 0's copy is read); a region of
 //                                      its own, since other ranks write it while this
@@ -110,8 +109,7 @@ template <int BITS, int NB, int MODE> struct MvLayout {
   static constexpr int kPartBytes = kCsum + NV * 32 * 4;
   static constexpr int kWBytes = NMAT * 16 * wpitch<BITS>() > kPartBytes ? NMAT * 16 * wpitch<BITS>() : kPartBytes;
   static constexpr int kSbf = kWBytes;
-  static constexpr int kBar = kSbf + NMAT * span_g<BITS>() * 16 * 16;
-  static constexpr int kCpart = (kBar + kNch * 8 + 15) / 16 * 16;
+  static constexpr int kCpart = (kSbf + NMAT * span_g<BITS>() * 16 * 16 + 15) / 16 * 16;
   static constexpr int kBytes = kCpart;  // without a cluster
   static int bytes(int cs) { return cs > 1 ? kCpart + cs * NV * 32 * 4 : kBytes; }
   static int max_bytes() { return bytes(kMvMaxCluster); }
@@ -221,7 +219,6 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
   float4 *sbf = reinterpret_cast<float4 *>(smem + Lay::kSbf);
   float *red = reinterpret_cast<float *>(smem + Lay::kRed);
   float *csum = reinterpret_cast<float *>(smem + (p.cs > 1 ? Lay::kCpart : Lay::kCsum));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
   uint8_t *wsm = smem + Lay::kW;
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -241,53 +238,30 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
   // this CTA's k-span: groups [gs0, gs1), in spans of SPAN groups
   const int gs0 = rank * p.span_g, gs1 = min(p.groups, gs0 + p.span_g);
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kNch; ++i) mbar_init(&bars[i], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
   float y[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) y[i] = 0.0f;
-  uint32_t phase = 0;
-  bool ok = true;
-  int armed = 0;  // chunks of the last span whose copies were started (warp 0)
 
   for (int ch0 = gs0; ch0 < gs1; ch0 += SPAN) {
     const int ch1 = min(gs1, ch0 + SPAN);
     const int ng = ch1 - ch0;
-    if (warp == 0) {
-      // ---- warp 0 first starts the span's copies, chunk by chunk, one bulk copy per
-      //      weight row of the chunk (every warp has finished the previous span: the
-      //      barrier at the end of each span)
-      const int t = lane >> 4, r = lane & 15;
-      const int row = tile * 16 + r;
-      const bool mine = lane < NMAT * 16 && row < n;
-      if (ch0 != gs0 && lane == 0) {
-        // the previous span's copies have landed (its consumers waited for them, unless
-        // a wait gave up) before this span's copies reuse the buffers and barriers
-        for (int cc = 0; cc < armed; ++cc) (void)mbar_wait_bounded(&bars[cc], phase ^ 1u, kMvDrainNs, nullptr);
-        fence_proxy_async_smem();
+    {
+      // ---- every warp starts the copies of the weight bytes it will read: its groups of
+      //      the span, every row of the tile, as 16-byte pieces (consecutive lanes on
+      //      consecutive pieces of a row, so a warp instruction reads whole 128-byte
+      //      lines); no other warp reads them, so the warp waits only for its own
+      static_assert(kNch == 1, "one chunk per span");
+      const int gw0 = ch0 + warp * GPW;
+      const int pieces = max(0, min(GPW, ch1 - gw0)) * (GB / 16);  // per row
+      for (int e = lane; e < NMAT * 16 * pieces; e += 32) {
+        const int rr = e / pieces, pc = e - rr * pieces;
+        const int row = tile * 16 + (rr & 15);
+        if (row < n)
+          cp_async16(wsm + rr * WP + (gw0 - ch0) * GB + pc * 16,
+                     reinterpret_cast<const uint8_t *>(p.m[mi + (rr >> 4)].wq) + (size_t)row * row_bytes +
+                         (size_t)gw0 * GB + pc * 16);
       }
-      armed = 0;
-      for (int cc = 0; cc < kNch; ++cc) {
-        const int ga = ch0 + cc * GPC;
-        if (ga >= ch1) break;
-        const int gb = min(ch1, ga + GPC);
-        const uint32_t wb = (uint32_t)((gb - ga) * GB);
-        uint32_t bytes = mine ? wb : 0u;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[cc], bytes);
-        __syncwarp();
-        if (mine) {
-          const uint8_t *src = reinterpret_cast<const uint8_t *>(p.m[mi + t].wq) + (size_t)row * row_bytes +
-                               (size_t)ga * GB;
-          bulk_g2s(wsm + (t * 16 + r) * WP + (ga - ch0) * GB, src, wb, &bars[cc]);
-        }
-        armed = cc + 1;
-      }
+      cp_async_commit();
     }
     {
       // ---- every warp computes
@@ -351,8 +325,8 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
           if (xv[h] && gcnt > 0)
             load_x_frag<kPair4>(p.x + (size_t)(8 * h + g4) * p.ldx + (size_t)gw0 * 64 + 16 * c, Xa[h], Xb[h]);
         }
-        if (ok) ok = mbar_wait_bounded(&bars[cc], phase, p.budget_ns, nullptr);
-        if (!ok) continue;  // keep every barrier below matched; the status word records why
+        cp_async_wait_all();  // this warp's weight bytes have landed
+        __syncwarp();
 #pragma unroll
         for (int gi = 0; gi < GPW; ++gi) {
           if (gi < gcnt) {
@@ -380,15 +354,9 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
         }
       }
     }
-    phase ^= 1u;
     if (ch1 < gs1) __syncthreads();  // the span's buffers are fully read before the next span refills them
   }
-  if (!ok && lane == 0) record_status(p.status, kErrTimeout);
-  if (warp == 0 && lane == 0) {
-    // every copy this CTA started has landed before the partials reuse the weight area
-    // and before the CTA exits (immediate unless a wait gave up)
-    for (int cc = 0; cc < armed; ++cc) (void)mbar_wait_bounded(&bars[cc], phase ^ 1u, kMvDrainNs, nullptr);
-  }
+  cp_async_wait_all();  // (a warp with no groups started no copies)
 
   // ---- partials: warps in order, then cluster ranks in order.  The partials reuse
   //      the weight area, so every compute warp is past its last group first.  In a
@@ -525,7 +493,7 @@ cudaError_t launch_mv(MvParams &p, int mode, int bits, int tiles, cudaStream_t s
   int nwarps;
   mv_geometry(p.k, bits, p.groups, p.span_g, nwarps, p.cs);
   p.wpr = p.k * bits / 32;
-  // scale/bias rows of a chunk can be bulk-copied when every copy starts and ends on
+  // scale/bias rows of a span can be read as 16-byte vectors when every vector starts on
   // a 16-byte boundary: groups and the per-CTA span multiples of 8, pointers aligned
   const int nm = mode == kMvAttn ? 4 : (mode == kMvFfn ? 2 : 1);
   bool sb = (p.groups % 8) == 0 && (p.span_g % 8) == 0;

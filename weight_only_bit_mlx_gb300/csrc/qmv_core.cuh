@@ -13,8 +13,8 @@
 namespace qlk {
 
 template <int BITS> struct Geo;
-// chunks per span, one mbarrier each (2, computing the first half while the second
-// lands, measured slower on the decode pass)
+// chunks per span (2, computing the first half while the second lands, measured slower
+// on the decode pass)
 constexpr int kNch = 1;
 // spans of 32 groups (4-bit) or 16 groups (6/8-bit), split over the compute warps and chunks
 template <> struct Geo<4> {
@@ -93,17 +93,17 @@ __device__ __forceinline__ uint32_t u4get(const uint4 &v, int j) {
   return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst)),
-               "l"(src), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
+// 16 bytes global -> shared, asynchronously (bypassing L1); completion per thread by
+// cp_async_wait_all
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-constexpr int kMvThreads = kMvWarps * 32;  // compute warps (warp 0 also starts the bulk copies)
+constexpr int kMvThreads = kMvWarps * 32;  // compute warps (each also copies its weight bytes)
 constexpr int kMvComputeThreads = kMvWarps * 32;
 constexpr int kBarCompute = 1;                   // named barrier of the compute warps
-constexpr uint64_t kMvDrainNs = 2000000000ull;
 
 // activation fragment of lane (g4, c) for one group: x[row][64g + 16c .. +16) as two
 // 16-byte pieces; 4-bit takes each 8-value block in the order x0 x4 x1 x5 x2 x6 x3 x7,
