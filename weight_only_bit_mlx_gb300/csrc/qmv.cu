@@ -252,14 +252,30 @@ __global__ void __launch_bounds__(kMvThreads, kMvCtasPerSm) qmv_kernel(const __g
       //      lines); no other warp reads them, so the warp waits only for its own
       static_assert(kNch == 1, "one chunk per span");
       const int gw0 = ch0 + warp * GPW;
-      const int pieces = max(0, min(GPW, ch1 - gw0)) * (GB / 16);  // per row
-      for (int e = lane; e < NMAT * 16 * pieces; e += 32) {
-        const int rr = e / pieces, pc = e - rr * pieces;
+      const int gcnt = max(0, min(GPW, ch1 - gw0));
+      auto piece = [&](int rr, int pc) {
         const int row = tile * 16 + (rr & 15);
         if (row < n)
           cp_async16(wsm + rr * WP + (gw0 - ch0) * GB + pc * 16,
                      reinterpret_cast<const uint8_t *>(p.m[mi + (rr >> 4)].wq) + (size_t)row * row_bytes +
                          (size_t)gw0 * GB + pc * 16);
+      };
+      constexpr int PC = GPW * GB / 16;  // pieces per row with all of the warp's groups
+      if (gcnt == GPW && (PC & (PC - 1)) == 0) {
+        // (4 and 8 bits) a power-of-two count per row: unrolled, no division (6 bits keeps
+        // the loop below: unrolled, its FFN variant spills and the pass measured slower)
+        static_assert((NMAT * 16 * PC) % 32 == 0, "whole warp instructions");
+#pragma unroll
+        for (int i = 0; i < NMAT * 16 * PC / 32; ++i) {
+          const int e = lane + 32 * i;
+          piece(e / PC, e % PC);
+        }
+      } else {
+        const int pieces = gcnt * (GB / 16);  // per row
+        for (int e = lane; e < NMAT * 16 * pieces; e += 32) {
+          const int rr = e / pieces;
+          piece(rr, e - rr * pieces);
+        }
       }
       cp_async_commit();
     }
