@@ -913,10 +913,11 @@ __global__ void __launch_bounds__(kXsumPairs) xsum_split_kernel(const uint16_t *
   // the GEMM that follows may start its set-up now (it reads these sums only after
   // this kernel completes)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // Launched after the code conversion with programmatic dependent launch, this waits
-  // until the conversion has ended, and with it the kernel before the conversion,
-  // which may have written X (a fused epilogue of the previous GEMM).  Launched
-  // plainly, the wait returns at once.
+  // Launched with programmatic dependent launch, this kernel may start while the kernel
+  // before it still runs (the code conversion, or the previous call's GEMM in its last
+  // tiles); it waits for that kernel, and so for every kernel before it, to end before it
+  // reads X (which a fused epilogue of the previous GEMM may have written) or writes the
+  // sums (which the previous GEMM reads).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ __align__(16) uint4 stage[kXsumPairs * 8];
   const int total = M * G;  // the host keeps this below 2^31
@@ -1271,11 +1272,9 @@ static int noalloc_scratch_addr(uint16_t **out) {
 
 int64_t pgemm_noalloc_max_elems() { return kNoAllocScratchElems; }
 
-// The row-sum pre-pass over m rows; with `after_conv` it is launched with programmatic
-// dependent launch right after the code conversion (it then waits for the conversion to
-// end before it reads X).
-static int launch_xsum(const uint16_t *X, int m, int G, int64_t ldx, uint16_t *S, int64_t lds, cudaStream_t st,
-                       bool after_conv) {
+// The row-sum pre-pass over m rows, launched with programmatic dependent launch (the
+// kernel waits for the kernel before it before it touches X or the sums).
+static int launch_xsum(const uint16_t *X, int m, int G, int64_t ldx, uint16_t *S, int64_t lds, cudaStream_t st) {
   const int64_t total = (int64_t)m * G;
   if (total >= (int64_t(1) << 31)) return QL_ERR_TOO_LARGE;
   // at most one wave of CTAs (resident CTAs per SM, by the kernel's shared memory)
@@ -1300,7 +1299,7 @@ static int launch_xsum(const uint16_t *X, int m, int G, int64_t ldx, uint16_t *S
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = after_conv ? 1 : 0;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, pg::xsum_split_kernel, X, m, G, ldx, S, lds) != cudaSuccess) {
     (void)cudaGetLastError();
     return QL_ERR_LAUNCH;
@@ -1318,7 +1317,7 @@ int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx,
   if (e) return e;
   // every scratch value the GEMM reads is written by this pre-pass first, so nothing
   // left by an earlier call needs clearing
-  if (int e2 = launch_xsum(X, m, G, ldx, S, lds, st, false)) return e2;
+  if (int e2 = launch_xsum(X, m, G, ldx, S, lds, st)) return e2;
   switch (w->bits) {
     case 4: return launch_pgemm<4, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
     case 6: return launch_pgemm<6, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, nullptr);
@@ -1386,7 +1385,7 @@ int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *
       return QL_ERR_LAUNCH;
     }
   }
-  if (int e2 = launch_xsum(X, m, G, ldx, S, lds, st, apre != nullptr)) return e2;
+  if (int e2 = launch_xsum(X, m, G, ldx, S, lds, st)) return e2;
   if (apre != nullptr) return launch_epi<0>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
   switch (w->bits) {
     case 4: return launch_epi<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
