@@ -196,3 +196,49 @@ def test_back_to_back_large_calls_bit_exact(q):
     assert torch.equal(r.view(torch.int16), rr.view(torch.int16)), "stored residual"
     for i, (a, b) in enumerate(zip(ys, ref)):
         assert torch.equal(a, b), f"call {i} differs from the same call made alone"
+
+
+def test_mixed_calls_back_to_back_bit_exact(q):
+    # Every call's row-sum pre-pass, every large call's code conversion and every GEMM are
+    # launched with programmatic dependent launch, each waiting for the kernel before it
+    # before it reads what that kernel may have written.  Here windows of 128 and 600 rows,
+    # the no-alloc entry point, large calls (with and without the conversion's early start)
+    # and a fused epilogue whose output is the next call's X follow each other with no
+    # synchronization.  Every output must equal the same call made alone.
+    eps = 1e-5
+    w_a = U.dev_weight(U.weight(4096, 2048, 4, config_id=66, tensor_id=1))
+    w_b = U.dev_weight(U.weight(2048, 4096, 6, config_id=66, tensor_id=2))
+    w_c = U.dev_weight(U.weight(1000, 2048, 8, config_id=66, tensor_id=3))
+    X = U.dev_x(synth.make_x(2048, 2048, config_id=67))
+    r0 = U.dev_x(synth.make_bf16((600, 4096), config_id=66, tensor_id=9))
+    gamma = U.dev_x(synth.make_bf16((4096,), 0.5, 1.5, config_id=66, tensor_id=10))
+
+    def calls(sync):
+        out = []
+
+        def step(fn):
+            out.append(fn())
+            if sync:
+                torch.cuda.synchronize()
+
+        r = r0.clone()
+        step(lambda: q.qlinear_pgemm(w_a, X[:128]))
+        step(lambda: q.qlinear_pgemm(w_c, X))                                   # large, after a small call
+        step(lambda: q.qlinear_pgemm_resid_norm(w_a, X[:600], r, gamma, eps))  # h: [600, 4096]
+        step(lambda: q.qlinear_pgemm(w_b, out[-1]))                             # X written just before
+        step(lambda: q.qlinear_pgemm_noalloc(w_c, X[:128], torch.empty(128, 1000, device=X.device)))
+        step(lambda: q.qlinear_pgemm(w_a, X))                                   # large, after a no-alloc call
+        step(lambda: q.qlinear_pgemm(w_c, X))                                   # large after large
+        step(lambda: q.qlinear_pgemm(w_a, X[100:228]))                          # small after large
+        return out, r
+
+    got, r_got = calls(sync=False)
+    torch.cuda.synchronize()
+    assert q.qlinear_last_error() == q.QL_OK
+    ref, r_ref = calls(sync=True)
+    assert q.qlinear_last_error() == q.QL_OK
+    assert torch.equal(r_got.view(torch.int16), r_ref.view(torch.int16)), "stored residual"
+    for i, (a, b) in enumerate(zip(got, ref)):
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), f"call {i} differs from the same call made alone"
