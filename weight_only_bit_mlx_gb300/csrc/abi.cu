@@ -142,8 +142,7 @@ int qlinear_mv_rows(const ql_weight *w, const uint16_t *x, int32_t rows, int64_t
   if ((e = device_setup(&status))) return e;
   MvParams p;
   std::memset(&p, 0, sizeof(p));
-  p.status = status;
-  p.budget_ns = wait_budget_ns();
+  (void)status;  // the decode kernels have no device-side waits to report
   p.m[0] = make_mat(w, y, ldy);
   p.x = x;
   p.ldx = ldx;
@@ -168,8 +167,7 @@ int qlinear_mv_resid_norm(const ql_weight *w, const uint16_t *x, int32_t rows, i
   MvParams p;
   std::memset(&p, 0, sizeof(p));
   if (mv_resid_scratch(&p.part, &p.counter)) return QL_ERR_CUDA;
-  p.status = status;
-  p.budget_ns = wait_budget_ns();
+  (void)status;  // the decode kernels have no device-side waits to report
   p.m[0] = make_mat(w, nullptr, 0);
   p.x = x;
   p.ldx = ldx;
@@ -204,8 +202,7 @@ int qffn_swiglu_mv(const ql_weight *w1, const ql_weight *w3, const uint16_t *x, 
   if ((e = device_setup(&status))) return e;
   MvParams p;
   std::memset(&p, 0, sizeof(p));
-  p.status = status;
-  p.budget_ns = wait_budget_ns();
+  (void)status;  // the decode kernels have no device-side waits to report
   p.m[0] = make_mat(w1, h, ldh);
   p.m[1] = make_mat(w3, h, ldh);
   p.x = x;
@@ -233,8 +230,7 @@ int qattn_proj_mv(const ql_weight *wq, const ql_weight *wk, const ql_weight *wv,
   if ((e = device_setup(&status))) return e;
   MvParams p;
   std::memset(&p, 0, sizeof(p));
-  p.status = status;
-  p.budget_ns = wait_budget_ns();
+  (void)status;  // the decode kernels have no device-side waits to report
   int tiles = 0;
   for (int i = 0; i < 4; ++i) {
     p.m[i] = make_mat(ws[i], outs[i], ws[i]->n);

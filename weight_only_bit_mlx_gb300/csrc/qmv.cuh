@@ -28,9 +28,7 @@ struct MvParams {
   int64_t ldx;
   int rows;
   int k;
-  int *status;           // device status word (bounded waits record QL_ERR_TIMEOUT)
   int sb_bulk;           // scales/biases rows are 16-byte aligned: read as 16-byte vectors
-  uint64_t budget_ns;    // bound of every device-side wait
   // kMvResid: the post-add / next-norm epilogue (one weight, like kMvPlain)
   uint16_t *resid;       // bf16 [rows, ldr], read and overwritten with bf16(resid + y)
   int64_t ldr;
