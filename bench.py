@@ -374,7 +374,9 @@ class Sweep:
         self.Ph = torch.empty(PROMPT, D_FF, dtype=torch.bfloat16, device=dev)
         self.Pout = torch.empty(PROMPT, D_MODEL, device=dev)
         self.Pq = torch.empty(PROMPT, D_MODEL, device=dev)
+        self.Pg = torch.empty(PROMPT, D_MODEL, device=dev)
         self.Pkv = torch.empty(PROMPT, D_KV, device=dev)
+        self.Pv = torch.empty(PROMPT, D_KV, device=dev)
         self.Patt = rnd(PROMPT, D_MODEL)
         self.Presid = rnd(PROMPT, D_MODEL)      # the residual stream of the prompt rows
         self.Pnorm = torch.empty(PROMPT, D_MODEL, dtype=torch.bfloat16, device=dev)  # next layer's input
@@ -497,9 +499,10 @@ class Sweep:
         SwiGLU as the up projection's epilogue (fused) or as a kernel of its own, and
         with post="fused" / "unfused" the post-add / next-norm after o and w2 (as the
         GEMM's epilogue plus the norm, or the plain GEMM plus qresid_rmsnorm).
-        timed="pairs": CUDA events around each layer's (w1, w3) pair of calls only (the
-        roofline kernel's launches, back to back as the layer runs them); timed="calls":
-        events around every GEMM call.  An event between two calls ends the programmatic
+        The weights that read the same X (q, k, v, gate; w1, w3) go through one
+        qlinear_pgemm_multi each.  timed="pairs": CUDA events around each layer's (w1, w3)
+        call only (the roofline kernel's launches, as the layer runs them); timed="calls":
+        every GEMM as a qlinear_pgemm call of its own, with events around each.  An event between two calls ends the programmatic
         overlap between them (a call's code conversion can then no longer run in the
         previous GEMM's last tiles), so the pass itself is timed with "pairs" at most.
         Returns the number of launches."""
@@ -511,6 +514,7 @@ class Sweep:
         X, Patt = self.X[lo:hi], self.Patt[lo:hi]
         Pa, Pc, Ph = self.Pa[lo:hi], self.Pc[lo:hi], self.Ph[lo:hi]
         Pq, Pkv, Pout = self.Pq[lo:hi], self.Pkv[lo:hi], self.Pout[lo:hi]
+        Pg, Pv = self.Pg[lo:hi], self.Pv[lo:hi]
         R, Rn = self.Presid[lo:hi], self.Pnorm[lo:hi]
 
         def down(w, Xin):  # o or w2, then the post-add / next-norm if asked for
@@ -525,39 +529,43 @@ class Sweep:
                     q.qresid_rmsnorm(Pout, R, self.pgamma, 1e-5, out=Rn)
                     n += 1
 
+        def multi(ws, outs):
+            # the weights that read X: one qlinear_pgemm_multi (the row sums of X formed
+            # once), or call by call when every call is timed alone
+            nonlocal n
+            if timed == "calls":
+                for w, out in zip(ws, outs):
+                    self._pgemm(w, X, out, timed)
+                n += len(ws) * pg
+            else:
+                q.qlinear_pgemm_multi(ws, X, outs)
+                n += len(ws) * (pg - 1) + 1
+
         for layer in range(N_LAYERS):
             p = f"L{layer}."
             if layer in ATTN_LAYERS:
-                self._pgemm(W[p + "q"], X, Pq, timed)
-                self._pgemm(W[p + "k"], X, Pkv, timed)
-                self._pgemm(W[p + "v"], X, Pkv, timed)
-                self._pgemm(W[p + "g"], X, Pq, timed)
-                n += 4 * pg
+                multi([W[p + "q"], W[p + "k"], W[p + "v"], W[p + "g"]], [Pq, Pkv, Pv, Pg])
                 down(W[p + "o"], Patt)
             if timed == "pairs" and not fused:
                 st = torch.cuda.current_stream()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(st)
-                q.qlinear_pgemm(W[p + "w1"], X, Pa)
-                q.qlinear_pgemm(W[p + "w3"], X, Pc)
+                multi([W[p + "w1"], W[p + "w3"]], [Pa, Pc])
                 e1.record(st)
                 rows = X.shape[0]
                 self.gemm_events.append((e0, e1, 2 * rows * W[p + "w1"].n * W[p + "w1"].k
                                          + 2 * rows * W[p + "w3"].n * W[p + "w3"].k, "ffn_pair"))
                 q.qswiglu(Pa, Pc, Ph)
-                n += 2 * pg + 1
-                down(W[p + "w2"], Ph)
-                continue
-            self._pgemm(W[p + "w1"], X, Pa, timed)
-            n += pg
-            if fused:
+                n += 1
+            elif not fused:
+                multi([W[p + "w1"], W[p + "w3"]], [Pa, Pc])
+                q.qswiglu(Pa, Pc, Ph)
+                n += 1
+            else:
+                self._pgemm(W[p + "w1"], X, Pa, timed)
                 self._timed_call(lambda: q.qlinear_pgemm_swiglu(W[p + "w3"], X, Pa, Ph), timed,
                                  2 * X.shape[0] * W[p + "w3"].n * W[p + "w3"].k, "swiglu")
-                n += pg
-            else:
-                self._pgemm(W[p + "w3"], X, Pc, timed)
-                q.qswiglu(Pa, Pc, Ph)
-                n += pg + 1
+                n += 2 * pg
             down(W[p + "w2"], Ph)
         return n
 
@@ -852,8 +860,9 @@ def run_ours(args):
                        "tok_s_modelled": 16.0 / (d16_ms / args.steps * 1e-3)},
         "prefill": {"TFLOP/s": pf_tflops / world, "ms_per_pass": pf_ms / args.steps,
                     "flops_per_pass": prefill_flops(),
-                    "includes": "pgemm (row-sum pre-pass + GEMM) and SwiGLU (qswiglu): the faster composition "
-                                "as measured; the up projection with the SwiGLU as its epilogue is timed beside it",
+                    "includes": "prompt GEMMs (q/k/v/gate and w1/w3 each as one qlinear_pgemm_multi, o and w2 as "
+                                "qlinear_pgemm) and SwiGLU (qswiglu): the faster composition as measured; the up "
+                                "projection with the SwiGLU as its epilogue is timed beside it",
                     "swiglu_epilogue_TFLOP/s": sw_tflops,
                     "tok_s_modelled": PROMPT / (pf_ms / args.steps * 1e-3),
                     "variants_ms_per_pass": dict(pf_variants, swiglu_separate_ms=pf_ms / args.steps,
@@ -875,18 +884,18 @@ def run_ours(args):
                                     "every window streams every weight again (64 x the sweep's weight bytes)"},
         "tok_s_note": "modelled from the linear layers only: decode R / (decode pass time), prefill "
                       "prompt rows / (prefill pass time); attention, norms and sampling excluded",
-        "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm (code conversion + row-sum pre-pass + tcgen05 "
-                                                  f"GEMM, timed together), M={PROMPT} N={D_FF} K={D_MODEL} launches "
-                                                  "(w1, w3)",
+        "roofline": {"bound": "tensor", "kernel": "qlinear_pgemm_multi(w1, w3): one row-sum pre-pass, then per "
+                                                  "weight the code conversion and the tcgen05 GEMM, timed together; "
+                                                  f"M={PROMPT} N={D_FF} K={D_MODEL}",
                      "achieved": ffn_tflops, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                      "frac": ffn_tflops / pk["bf16_sus"], "frac_of_burst": ffn_tflops / pk["bf16"],
                      "traffic": traffic,
                      "traffic_unit": "bytes per launch (DRAM read + write, one ncu capture of this shape)",
                      "algorithmic_bytes_per_launch": PROMPT * D_MODEL * 2 + weight_bytes(D_FF, D_MODEL, bits)
                      + PROMPT * D_FF * 4,
-                     "timing": "CUDA events around each layer's (w1, w3) pair of calls in the timed prefill "
-                               "passes, as the layer runs them: the w3 call's code conversion runs in the w1 "
-                               "GEMM's last tiles",
+                     "timing": "CUDA events around each layer's qlinear_pgemm_multi(w1, w3) call in the timed "
+                               "prefill passes, as the layer runs it: the w3 code conversion runs in the w1 GEMM's "
+                               "last tiles",
                      "all_gemm_launches_TFLOP/s": gemm_tflops,
                      "all_gemm_launches_timing": "one prefill pass after the timed region, CUDA events around "
                                                  "every call (which ends the overlap between calls)",

@@ -146,6 +146,23 @@ int qlinear_pgemm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx,
                   int64_t ldy, void *stream);
 
 /*
+ * qlinear_pgemm_multi - qlinear_pgemm for nw weights that read the same X (a layer's
+ * q/k/v/gate projections, or its w1 and w3): Y[i] = X w[i]^T for i < nw, each bit-equal to
+ * qlinear_pgemm(w[i], X, ...) on its own.  [P1696] "What it adds": decode fuses the four
+ * attention matvecs (qattn_proj_mv) and w1 + w3 (qffn_swiglu_mv); this is the prompt-window
+ * counterpart.  Every call on X forms the split row sums S_b of X; here they are formed
+ * once for all nw weights, then each weight's GEMM (and, from 2048 rows on, its code
+ * conversion) runs in turn.
+ *   w: nw weight pointers (1 <= nw <= 16), all with the same k; X as for qlinear_pgemm;
+ *   Y[i]: float [m, ldy[i]] with ldy[i] >= w[i]->n (4-byte aligned).  The output buffers
+ *   must not overlap X or each other.  m may be 0 (nothing enqueued).  Scratch, stream
+ *   ordering and errors as qlinear_pgemm; QL_ERR_SHAPE if nw is out of range or the k
+ *   differ.
+ */
+int qlinear_pgemm_multi(const ql_weight *const *w, int32_t nw, const uint16_t *X, int32_t m, int64_t ldx,
+                        float *const *Y, const int64_t *ldy, void *stream);
+
+/*
  * qlinear_pgemm_noalloc - qlinear_pgemm for callers that cannot allocate device
  * memory when they call: code whose device memory belongs to another allocator or
  * is held to a fixed budget, and code that must not pay the device-wide

@@ -188,3 +188,31 @@ def test_fused_prompt_gemm_epilogues_reject_bad_arguments_on_host(q):
     assert rn(ctypes.byref(w), P, 4, 120, P, 64, P, 1e-5, P, 64, None) == q.QL_ERR_ALIGN
     w5 = _w(q, bits=5)
     assert rn(ctypes.byref(w5), P, 4, 128, P, 64, P, 1e-5, P, 64, None) == q.QL_ERR_BITS
+
+
+def test_pgemm_multi_rejects_bad_arguments_on_host(q):
+    # qlinear_pgemm_multi: every weight checked as qlinear_pgemm checks it, the k equal,
+    # 1 <= nw <= 16, outputs and their pitches checked per weight, all before the device
+    L = q.LIB
+    W = ctypes.POINTER(q.ql_weight)
+    w, w2, wk, wbad = _w(q), _w(q, n=32), _w(q, k=256), _w(q, bits=5)
+
+    def call(ws, nw, x=0x40000, m=8, ldx=128, ys=None, lds=None):
+        wp = (W * max(1, len(ws)))(*[ctypes.pointer(v) for v in ws])
+        n = max(1, len(ws))
+        yp = (ctypes.c_void_p * n)(*(ys or [0x50000 + 0x10000 * i for i in range(n)]))
+        ld = (ctypes.c_int64 * n)(*(lds or [64] * n))
+        return L.qlinear_pgemm_multi(wp, nw, x, m, ldx, yp, ld, None)
+
+    assert call([w, w2], 0) == q.QL_ERR_SHAPE
+    assert call([w] * 16, 17) == q.QL_ERR_SHAPE
+    assert call([w, wk], 2) == q.QL_ERR_SHAPE              # the k differ
+    assert call([w, wbad], 2) == q.QL_ERR_BITS             # a bad weight
+    assert call([w, w2], 2, m=-1) == q.QL_ERR_SHAPE
+    assert call([w, w2], 2, m=0) == q.QL_OK               # an empty window: nothing enqueued
+    assert call([w, w2], 2, x=0) == q.QL_ERR_NULL
+    assert call([w, w2], 2, x=0x40008) == q.QL_ERR_ALIGN
+    assert call([w, w2], 2, ldx=120) == q.QL_ERR_ALIGN
+    assert call([w, w2], 2, ys=[0x50000, 0]) == q.QL_ERR_NULL
+    assert call([w, w2], 2, lds=[64, 16]) == q.QL_ERR_ALIGN  # w2 has n = 32 > 16
+    assert L.qlinear_pgemm_multi(None, 1, 0x40000, 8, 128, None, None, None) == q.QL_ERR_NULL

@@ -242,3 +242,29 @@ def test_mixed_calls_back_to_back_bit_exact(q):
         if a.dtype == torch.bfloat16:
             a, b = a.view(torch.int16), b.view(torch.int16)
         assert torch.equal(a, b), f"call {i} differs from the same call made alone"
+
+
+@pytest.mark.parametrize("m", [100, 2100])
+def test_multi_equals_separate_calls(q, m):
+    # qlinear_pgemm_multi forms the split row sums of X once for all its weights; every
+    # output must equal the weight's own qlinear_pgemm call bit for bit, below and above
+    # the row count from which the codes are converted once per call, with weights of
+    # other widths and sizes, and outputs with padded pitches.
+    k = 2048
+    specs = [(1024, 4), (256, 6), (320, 8), (1024, 4)]
+    ws = [U.dev_weight(U.weight(n, k, b, config_id=68, tensor_id=i)) for i, (n, b) in enumerate(specs)]
+    X = U.dev_x(synth.make_x(m, k, config_id=69))
+    Ys = [torch.full((m, n + 8 * i), float("nan"), device=X.device)[:, :n] for i, (n, _) in enumerate(specs)]
+    got = q.qlinear_pgemm_multi(ws, X, Ys)
+    torch.cuda.synchronize()
+    assert q.qlinear_last_error() == q.QL_OK
+    for i, w in enumerate(ws):
+        ref = q.qlinear_pgemm(w, X)
+        torch.cuda.synchronize()
+        assert torch.equal(got[i], ref), f"weight {i} differs from its own call"
+    one = q.qlinear_pgemm_multi(ws[:1], X)[0]
+    torch.cuda.synchronize()
+    assert torch.equal(one, got[0])
+    rows = np.array([0, m // 2, m - 1])
+    y64, A = orc.pgemm(synth.make_x(m, k, config_id=69)[rows], U.weight(320, k, 8, config_id=68, tensor_id=2))
+    U.assert_close(got[2][torch.from_numpy(rows).cuda()], y64, A, f"pgemm_multi m={m}")

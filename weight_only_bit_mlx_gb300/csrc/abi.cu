@@ -257,6 +257,32 @@ int qlinear_pgemm(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx,
   return pgemm_run(w, X, m, ldx, Y, ldy, static_cast<cudaStream_t>(stream), status);
 }
 
+constexpr int kPgemmMultiMax = 16;  // weights of one qlinear_pgemm_multi call
+
+// Each weight checked as qlinear_pgemm checks it, every k equal; then one row-sum
+// pre-pass and the weights' GEMMs in turn.
+int qlinear_pgemm_multi(const ql_weight *const *w, int32_t nw, const uint16_t *X, int32_t m, int64_t ldx,
+                        float *const *Y, const int64_t *ldy, void *stream) {
+  if (w == nullptr || Y == nullptr || ldy == nullptr) return QL_ERR_NULL;
+  if (nw < 1 || nw > kPgemmMultiMax) return QL_ERR_SHAPE;
+  int e = QL_OK;
+  for (int i = 0; i < nw; ++i) {
+    if ((e = check_weight(w[i]))) return e;
+    if (w[i]->k != w[0]->k) return QL_ERR_SHAPE;
+  }
+  if (m < 0) return QL_ERR_SHAPE;
+  if (m == 0) return QL_OK;  // an empty window: nothing to read or write
+  if (X == nullptr) return QL_ERR_NULL;
+  if (!aligned(X, 16) || (ldx % 8) != 0 || ldx < w[0]->k) return QL_ERR_ALIGN;
+  for (int i = 0; i < nw; ++i) {
+    if (Y[i] == nullptr) return QL_ERR_NULL;
+    if (ldy[i] < w[i]->n || !aligned(Y[i], 4)) return QL_ERR_ALIGN;
+  }
+  int *status = nullptr;
+  if ((e = device_setup(&status))) return e;
+  return pgemm_run_multi(w, nw, X, m, ldx, Y, ldy, static_cast<cudaStream_t>(stream), status);
+}
+
 // Same checks as qlinear_pgemm, then the fixed-scratch variant (allocates nothing).
 int qlinear_pgemm_noalloc(const ql_weight *w, const uint16_t *X, int32_t m, int64_t ldx, float *Y, int64_t ldy,
                           void *stream) {

@@ -1347,51 +1347,82 @@ static unsigned apre_flip(int dev) {
   return calls[dev].fetch_add(1u, std::memory_order_relaxed);
 }
 
-int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy, cudaStream_t st,
-              int *status, const PgEpilogue *epi) {
-  const int G = w->k / 64;
-  const int64_t lds = ((3 * (int64_t)G + 63) / 64) * 64;  // row pitch of the split sums (elements)
-  uint16_t *S = static_cast<uint16_t *>(scratch_get(0, (size_t)m * lds * 2));
-  if (S == nullptr) return QL_ERR_NOMEM;
-  uint16_t *apre = nullptr;
-  if (m >= kPreRows && (int64_t)w->n * (((int64_t)w->k + lds) / 8) < (int64_t(1) << 31)) {
-    const int64_t kp = (int64_t)w->k + lds;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return QL_ERR_LAUNCH;
-    // Consecutive calls write alternate buffers: this call's conversion may run while
-    // the previous call's GEMM (reading the other buffer) finishes.
-    const int slot = 1 + (int)(apre_flip(dev) & 1u);
-    apre = static_cast<uint16_t *>(scratch_get(slot, (size_t)w->n * (size_t)kp * 2));
-    if (apre == nullptr) return QL_ERR_NOMEM;
-    const int64_t chunks = (int64_t)w->n * (kp / 8);
-    constexpr int per_block = pg::kWconvThreads * pg::kWconvChunks;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((chunks + per_block - 1) / per_block));
-    cfg.blockDim = dim3((unsigned)pg::kWconvThreads);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t ce;
-    switch (w->bits) {
-      case 4: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<4>, w->wq, w->biases, w->n, w->k, kp, apre); break;
-      case 6: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<6>, w->wq, w->biases, w->n, w->k, kp, apre); break;
-      default: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<8>, w->wq, w->biases, w->n, w->k, kp, apre); break;
-    }
-    if (ce != cudaSuccess) {
-      (void)cudaGetLastError();
-      return QL_ERR_LAUNCH;
-    }
+// From kPreRows rows on (and while the converted codes stay below 2^31 chunks), the call
+// converts its codes once into one of two alternating buffers (wconv_kernel, launched
+// with programmatic dependent launch so that it may run in the previous GEMM's last
+// tiles) and sets *apre; otherwise *apre stays null and the GEMM converts in the kernel.
+static int pgemm_convert(const ql_weight *w, int m, int64_t lds, cudaStream_t st, uint16_t **apre) {
+  *apre = nullptr;
+  if (m < kPreRows || (int64_t)w->n * (((int64_t)w->k + lds) / 8) >= (int64_t(1) << 31)) return QL_OK;
+  const int64_t kp = (int64_t)w->k + lds;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return QL_ERR_LAUNCH;
+  // Consecutive calls write alternate buffers: this call's conversion may run while
+  // the previous call's GEMM (reading the other buffer) finishes.
+  const int slot = 1 + (int)(apre_flip(dev) & 1u);
+  uint16_t *a = static_cast<uint16_t *>(scratch_get(slot, (size_t)w->n * (size_t)kp * 2));
+  if (a == nullptr) return QL_ERR_NOMEM;
+  const int64_t chunks = (int64_t)w->n * (kp / 8);
+  constexpr int per_block = pg::kWconvThreads * pg::kWconvChunks;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((chunks + per_block - 1) / per_block));
+  cfg.blockDim = dim3((unsigned)pg::kWconvThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t ce;
+  switch (w->bits) {
+    case 4: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<4>, w->wq, w->biases, w->n, w->k, kp, a); break;
+    case 6: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<6>, w->wq, w->biases, w->n, w->k, kp, a); break;
+    default: ce = cudaLaunchKernelEx(&cfg, pg::wconv_kernel<8>, w->wq, w->biases, w->n, w->k, kp, a); break;
   }
-  if (int e2 = launch_xsum(X, m, G, ldx, S, lds, st)) return e2;
+  if (ce != cudaSuccess) {
+    (void)cudaGetLastError();
+    return QL_ERR_LAUNCH;
+  }
+  *apre = a;
+  return QL_OK;
+}
+
+// The GEMM of one weight on split row sums S already enqueued (pre-converted codes if
+// apre is set).
+static int pgemm_launch(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
+                        const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi,
+                        const uint16_t *apre) {
   if (apre != nullptr) return launch_epi<0>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
   switch (w->bits) {
     case 4: return launch_epi<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
     case 6: return launch_epi<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
     default: return launch_epi<8>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
   }
+}
+
+int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy, cudaStream_t st,
+              int *status, const PgEpilogue *epi) {
+  return pgemm_run_multi(&w, 1, X, m, ldx, &Y, &ldy, st, status, epi);
+}
+
+int pgemm_run_multi(const ql_weight *const *w, int nw, const uint16_t *X, int m, int64_t ldx, float *const *Y,
+                    const int64_t *ldy, cudaStream_t st, int *status, const PgEpilogue *epi) {
+  const int G = w[0]->k / 64;
+  const int64_t lds = ((3 * (int64_t)G + 63) / 64) * 64;  // row pitch of the split sums (elements)
+  if ((int64_t)m * G >= (int64_t(1) << 31)) return QL_ERR_TOO_LARGE;
+  uint16_t *S = static_cast<uint16_t *>(scratch_get(0, (size_t)m * lds * 2));
+  if (S == nullptr) return QL_ERR_NOMEM;
+  // The first weight's conversion goes before the row sums, so that it can start in the
+  // previous call's last tiles (the row sums must wait for the kernel before them).
+  uint16_t *apre = nullptr;
+  if (int e = pgemm_convert(w[0], m, lds, st, &apre)) return e;
+  if (int e = launch_xsum(X, m, G, ldx, S, lds, st)) return e;
+  for (int i = 0; i < nw; ++i) {
+    if (i > 0)
+      if (int e = pgemm_convert(w[i], m, lds, st, &apre)) return e;
+    if (int e = pgemm_launch(w[i], X, m, ldx, Y[i], ldy[i], S, lds, st, status, epi, apre)) return e;
+  }
+  return QL_OK;
 }
 
 }  // namespace qlk

@@ -28,6 +28,11 @@ struct PgEpilogue {
 int pgemm_run(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
               cudaStream_t st, int *status, const PgEpilogue *epi = nullptr);
 
+// The same for nw weights with the same k that read the same X: one row-sum pre-pass,
+// then each weight's GEMM (and code conversion) in turn.  Arguments are already checked.
+int pgemm_run_multi(const ql_weight *const *w, int nw, const uint16_t *X, int m, int64_t ldx, float *const *Y,
+                    const int64_t *ldy, cudaStream_t st, int *status, const PgEpilogue *epi = nullptr);
+
 // The post-add / next-norm kernels (qpost.cu); y == nullptr normalises the residual as
 // it stands.
 cudaError_t launch_resid_rmsnorm(const float *y, int64_t ldy, uint16_t *resid, int64_t ldr, int rows, int n,

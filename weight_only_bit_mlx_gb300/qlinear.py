@@ -57,6 +57,8 @@ def _load() -> ctypes.CDLL:
         "qattn_proj_mv": (ctypes.c_int, [W, W, W, W, P, I32, I64, P, P, P, P, P]),
         "qlinear_pgemm": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
         "qlinear_pgemm_noalloc": (ctypes.c_int, [W, P, I32, I64, P, I64, P]),
+        "qlinear_pgemm_multi": (ctypes.c_int, [ctypes.POINTER(W), I32, P, I32, I64, ctypes.POINTER(P),
+                                               ctypes.POINTER(I64), P]),
         "qlinear_pgemm_swiglu": (ctypes.c_int, [W, P, I32, I64, P, I64, P, I64, P]),
         "qlinear_pgemm_resid_norm": (ctypes.c_int, [W, P, I32, I64, P, I64, P, ctypes.c_float, P, I64, P]),
         "qswiglu": (ctypes.c_int, [P, P, I32, I32, I64, P, I64, P]),
@@ -197,6 +199,29 @@ def qlinear_pgemm(w: QWeight, X: torch.Tensor, Y: torch.Tensor | None = None, st
     _check(LIB.qlinear_pgemm(ctypes.byref(w.c), X.data_ptr(), m, X.stride(0), Y.data_ptr(), Y.stride(0),
                              _stream(stream)), "qlinear_pgemm")
     return Y
+
+
+def qlinear_pgemm_multi(ws, X: torch.Tensor, Ys=None, stream=None) -> list:
+    """qlinear_pgemm for several weights that read the same X (the split row sums of X are
+    formed once); returns the outputs, each bit-equal to its own qlinear_pgemm call."""
+    ws = list(ws)
+    if not ws:
+        raise ValueError("at least one weight")
+    k = ws[0].k
+    if X.dtype != torch.bfloat16 or not X.is_cuda or X.dim() != 2 or X.shape[1] != k or X.stride(1) != 1:
+        raise ValueError(f"X must be a CUDA bfloat16 [m, {k}] tensor with unit column stride")
+    m = int(X.shape[0])
+    if Ys is None:
+        Ys = [torch.empty(m, w.n, dtype=torch.float32, device=X.device) for w in ws]
+    if len(Ys) != len(ws):
+        raise ValueError("one output per weight")
+    nw = len(ws)
+    wp = (ctypes.POINTER(ql_weight) * nw)(*[ctypes.pointer(w.c) for w in ws])
+    yp = (ctypes.c_void_p * nw)(*[Y.data_ptr() for Y in Ys])
+    ld = (ctypes.c_int64 * nw)(*[Y.stride(0) for Y in Ys])
+    _check(LIB.qlinear_pgemm_multi(wp, nw, X.data_ptr(), m, X.stride(0), yp, ld, _stream(stream)),
+           "qlinear_pgemm_multi")
+    return Ys
 
 
 def qlinear_pgemm_noalloc(w: QWeight, X: torch.Tensor, Y: torch.Tensor, stream=None) -> torch.Tensor:
