@@ -32,6 +32,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -51,7 +52,7 @@ PROMPT = 8192
 # hash of the kernel source it was taken on; reported as null once the source changes.
 # rows from which the library converts the codes once per prompt-GEMM call (one more launch)
 PRE_ROWS = 2048
-NCU_TRAFFIC = {"1cec53752360d9ce": 131443200 + 231690752}  # pgemm M=8192 N=8192 K=2048, 4-bit (device code as captured)
+NCU_TRAFFIC = {"fbbbe62a77946797": 131443200 + 231690752}  # pgemm M=8192 N=8192 K=2048, 4-bit (device code as captured)
 
 
 def parse():
@@ -74,10 +75,15 @@ def parse():
 
 
 def source_hash(names):
+    """Hash of the sources' code: comments and whitespace removed, so that the key of a
+    DRAM capture outlives edits that leave the device code as it was."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "weight_only_bit_mlx_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "weight_only_bit_mlx_gb300", "csrc", n)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

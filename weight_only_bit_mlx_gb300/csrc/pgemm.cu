@@ -50,6 +50,17 @@
 //               of X each, held in registers across the k loop
 // The launch gives every thread 128 registers; setmaxnreg moves them from the first two
 // warpgroups to the epilogue, whose running sums (128 fp32 per thread) need them.
+//
+// Windows of 2048 rows and more: the codes are converted once per call into a bf16
+// buffer (wconv_kernel, the same values the converters write), and the GEMM (BITS = 0)
+// TMA-loads ready A tiles; its converters only stage the scales.  A call enqueues the
+// conversion (for those windows), the row-sum pre-pass and the GEMM, each with
+// programmatic dependent launch.  The GEMM triggers its dependents once each CTA has
+// started its last tile, so the next call's conversion (into the other of two
+// alternating buffers) runs on the SMs the last round leaves idle; the row sums and the
+// GEMM wait for the kernel before them before they touch X, the sums or the outputs.
+// Several weights on one X (pgemm_run_multi): one row-sum pre-pass, then each weight's
+// conversion and GEMM in turn.
 // Every wait is a bounded mbarrier wait (sync.cuh); a wait that gives up records
 // QL_ERR_TIMEOUT, the CTA drains its own copies and MMAs, and both CTAs pass a final
 // cluster barrier (neither leaves while the other may still touch its shared memory)
