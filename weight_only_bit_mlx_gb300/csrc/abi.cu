@@ -94,6 +94,7 @@ static MvMat make_mat(const ql_weight *w, void *out, int64_t ldo) {
 // ---------------------------------------------------------------------------------
 __global__ void swiglu_kernel(const float *a, const float *c, int rows, int n, int64_t lda, uint16_t *h,
                               int64_t ldh) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in swiglu_vec4_kernel
   const int64_t total = (int64_t)rows * n;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / n, j = i % n;
@@ -103,6 +104,10 @@ __global__ void swiglu_kernel(const float *a, const float *c, int rows, int n, i
 
 // Contiguous rows and 16-byte aligned data: four elements per thread step.
 __global__ void swiglu_vec4_kernel(const float4 *a, const float4 *c, int64_t n4, uint2 *h) {
+  // a kernel launched after this one with programmatic dependent launch (the next prompt
+  // GEMM call's code conversion, which reads only its weights) may start now; every
+  // library kernel waits for this one before it reads what this one writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
     const float4 av = a[i], cv = c[i];
     const uint32_t h0 = swiglu_bf16(av.x, cv.x), h1 = swiglu_bf16(av.y, cv.y);
