@@ -254,14 +254,20 @@ def test_multi_equals_separate_calls(q, m):
     specs = [(1024, 4), (256, 6), (320, 8), (1024, 4)]
     ws = [U.dev_weight(U.weight(n, k, b, config_id=68, tensor_id=i)) for i, (n, b) in enumerate(specs)]
     X = U.dev_x(synth.make_x(m, k, config_id=69))
+    X2 = U.dev_x(synth.make_x(m, k, config_id=70))
     Ys = [torch.full((m, n + 8 * i), float("nan"), device=X.device)[:, :n] for i, (n, _) in enumerate(specs)]
+    # below 2048 rows the GEMMs of one call run beside each other; a second call on
+    # another X follows at once (its row sums replace the first call's)
     got = q.qlinear_pgemm_multi(ws, X, Ys)
+    got2 = q.qlinear_pgemm_multi(ws[::-1], X2)
     torch.cuda.synchronize()
     assert q.qlinear_last_error() == q.QL_OK
     for i, w in enumerate(ws):
         ref = q.qlinear_pgemm(w, X)
+        ref2 = q.qlinear_pgemm(w, X2)
         torch.cuda.synchronize()
         assert torch.equal(got[i], ref), f"weight {i} differs from its own call"
+        assert torch.equal(got2[len(ws) - 1 - i], ref2), f"weight {i} of the second call differs"
     one = q.qlinear_pgemm_multi(ws[:1], X)[0]
     torch.cuda.synchronize()
     assert torch.equal(one, got[0])

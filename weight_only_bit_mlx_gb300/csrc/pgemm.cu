@@ -160,6 +160,12 @@ struct Params {
   int tiles_n, tiles;  // 256-channel tiles per 256-row band; tiles in all
   int *status;
   uint64_t budget_ns;
+  // A GEMM of a multi-weight call after the first (windows below the pre-conversion
+  // size): it reads only X and the row sums, complete before the GEMM before it could
+  // release this one, and writes its own output, so it skips the dependency wait at the
+  // start and runs beside that GEMM; one thread waits for it before the CTA exits, so
+  // that the last GEMM of the call still ends after every other.
+  int follow;
 };
 
 // ---- PTX wrappers --------------------------------------------------------------
@@ -403,6 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 1;
     record_status(p.status, kErrTimeout);
   };
+  // the wait for the kernels before this one (none at the start for a follower)
+  auto dep_wait = [&]() {
+    if (!p.follow) griddep_wait();
+  };
 
   // Each role first sets its warpgroup's register budget (the warpgroups that give
   // registers up do so before the epilogue's increase can be granted).
@@ -477,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // the bf16 A tile (main or bias block) and X or the row-sum parts; A is
               // written by the conversion pre-pass, so both wait for the earlier kernels
               if (!dep_done) {
-                griddep_wait();
+                dep_wait();
                 dep_done = true;
               }
               mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
@@ -490,14 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kXBytes + C::kWBytes));
               tma_load_2d(sW + s * C::kWBytes, &tmW, &tma_full[s], kb * (BK * BITS / 32), n0);
               if (!dep_done) {  // the weights are constant; X is written by earlier kernels
-                griddep_wait();
+                dep_wait();
                 dep_done = true;
               }
               tma_load_2d(sX + s * kXBytes, &tmX, &tma_full[s], kb * BK, m0);
             } else {
               mbar_arrive_expect_tx(&tma_full[s], (uint32_t)kXBytes);
               if (!dep_done) {
-                griddep_wait();
+                dep_wait();
                 dep_done = true;
               }
               tma_load_2d(sX + s * kXBytes, &tmS, &tma_full[s], (kb - G) * BK, m0);
@@ -507,7 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               // This CTA has started its last tile: a kernel launched after this one
               // with programmatic dependent launch (the next call's code conversion)
               // may take the SMs that the pairs without a tile left leave idle.  Only
-              // after griddep_wait(), so that every kernel before this one has ended.
+              // after the dependency wait, so that every kernel before this one has ended
+              // (a follower's predecessor released it only after its own wait).
               asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
               released = true;
             }
@@ -748,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_inc<kRegsEpi>();
     // ------------------------------------------------------------ epilogue
-    griddep_wait();  // the outputs (and the fused epilogues' inputs) belong to earlier kernels until then
+    dep_wait();  // the outputs (and the fused epilogues' inputs) belong to earlier kernels until then
     constexpr int CW = kEpiRows;  // rows of X owned by one thread
     const int q = warp & 3;       // tensor-memory lane quarter this warp may access
     const int slice = (warp - kEpiWarp0) >> 2;
@@ -897,6 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (p.follow && threadIdx.x == 0) griddep_wait();  // a follower ends after the GEMM before it
   // neither CTA leaves (or frees the pair's tensor memory) while the other may still
   // read its shared memory, write its barriers or run MMAs into its tensor memory
   tc_fence_before();
@@ -1145,7 +1157,7 @@ static int sm_count() {
 template <int BITS, int EPI>
 static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
                         const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi,
-                        const uint16_t *apre = nullptr) {
+                        const uint16_t *apre = nullptr, bool follow = false) {
   using C = pg::Cfg<BITS>;
   const int G = w->k / 64;
   CUtensorMap tmX, tmW, tmS, tmSc, tmBi;
@@ -1220,6 +1232,7 @@ static int launch_pgemm(const ql_weight *w, const uint16_t *X, int m, int64_t ld
   p.NBB = (int)(lds / pg::BK);
   p.status = status;
   p.budget_ns = wait_budget_ns();
+  p.follow = follow ? 1 : 0;
   p.tiles_n = (w->n + 2 * pg::BN - 1) / (2 * pg::BN);
   p.tiles = p.tiles_n * ((m + pg::BM - 1) / pg::BM);
   // persistent: one CTA pair per two SMs, as a cluster of two
@@ -1339,11 +1352,11 @@ int pgemm_run_noalloc(const ql_weight *w, const uint16_t *X, int m, int64_t ldx,
 template <int BITS>
 static int launch_epi(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
                       const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi,
-                      const uint16_t *apre = nullptr) {
+                      const uint16_t *apre = nullptr, bool follow = false) {
   switch (epi ? epi->mode : kPgStore) {
-    case kPgSwiglu: return launch_pgemm<BITS, kPgSwiglu>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
-    case kPgResid: return launch_pgemm<BITS, kPgResid>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
-    default: return launch_pgemm<BITS, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
+    case kPgSwiglu: return launch_pgemm<BITS, kPgSwiglu>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre, follow);
+    case kPgResid: return launch_pgemm<BITS, kPgResid>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre, follow);
+    default: return launch_pgemm<BITS, kPgStore>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre, follow);
   }
 }
 
@@ -1402,12 +1415,12 @@ static int pgemm_convert(const ql_weight *w, int m, int64_t lds, cudaStream_t st
 // apre is set).
 static int pgemm_launch(const ql_weight *w, const uint16_t *X, int m, int64_t ldx, float *Y, int64_t ldy,
                         const uint16_t *S, int64_t lds, cudaStream_t st, int *status, const PgEpilogue *epi,
-                        const uint16_t *apre) {
+                        const uint16_t *apre, bool follow) {
   if (apre != nullptr) return launch_epi<0>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, apre);
   switch (w->bits) {
-    case 4: return launch_epi<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
-    case 6: return launch_epi<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
-    default: return launch_epi<8>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi);
+    case 4: return launch_epi<4>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, nullptr, follow);
+    case 6: return launch_epi<6>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, nullptr, follow);
+    default: return launch_epi<8>(w, X, m, ldx, Y, ldy, S, lds, st, status, epi, nullptr, follow);
   }
 }
 
@@ -1431,7 +1444,9 @@ int pgemm_run_multi(const ql_weight *const *w, int nw, const uint16_t *X, int m,
   for (int i = 0; i < nw; ++i) {
     if (i > 0)
       if (int e = pgemm_convert(w[i], m, lds, st, &apre)) return e;
-    if (int e = pgemm_launch(w[i], X, m, ldx, Y[i], ldy[i], S, lds, st, status, epi, apre)) return e;
+    // below the pre-conversion size the later GEMMs run beside the ones before them
+    const bool follow = i > 0 && m < kPreRows;
+    if (int e = pgemm_launch(w[i], X, m, ldx, Y[i], ldy[i], S, lds, st, status, epi, apre, follow)) return e;
   }
   return QL_OK;
 }
